@@ -1,0 +1,440 @@
+// api.cu -- host side of the C ABI declared in include/ccg.h: argument
+// validation (fail-closed), workspace layout, TMA tensor maps and the
+// launch sequence of each entry point.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace ccg {
+
+
+cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp, int bm,
+                        int bn, int cap_q, int cap_kv, int want, PlanHeader* hdr,
+                        WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items,
+                        int32_t* status, cudaStream_t stream);
+cudaError_t launch_chunk_table(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp,
+                               int32_t* table, int32_t* status, cudaStream_t stream);
+cudaError_t launch_bwd_dot(const void* o, const void* dout, int64_t rows, int D, float* delta,
+                           const int32_t* status, int num_sms, cudaStream_t stream);
+cudaError_t launch_thd_permute(bool pack, const void* src, void* dst, const int32_t* cu_pad, int B,
+                               int64_t T, int H, int D, int cp, int32_t* status, int num_sms,
+                               cudaStream_t stream);
+cudaError_t launch_attn_fwd_step(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
+                                 const int32_t* cu_pad, void* o, float* lse, int32_t* status,
+                                 int step, int cp, int hq, int hkv, int head_groups, int64_t T,
+                                 int D, float scale, int grid_x, cudaStream_t stream);
+cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items,
+                            const WorkItem* kv_items, const PlanHeader* hdr, const int32_t* cu,
+                            const int32_t* cu_pad, const float* lse, const float* delta, void* dq,
+                            void* dk, void* dv, int32_t* status, int cp, int hq, int hkv,
+                            int head_groups, int64_t T, int D, float scale, int grid_q,
+                            int grid_kv, int* launches, cudaStream_t stream);
+int bwd_kv_tile_rows(int D);
+int bwd_q_tile_rows(int D);
+int bwd_map_rows(int which, int D);
+
+cudaError_t launch_lse_merge(const MergeArgs& a, int num_sms, cudaStream_t stream);
+
+}  // namespace ccg
+
+namespace {
+
+using namespace ccg;
+
+thread_local int32_t g_last_launches = 0;
+
+constexpr int kQTile = 128;          // query-tile rows of the forward and dQ pass
+constexpr int kMinKvTile = 64;       // smallest KV-tile rows of any pass (plan capacity)
+
+int num_sms_cached() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ccg_status check_desc(const ccg_attn_desc* d) {
+  if (d == nullptr) return CCG_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->hq < 1 || d->hkv < 1 || d->total_tokens < 0 || d->reserved != 0)
+    return CCG_ERR_INVALID_ARG;
+  if (d->causal != 1) return CCG_ERR_UNSUPPORTED;
+  if (d->head_dim != 128 && d->head_dim != 256) return CCG_ERR_UNSUPPORTED;
+  if (d->hq % d->hkv != 0) return CCG_ERR_UNSUPPORTED;
+  if (d->cp < 1 || d->cp > kMaxCP) return CCG_ERR_UNSUPPORTED;
+  if (d->head_groups != 1 && d->head_groups != d->cp) return CCG_ERR_UNSUPPORTED;
+  if (d->hq % d->head_groups != 0 || d->hkv % d->head_groups != 0) return CCG_ERR_UNSUPPORTED;
+  if (d->total_tokens % (2 * d->cp) != 0) return CCG_ERR_UNSUPPORTED;
+  // 32-bit coordinates inside the kernels and TMA maps
+  if (d->total_tokens * d->head_groups >= (int64_t(1) << 31)) return CCG_ERR_UNSUPPORTED;
+  if (d->batch > (1 << 20)) return CCG_ERR_UNSUPPORTED;
+  return CCG_OK;
+}
+
+float softmax_scale(const ccg_attn_desc* d) {
+  return d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt(static_cast<float>(d->head_dim));
+}
+
+struct Layout {
+  size_t hdr, fwd_items, dq_items, kv_items, o_parts, lse_parts, delta, total;
+  int cap_q, cap_kv;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+Layout workspace_layout(const ccg_attn_desc* d, int is_bwd) {
+  Layout L{};
+  const int64_t C = 2 * d->cp;
+  L.cap_q = static_cast<int>(d->total_tokens / kQTile + d->batch * C + 1);
+  L.cap_kv = static_cast<int>(d->total_tokens / kMinKvTile + d->batch * C + 1);
+  size_t off = 0;
+  L.hdr = off;
+  off += kPlanHeaderBytes;
+  L.fwd_items = off;
+  off = align_up(off + (is_bwd ? 0 : size_t(d->cp) * L.cap_q * sizeof(WorkItem)), 256);
+  L.dq_items = off;
+  off = align_up(off + (is_bwd ? size_t(L.cap_q) * sizeof(WorkItem) : 0), 256);
+  L.kv_items = off;
+  off = align_up(off + (is_bwd ? size_t(L.cap_kv) * sizeof(WorkItem) : 0), 256);
+  const size_t rows = size_t(d->total_tokens) * d->hq;
+  L.o_parts = off;
+  off = align_up(off + (is_bwd ? 0 : size_t(d->cp) * rows * d->head_dim * 2), 256);
+  L.lse_parts = off;
+  off = align_up(off + (is_bwd ? 0 : size_t(d->cp) * rows * 4), 256);
+  L.delta = off;
+  off = align_up(off + (is_bwd ? rows * 4 : 0), 256);
+  L.total = off;
+  return L;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so that
+// the library has no link-time dependency on the driver library.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a head-grouped THD tensor: dims (D, H/G_h, G_h*T), 128-byte
+// swizzled boxes of 64 columns x 1 head x `box_rows` rows.
+bool make_thd_map(CUtensorMap* m, const void* base, int D, int hpg, int64_t rows, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hpg),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(hpg) * D * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+#define CCG_CUDA(expr)                       \
+  do {                                       \
+    if ((expr) != cudaSuccess) return CCG_ERR_CUDA; \
+    ++launches;                              \
+  } while (0)
+
+ccg_status fwd_prepare(const ccg_attn_desc* d, const void* q, const void* k, const void* v,
+                       const int32_t* cu, const int32_t* cu_pad, void* workspace, size_t ws_bytes,
+                       int32_t* status, Layout* L) {
+  ccg_status st = check_desc(d);
+  if (st != CCG_OK) return st;
+  if (!q || !k || !v || !cu || !cu_pad || !status) return CCG_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return CCG_ERR_ALIGNMENT;
+  *L = workspace_layout(d, 0);
+  if (workspace == nullptr || ws_bytes < L->total) return CCG_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CCG_ERR_ALIGNMENT;
+  return CCG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ccg_workspace_size(const ccg_attn_desc* desc, int is_bwd) {
+  if (check_desc(desc) != CCG_OK) return 0;
+  return workspace_layout(desc, is_bwd ? 1 : 0).total;
+}
+
+const char* ccg_status_str(ccg_status s) {
+  switch (s) {
+    case CCG_OK: return "ok";
+    case CCG_ERR_INVALID_ARG: return "invalid argument";
+    case CCG_ERR_UNSUPPORTED: return "unsupported problem (shape, head dim, CP size or layout)";
+    case CCG_ERR_ALIGNMENT: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case CCG_ERR_WORKSPACE: return "workspace missing or too small";
+    case CCG_ERR_SEQLENS: return "sequence lengths / padded offsets break the promise";
+    case CCG_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case CCG_ERR_CUDA: return "CUDA runtime or driver call failed";
+  }
+  return "unknown status";
+}
+
+int32_t ccg_last_launch_count(void) { return g_last_launches; }
+
+ccg_status ccg_get_status(const int32_t* d_status, ccg_stream_t stream) {
+  if (d_status == nullptr) return CCG_ERR_INVALID_ARG;
+  int32_t h = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&h, d_status, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return CCG_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CCG_ERR_CUDA;
+  return static_cast<ccg_status>(h);
+}
+
+ccg_status ccg_cp_split(const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded, int32_t batch,
+                        int64_t total_tokens, int32_t cp, int32_t* chunk_table, int32_t* d_status,
+                        ccg_stream_t stream) {
+  int launches = 0;
+  g_last_launches = 0;
+  if (!cu_seqlens || !cu_seqlens_padded || !chunk_table || !d_status) return CCG_ERR_INVALID_ARG;
+  if (batch < 1 || total_tokens < 0) return CCG_ERR_INVALID_ARG;
+  if (cp < 1 || cp > kMaxCP) return CCG_ERR_UNSUPPORTED;
+  CCG_CUDA(launch_chunk_table(cu_seqlens, cu_seqlens_padded, batch, total_tokens, cp, chunk_table,
+                              d_status, reinterpret_cast<cudaStream_t>(stream)));
+  g_last_launches = launches;
+  return CCG_OK;
+}
+
+ccg_status ccg_cp_lse_merge(int32_t nparts, const void* const* o_parts, const float* const* lse_parts,
+                            int64_t rows, int32_t head_dim, void* o, float* lse, ccg_stream_t stream) {
+  int launches = 0;
+  g_last_launches = 0;
+  if (nparts < 1 || nparts > kMaxCP || rows < 0 || !o_parts || !lse_parts || !o || !lse)
+    return CCG_ERR_INVALID_ARG;
+  if (head_dim != 128 && head_dim != 256) return CCG_ERR_UNSUPPORTED;
+  MergeArgs a{};
+  for (int s = 0; s < nparts; ++s) {
+    if (!o_parts[s] || !lse_parts[s]) return CCG_ERR_INVALID_ARG;
+    if (!aligned16(o_parts[s])) return CCG_ERR_ALIGNMENT;
+    a.o_parts[s] = o_parts[s];
+    a.lse_parts[s] = lse_parts[s];
+  }
+  if (!aligned16(o)) return CCG_ERR_ALIGNMENT;
+  if (rows == 0) return CCG_OK;
+  a.nparts = nparts;
+  a.o = o;
+  a.lse = lse;
+  a.rows = rows;
+  a.D = head_dim;
+  a.status = nullptr;
+  CCG_CUDA(launch_lse_merge(a, num_sms_cached(), reinterpret_cast<cudaStream_t>(stream)));
+  g_last_launches = launches;
+  return CCG_OK;
+}
+
+ccg_status ccg_bwd_dot(const void* o, const void* dout, int64_t rows, int32_t head_dim, float* delta,
+                       ccg_stream_t stream) {
+  int launches = 0;
+  g_last_launches = 0;
+  if (!o || !dout || !delta || rows < 0) return CCG_ERR_INVALID_ARG;
+  if (head_dim != 128 && head_dim != 256) return CCG_ERR_UNSUPPORTED;
+  if (!aligned16(o) || !aligned16(dout)) return CCG_ERR_ALIGNMENT;
+  if (rows == 0) return CCG_OK;
+  CCG_CUDA(launch_bwd_dot(o, dout, rows, head_dim, delta, nullptr, num_sms_cached(),
+                          reinterpret_cast<cudaStream_t>(stream)));
+  g_last_launches = launches;
+  return CCG_OK;
+}
+
+static ccg_status thd_permute(bool pack, const void* src, const int32_t* cu_pad, int32_t batch,
+                              int64_t T, int32_t heads, int32_t head_dim, int32_t cp, void* dst,
+                              int32_t* d_status, ccg_stream_t stream) {
+  int launches = 0;
+  g_last_launches = 0;
+  if (!src || !dst || !cu_pad || !d_status || batch < 1 || T < 0 || heads < 1 || head_dim < 1)
+    return CCG_ERR_INVALID_ARG;
+  if (cp < 1 || cp > kMaxCP || heads % cp != 0 || T % (2 * cp) != 0) return CCG_ERR_UNSUPPORTED;
+  if ((static_cast<int64_t>(heads / cp) * head_dim) % 8 != 0) return CCG_ERR_UNSUPPORTED;
+  if (!aligned16(src) || !aligned16(dst)) return CCG_ERR_ALIGNMENT;
+  if (T == 0) return CCG_OK;
+  CCG_CUDA(launch_thd_permute(pack, src, dst, cu_pad, batch, T, heads, head_dim, cp, d_status,
+                              num_sms_cached(), reinterpret_cast<cudaStream_t>(stream)));
+  g_last_launches = launches;
+  return CCG_OK;
+}
+
+ccg_status ccg_thd_pack(const void* x_rank_major, const int32_t* cu_seqlens_padded, int32_t batch,
+                        int64_t total_tokens, int32_t heads, int32_t head_dim, int32_t cp,
+                        void* out_head_split, int32_t* d_status, ccg_stream_t stream) {
+  return thd_permute(true, x_rank_major, cu_seqlens_padded, batch, total_tokens, heads, head_dim, cp,
+                     out_head_split, d_status, stream);
+}
+
+ccg_status ccg_thd_unpack(const void* in_head_split, const int32_t* cu_seqlens_padded, int32_t batch,
+                          int64_t total_tokens, int32_t heads, int32_t head_dim, int32_t cp,
+                          void* x_rank_major, int32_t* d_status, ccg_stream_t stream) {
+  return thd_permute(false, in_head_split, cu_seqlens_padded, batch, total_tokens, heads, head_dim, cp,
+                     x_rank_major, d_status, stream);
+}
+
+static ccg_status fwd_steps(const ccg_attn_desc* d, int first, int last, const void* q, const void* k,
+                            const void* v, const int32_t* cu, const int32_t* cu_pad, void* o_part,
+                            size_t o_stride, float* lse_part, size_t lse_stride, void* workspace,
+                            const Layout& L, int32_t* status, cudaStream_t s, int* launches_out) {
+  int launches = *launches_out;
+  auto* base = static_cast<uint8_t*>(workspace);
+  auto* hdr = reinterpret_cast<PlanHeader*>(base + L.hdr);
+  auto* items = reinterpret_cast<WorkItem*>(base + L.fwd_items);
+  CCG_CUDA(launch_plan(cu, cu_pad, d->batch, d->total_tokens, d->cp, kQTile, kMinKvTile, L.cap_q,
+                       L.cap_kv, 1, hdr, items, nullptr, nullptr, status, s));
+  const int hg = d->head_groups;
+  const int64_t rows = d->total_tokens * hg;
+  const int bn = d->head_dim == 128 ? 128 : 64;
+  CUtensorMap tq, tk, tv;
+  if (!make_thd_map(&tq, q, d->head_dim, d->hq / hg, rows, kQTile) ||
+      !make_thd_map(&tk, k, d->head_dim, d->hkv / hg, rows, bn) ||
+      !make_thd_map(&tv, v, d->head_dim, d->hkv / hg, rows, bn))
+    return CCG_ERR_CUDA;
+  const float scale = softmax_scale(d);
+  for (int stp = first; stp <= last; ++stp) {
+    auto* o_s = static_cast<uint8_t*>(o_part) + size_t(stp - first) * o_stride;
+    auto* l_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(lse_part) + size_t(stp - first) * lse_stride);
+    CCG_CUDA(launch_attn_fwd_step(tq, tk, tv, items + size_t(stp) * L.cap_q, hdr, cu, cu_pad, o_s, l_s,
+                                  status, stp, d->cp, d->hq, d->hkv, hg, d->total_tokens, d->head_dim,
+                                  scale, L.cap_q, s));
+  }
+  *launches_out = launches;
+  return CCG_OK;
+}
+
+ccg_status ccg_attn_fwd_step(const ccg_attn_desc* desc, int32_t step, const void* q, const void* k,
+                             const void* v, const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded,
+                             void* o_part, float* lse_part, void* workspace, size_t workspace_bytes,
+                             int32_t* d_status, ccg_stream_t stream) {
+  g_last_launches = 0;
+  Layout L;
+  ccg_status st = fwd_prepare(desc, q, k, v, cu_seqlens, cu_seqlens_padded, workspace, workspace_bytes,
+                              d_status, &L);
+  if (st != CCG_OK) return st;
+  if (step < 0 || step >= desc->cp) return CCG_ERR_INVALID_ARG;
+  if (!o_part || !lse_part) return CCG_ERR_INVALID_ARG;
+  if (!aligned16(o_part)) return CCG_ERR_ALIGNMENT;
+  if (desc->total_tokens == 0) return CCG_OK;
+  int launches = 0;
+  st = fwd_steps(desc, step, step, q, k, v, cu_seqlens, cu_seqlens_padded, o_part, 0, lse_part, 0,
+                 workspace, L, d_status, reinterpret_cast<cudaStream_t>(stream), &launches);
+  g_last_launches = launches;
+  return st;
+}
+
+ccg_status ccg_attn_fwd(const ccg_attn_desc* desc, const void* q, const void* k, const void* v,
+                        const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded, void* o, float* lse,
+                        void* workspace, size_t workspace_bytes, int32_t* d_status, ccg_stream_t stream) {
+  g_last_launches = 0;
+  Layout L;
+  ccg_status st = fwd_prepare(desc, q, k, v, cu_seqlens, cu_seqlens_padded, workspace, workspace_bytes,
+                              d_status, &L);
+  if (st != CCG_OK) return st;
+  if (!o || !lse) return CCG_ERR_INVALID_ARG;
+  if (!aligned16(o)) return CCG_ERR_ALIGNMENT;
+  if (desc->total_tokens == 0) return CCG_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto* base = static_cast<uint8_t*>(workspace);
+  const size_t rows = size_t(desc->total_tokens) * desc->hq;
+  const size_t o_stride = rows * desc->head_dim * 2, l_stride = rows * 4;
+  int launches = 0;
+  st = fwd_steps(desc, 0, desc->cp - 1, q, k, v, cu_seqlens, cu_seqlens_padded, base + L.o_parts,
+                 o_stride, reinterpret_cast<float*>(base + L.lse_parts), l_stride, workspace, L, d_status,
+                 s, &launches);
+  if (st != CCG_OK) return st;
+  MergeArgs a{};
+  for (int p = 0; p < desc->cp; ++p) {
+    a.o_parts[p] = base + L.o_parts + p * o_stride;
+    a.lse_parts[p] = reinterpret_cast<const float*>(base + L.lse_parts + p * l_stride);
+  }
+  a.nparts = desc->cp;
+  a.cu = cu_seqlens;
+  a.cu_pad = cu_seqlens_padded;
+  a.B = desc->batch;
+  a.cp = desc->cp;
+  a.hpg = desc->hq / desc->head_groups;
+  a.T = desc->total_tokens;
+  a.o = o;
+  a.lse = lse;
+  a.rows = static_cast<int64_t>(rows);
+  a.D = desc->head_dim;
+  a.status = d_status;
+  CCG_CUDA(launch_lse_merge(a, num_sms_cached(), s));
+  g_last_launches = launches;
+  return CCG_OK;
+}
+
+ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k, const void* v,
+                        const void* o, const void* dout, const float* lse, const int32_t* cu_seqlens,
+                        const int32_t* cu_seqlens_padded, void* dq, void* dk, void* dv, void* workspace,
+                        size_t workspace_bytes, int32_t* d_status, ccg_stream_t stream) {
+  g_last_launches = 0;
+  ccg_status st = check_desc(desc);
+  if (st != CCG_OK) return st;
+  if (!q || !k || !v || !o || !dout || !lse || !cu_seqlens || !cu_seqlens_padded || !dq || !dk || !dv ||
+      !d_status)
+    return CCG_ERR_INVALID_ARG;
+  for (const void* p : {q, k, v, o, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv)})
+    if (!aligned16(p)) return CCG_ERR_ALIGNMENT;
+  const Layout L = workspace_layout(desc, 1);
+  if (workspace == nullptr || workspace_bytes < L.total) return CCG_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CCG_ERR_ALIGNMENT;
+  if (desc->total_tokens == 0) return CCG_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto* base = static_cast<uint8_t*>(workspace);
+  auto* hdr = reinterpret_cast<PlanHeader*>(base + L.hdr);
+  auto* dq_items = reinterpret_cast<WorkItem*>(base + L.dq_items);
+  auto* kv_items = reinterpret_cast<WorkItem*>(base + L.kv_items);
+  auto* delta = reinterpret_cast<float*>(base + L.delta);
+  const int D = desc->head_dim;
+  const int hg = desc->head_groups;
+  const int64_t rows = desc->total_tokens * hg;
+  int launches = 0;
+  CCG_CUDA(launch_plan(cu_seqlens, cu_seqlens_padded, desc->batch, desc->total_tokens, desc->cp,
+                       bwd_q_tile_rows(D), bwd_kv_tile_rows(D), L.cap_q, L.cap_kv, 2, hdr, nullptr,
+                       dq_items, kv_items, d_status, s));
+  CCG_CUDA(launch_bwd_dot(o, dout, desc->total_tokens * desc->hq, D, delta, d_status, num_sms_cached(), s));
+  // maps: 0 q, 1 k, 2 v, 3 dO -- row boxes per pass
+  CUtensorMap maps[8];
+  const int hq_g = desc->hq / hg, hkv_g = desc->hkv / hg;
+  const void* bases[4] = {q, k, v, dout};
+  const int hpgs[4] = {hq_g, hkv_g, hkv_g, hq_g};
+  for (int i = 0; i < 4; ++i) {
+    if (!make_thd_map(&maps[i], bases[i], D, hpgs[i], rows, bwd_map_rows(i, D)) ||
+        !make_thd_map(&maps[4 + i], bases[i], D, hpgs[i], rows, bwd_map_rows(4 + i, D)))
+      return CCG_ERR_CUDA;
+  }
+  int kl = 0;
+  if (launch_attn_bwd(maps, dq_items, kv_items, hdr, cu_seqlens, cu_seqlens_padded, lse, delta, dq, dk, dv,
+                      d_status, desc->cp, desc->hq, desc->hkv, hg, desc->total_tokens, D,
+                      softmax_scale(desc), L.cap_q, L.cap_kv, &kl, s) != cudaSuccess)
+    return CCG_ERR_CUDA;
+  launches += kl;
+  g_last_launches = launches;
+  return CCG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,209 @@
+// elementwise.cu -- the HBM-bound steps of the path:
+//   a4  K-way LSE merge of the per-step partial outputs,
+//   a5  Delta = rowsum(O * dO) for the backward,
+//   a2/a8  A2A head-split pack / unpack copies.
+// All use 16-byte vector loads/stores and 64-bit row arithmetic.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace ccg {
+
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+template <int TPR>
+__global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a) {
+  if (a.status != nullptr && status_bad(a.status)) return;
+  const int sub = threadIdx.x % TPR;
+  const int64_t rows_per_block = 256 / TPR;
+  const int64_t row0 = blockIdx.x * rows_per_block + threadIdx.x / TPR;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * rows_per_block;
+  for (int64_t r = row0; r < a.rows; r += stride) {
+    int K = a.nparts;
+    bool valid = true;
+    if (a.cu_pad != nullptr) {
+      const int64_t t = (r / a.hpg) % a.T;
+      const int b = find_sequence(a.cu_pad, a.B, t);
+      const int start = __ldg(a.cu_pad + b);
+      const int pos = static_cast<int>(t - start);
+      const int L = (__ldg(a.cu_pad + b + 1) - start) / (2 * a.cp);
+      const int S = __ldg(a.cu + b + 1) - __ldg(a.cu + b);
+      valid = pos < S;
+      const int c = L > 0 ? pos / L : 0;
+      K = c >= a.cp ? a.cp : c + 1;
+    }
+    float l[kMaxCP];
+    float m = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kMaxCP; ++s) {
+      l[s] = (s < K) ? __ldg(a.lse_parts[s] + r) : -INFINITY;
+      m = fmaxf(m, l[s]);
+    }
+    const int64_t off = r * a.D + sub * 8;
+    uint4 outv;
+    float lse_out;
+    if (!valid || m == -INFINITY) {
+      outv = make_uint4(0, 0, 0, 0);
+      lse_out = -INFINITY;
+    } else {
+      float sigma = 0.f;
+#pragma unroll
+      for (int s = 0; s < kMaxCP; ++s)
+        if (s < K) sigma += ex2_approx((l[s] - m) * kLog2e);
+      lse_out = m + __logf(sigma);
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+      for (int s = 0; s < kMaxCP; ++s) {
+        if (s < K && l[s] != -INFINITY) {
+          const float w = ex2_approx((l[s] - lse_out) * kLog2e);
+          const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o_parts[s]) + off));
+          float f[8];
+          bf16x8_to_f32(u, f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+        }
+      }
+      outv.x = pack_bf16x2(acc[0], acc[1]);
+      outv.y = pack_bf16x2(acc[2], acc[3]);
+      outv.z = pack_bf16x2(acc[4], acc[5]);
+      outv.w = pack_bf16x2(acc[6], acc[7]);
+    }
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + off) = outv;
+    if (sub == 0) a.lse[r] = lse_out;
+  }
+}
+
+template <int TPR>
+__global__ void __launch_bounds__(256)
+bwd_dot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+               int64_t rows, int D, float* __restrict__ delta, const int32_t* status) {
+  if (status != nullptr && status_bad(status)) return;
+  const int sub = threadIdx.x % TPR;
+  const int64_t rows_per_block = 256 / TPR;
+  const int64_t row0 = blockIdx.x * rows_per_block + threadIdx.x / TPR;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * rows_per_block;
+  for (int64_t r = row0; r < rows; r += stride) {
+    const int64_t off = r * D + sub * 8;
+    float a[8], b[8];
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(o + off)), a);
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(dout + off)), b);
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
+#pragma unroll
+    for (int w = TPR / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w, TPR);
+    if (sub == 0) delta[r] = acc;
+  }
+}
+
+// Rank-major row of sequence-order physical row t (load-balanced split).
+__device__ __forceinline__ int64_t rank_major_row(const int32_t* cu_pad, int B, int64_t T, int cp,
+                                                  int64_t t, bool* ok) {
+  const int C = 2 * cp;
+  const int b = find_sequence(cu_pad, B, t);
+  const int start = __ldg(cu_pad + b);
+  const int P = __ldg(cu_pad + b + 1) - start;
+  if (P % C != 0 || P <= 0) {
+    *ok = false;
+    return 0;
+  }
+  const int L = P / C;
+  const int pos = static_cast<int>(t - start);
+  const int c = pos / L, i = pos % L;
+  const int r = chunk_owner(c, cp);
+  *ok = true;
+  return static_cast<int64_t>(r) * (T / cp) + start / cp + (c == r ? 0 : L) + i;
+}
+
+// One warp per (head group g, sequence row t): copies hpg*D contiguous
+// 16-bit elements between the rank-major row and the head-split row.
+template <bool kPack>
+__global__ void __launch_bounds__(256)
+thd_permute_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                   const int32_t* __restrict__ cu_pad, int B, int64_t T, int H, int D, int cp,
+                   int32_t* status) {
+  if (status_bad(status)) return;
+  const int lane = threadIdx.x & 31;
+  const int hpg = H / cp;
+  const int64_t w16 = static_cast<int64_t>(hpg) * D / 8;   // uint4 per head-split row
+  const int64_t row_w16 = static_cast<int64_t>(H) * D / 8;  // uint4 per rank-major row
+  const int64_t nrows = static_cast<int64_t>(cp) * T;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < nrows; w += warps) {
+    const int g = static_cast<int>(w / T);
+    const int64_t t = w % T;
+    bool ok;
+    const int64_t pr = rank_major_row(cu_pad, B, T, cp, t, &ok);
+    if (!ok) {
+      if (lane == 0) raise_status(status, CCG_ERR_SEQLENS);
+      return;
+    }
+    const uint4* s;
+    uint4* d;
+    if (kPack) {
+      s = src + pr * row_w16 + static_cast<int64_t>(g) * w16;
+      d = dst + w * w16;
+    } else {
+      s = src + w * w16;
+      d = dst + pr * row_w16 + static_cast<int64_t>(g) * w16;
+    }
+    for (int64_t u = lane; u < w16; u += 32) d[u] = __ldg(s + u);
+  }
+}
+
+int grid_for(int64_t units, int per_block, int max_blocks) {
+  int64_t g = (units + per_block - 1) / per_block;
+  if (g > max_blocks) g = max_blocks;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+
+cudaError_t launch_lse_merge(const MergeArgs& a, int num_sms, cudaStream_t stream) {
+  const int tpr = a.D / 8;
+  const int grid = grid_for(a.rows, 256 / tpr, num_sms * 16);
+  if (tpr == 16) lse_merge_kernel<16><<<grid, 256, 0, stream>>>(a);
+  else if (tpr == 32) lse_merge_kernel<32><<<grid, 256, 0, stream>>>(a);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dot(const void* o, const void* dout, int64_t rows, int D, float* delta,
+                           const int32_t* status, int num_sms, cudaStream_t stream) {
+  const int tpr = D / 8;
+  const int grid = grid_for(rows, 256 / tpr, num_sms * 16);
+  auto* po = static_cast<const __nv_bfloat16*>(o);
+  auto* pd = static_cast<const __nv_bfloat16*>(dout);
+  if (tpr == 16) bwd_dot_kernel<16><<<grid, 256, 0, stream>>>(po, pd, rows, D, delta, status);
+  else if (tpr == 32) bwd_dot_kernel<32><<<grid, 256, 0, stream>>>(po, pd, rows, D, delta, status);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_thd_permute(bool pack, const void* src, void* dst, const int32_t* cu_pad, int B,
+                               int64_t T, int H, int D, int cp, int32_t* status, int num_sms,
+                               cudaStream_t stream) {
+  const int64_t nrows = static_cast<int64_t>(cp) * T;
+  const int grid = grid_for(nrows, 8, num_sms * 16);
+  auto* s = static_cast<const uint4*>(src);
+  auto* d = static_cast<uint4*>(dst);
+  if (pack) thd_permute_kernel<true><<<grid, 256, 0, stream>>>(s, d, cu_pad, B, T, H, D, cp, status);
+  else thd_permute_kernel<false><<<grid, 256, 0, stream>>>(s, d, cu_pad, B, T, H, D, cp, status);
+  return cudaGetLastError();
+}
+
+}  // namespace ccg

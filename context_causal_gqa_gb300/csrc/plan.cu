@@ -1,0 +1,193 @@
+// plan.cu -- the CP split (a1): validates the sequence promise on device
+// and writes the work plan every later kernel reads: forward items per ring
+// step, dQ-pass items and dK/dV-pass items.
+//
+// TransformerEngine PR "Optimize context parallel attention layouts and
+// gradient accumulation", Changes: the promised sequence lengths and
+// physical offsets are checked on device on each execution.  Here a broken
+// promise writes CCG_ERR_SEQLENS into the status word (no trap) and an
+// empty plan, so that every later kernel returns without writing.
+#include "common.cuh"
+
+namespace ccg {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+// Inclusive block-wide prefix sum of one int per thread; returns the
+// inclusive value and the block total through *total.
+__device__ int block_inclusive_scan(int v, int* total) {
+  __shared__ int warp_sums[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int prefix = warp > 0 ? warp_sums[warp - 1] : 0;
+  *total = warp_sums[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return x + prefix;
+}
+
+// Emits, for i = 0..n-1 in order, count(i) consecutive items written by
+// write(i, first_slot, count).  Returns the running slot after the last.
+template <class CountF, class WriteF>
+__device__ int block_emit(int n, int base, CountF count, WriteF write) {
+  int carry = base;
+  for (int start = 0; start < n; start += blockDim.x) {
+    const int i = start + threadIdx.x;
+    const int c = i < n ? count(i) : 0;
+    int total;
+    const int incl = block_inclusive_scan(c, &total);
+    if (i < n && c > 0) write(i, carry + incl - c, c);
+    carry += total;
+  }
+  return carry;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, int B, int64_t T,
+            int cp, int bm, int bn, int cap_q, int cap_kv, int want, PlanHeader* hdr,
+            WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items, int32_t* status) {
+  __shared__ int bad;
+  const int C = 2 * cp;
+  if (threadIdx.x == 0) {
+    bad = 0;
+    if (__ldg(cu) != 0 || __ldg(cu_pad) != 0 || static_cast<int64_t>(__ldg(cu_pad + B)) != T) bad = 1;
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int S = __ldg(cu + b + 1) - __ldg(cu + b);
+    const int P = __ldg(cu_pad + b + 1) - __ldg(cu_pad + b);
+    if (S < 0 || P < S || P % C != 0) atomicExch(&bad, 1);
+  }
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) {
+      raise_status(status, CCG_ERR_SEQLENS);
+      for (int s = 0; s < kMaxCP; ++s) hdr->n_fwd[s] = 0;
+      hdr->n_dq = 0;
+      hdr->n_kv = 0;
+      hdr->valid = 0;
+    }
+    return;
+  }
+  const int npairs = B * C;
+  auto seq_len = [&](int b) { return __ldg(cu + b + 1) - __ldg(cu + b); };
+  auto chunk_len = [&](int b) { return (__ldg(cu_pad + b + 1) - __ldg(cu_pad + b)) / C; };
+  // tiles of `rows` rows covering the real tokens of chunk c of sequence b
+  auto valid_tiles = [&](int b, int c, int rows) {
+    const int L = chunk_len(b);
+    const int real = min(L, max(0, seq_len(b) - c * L));
+    return (real + rows - 1) / rows;
+  };
+  auto all_tiles = [&](int b, int rows) { return (chunk_len(b) + rows - 1) / rows; };
+
+  int overflow = 0;
+  if (want & 1) {
+    for (int s = 0; s < cp; ++s) {
+      WorkItem* out = fwd_items + static_cast<int64_t>(s) * cap_q;
+      int slot = 0;
+      // heavy items first: two visible KV chunks, then one full chunk, then
+      // the diagonal chunk alone
+      for (int cls = 0; cls < 3; ++cls) {
+        auto count = [&](int i) {
+          const int b = i / C, c = i % C;
+          int vis[2];
+          const int nv = visible_kv_chunks(c, ring_source(chunk_owner(c, cp), s, cp), cp, vis);
+          int k = nv == 2 ? 0 : (nv == 1 ? (vis[0] == c ? 2 : 1) : -1);
+          return k == cls ? valid_tiles(b, c, bm) : 0;
+        };
+        auto write = [&](int i, int first, int n) {
+          const int b = i / C, c = i % C;
+          for (int t = 0; t < n && first + t < cap_q; ++t) out[first + t] = WorkItem{b, c, t, cls};
+        };
+        slot = block_emit(npairs, slot, count, write);
+      }
+      if (slot > cap_q) overflow = 1;
+      if (threadIdx.x == 0) hdr->n_fwd[s] = min(slot, cap_q);
+    }
+    if (threadIdx.x == 0)
+      for (int s = cp; s < kMaxCP; ++s) hdr->n_fwd[s] = 0;
+  }
+  if (want & 2) {
+    // dQ pass: later query chunks see more keys, so they go first
+    int slot = 0;
+    for (int c = C - 1; c >= 0; --c) {
+      auto count = [&](int b) { return all_tiles(b, bm); };
+      auto write = [&](int b, int first, int n) {
+        for (int t = 0; t < n && first + t < cap_q; ++t) dq_items[first + t] = WorkItem{b, c, t, 0};
+      };
+      slot = block_emit(B, slot, count, write);
+    }
+    if (slot > cap_q) overflow = 1;
+    if (threadIdx.x == 0) hdr->n_dq = min(slot, cap_q);
+    // dK/dV pass: earlier KV chunks are seen by more queries, so they go first
+    slot = 0;
+    for (int j = 0; j < C; ++j) {
+      auto count = [&](int b) { return all_tiles(b, bn); };
+      auto write = [&](int b, int first, int n) {
+        for (int t = 0; t < n && first + t < cap_kv; ++t) kv_items[first + t] = WorkItem{b, j, t, 0};
+      };
+      slot = block_emit(B, slot, count, write);
+    }
+    if (slot > cap_kv) overflow = 1;
+    if (threadIdx.x == 0) hdr->n_kv = min(slot, cap_kv);
+  }
+  if (threadIdx.x == 0) {
+    hdr->valid = 1;
+    if (overflow) raise_status(status, CCG_ERR_SEQLENS);
+  }
+}
+
+__global__ void chunk_table_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad,
+                                   int B, int64_t T, int cp, int32_t* table, int32_t* status) {
+  const int C = 2 * cp;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= B * C) return;
+  const int b = i / C, c = i % C;
+  const int S = __ldg(cu + b + 1) - __ldg(cu + b);
+  const int P = __ldg(cu_pad + b + 1) - __ldg(cu_pad + b);
+  bool ok = S >= 0 && P >= S && P % C == 0;
+  if (i == 0) ok = ok && __ldg(cu) == 0 && __ldg(cu_pad) == 0 && static_cast<int64_t>(__ldg(cu_pad + B)) == T;
+  if (!ok) raise_status(status, CCG_ERR_SEQLENS);
+  const int L = ok ? P / C : 0;
+  table[2 * i + 0] = __ldg(cu_pad + b) + c * L;
+  table[2 * i + 1] = L;
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp, int bm,
+                        int bn, int cap_q, int cap_kv, int want, PlanHeader* hdr,
+                        WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items,
+                        int32_t* status, cudaStream_t stream) {
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(cu, cu_pad, B, T, cp, bm, bn, cap_q, cap_kv, want,
+                                               hdr, fwd_items, dq_items, kv_items, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_table(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp,
+                               int32_t* table, int32_t* status, cudaStream_t stream) {
+  const int n = B * 2 * cp;
+  chunk_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(cu, cu_pad, B, T, cp, table, status);
+  return cudaGetLastError();
+}
+
+}  // namespace ccg

@@ -1,0 +1,200 @@
+/*
+ * ccg.h -- C ABI of libccg: context-parallel causal grouped-query attention
+ * over packed THD BF16 sequences, computed the way a context-parallel (CP)
+ * rank computes it, with every CP rank emulated as a partition of one GPU.
+ *
+ * The operation is the one described by the TransformerEngine pull request
+ * "Optimize context parallel attention layouts and gradient accumulation"
+ * (sections Description, Changes, CP8 first-gradient accumulator reuse,
+ * Independent-node complete-CP evidence): BF16 causal THD attention, GQA
+ * (Hq query heads sharing Hkv key/value heads), D = 128 or 256, each
+ * sequence cut into 2*CP load-balanced chunks (rank r holds chunks r and
+ * 2CP-1-r), per-rank partial outputs carrying log-sum-exp (LSE) stats that
+ * are merged by LSE rescaling, dK/dV accumulated in a fixed order with the
+ * first contribution used as the accumulator, and the A2A head-split
+ * pack/unpack layout copies.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - All tensor pointers are DEVICE pointers unless stated otherwise, 16-byte
+ *    aligned, contiguous.  The caller owns every buffer; the library
+ *    allocates no device memory and keeps no per-call state.
+ *  - Every call is asynchronous on the caller's `stream`; none synchronises
+ *    except ccg_get_status.
+ *  - Errors are fail-closed: an unsupported shape, dtype, head dimension, CP
+ *    size or alignment returns an error code and launches nothing.  There is
+ *    no fallback route.
+ *  - Device-detected errors (broken sequence-length promises, a bounded wait
+ *    that ran out) are written into the caller's int32 status word
+ *    `d_status` (device memory, zeroed by the caller before first use).  A
+ *    status word is sticky: kernels only ever write a non-zero code into it,
+ *    and every kernel of this library that is given a non-zero status word
+ *    returns without writing its outputs.  Read it with ccg_get_status.
+ *  - Tensor layout "THD with head groups": a tensor with H heads of width D
+ *    and `head_groups` = G_h (1 or CP) is stored as [G_h][T][H/G_h][D]; head
+ *    h of token t lives at row (h / (H/G_h)) * T + t, slot h % (H/G_h).
+ *    G_h = 1 is the plain packed THD layout [T][H][D].  G_h = CP is the A2A
+ *    head-split layout produced by ccg_thd_pack.  LSE tensors use the same
+ *    grouping with D = 1: [G_h][T][Hq/G_h] float.
+ *  - Sequences: cu_seqlens[B+1] (logical lengths S_b) and
+ *    cu_seqlens_padded[B+1] (physical offsets, padded lengths P_b), int32,
+ *    device memory.  Sequence b occupies physical rows
+ *    [cu_seqlens_padded[b], cu_seqlens_padded[b+1]); its first S_b rows are
+ *    tokens, the rest padding.  cu_seqlens_padded may equal cu_seqlens.
+ *    Every P_b must be a multiple of 2*CP (the chunks are cut on P_b) and
+ *    cu_seqlens_padded[B] must equal T.  Padding rows neither attend nor are
+ *    attended: their O, dQ, dK, dV are written as 0 and their LSE as -inf.
+ */
+#ifndef CCG_H_
+#define CCG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ccg_stream_t;   /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  CCG_OK = 0,
+  CCG_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shapes      */
+  CCG_ERR_UNSUPPORTED = 2,   /* D not in {128,256}, Hq % Hkv, CP out of range, ...     */
+  CCG_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned                       */
+  CCG_ERR_WORKSPACE = 4,     /* workspace missing or smaller than ccg_workspace_size   */
+  CCG_ERR_SEQLENS = 5,       /* device-detected: cu_seqlens / cu_seqlens_padded break
+                                the promise (not monotone, S_b > P_b, P_b % 2CP != 0,
+                                cu_seqlens_padded[B] != T)                              */
+  CCG_ERR_TIMEOUT = 6,       /* device-detected: a bounded wait inside a kernel ran out */
+  CCG_ERR_CUDA = 7           /* a CUDA runtime/driver call failed (launch, tensor map)  */
+} ccg_status;
+
+/* Problem description shared by ccg_attn_fwd / ccg_attn_bwd. */
+typedef struct {
+  int32_t batch;          /* B, number of packed sequences (>= 1)                     */
+  int32_t hq;             /* query heads                                               */
+  int32_t hkv;            /* key/value heads; hq % hkv == 0; q head h uses kv head
+                             h / (hq/hkv) (contiguous GQA groups)                       */
+  int32_t head_dim;       /* D: 128 or 256                                             */
+  int32_t causal;         /* must be 1 (the path is causal attention)                  */
+  int32_t cp;             /* emulated context-parallel ranks, 1..16                    */
+  int32_t head_groups;    /* 1 (plain THD) or cp (head-split); hq, hkv divisible by it */
+  int32_t reserved;       /* must be 0                                                 */
+  int64_t total_tokens;   /* T = cu_seqlens_padded[B]                                  */
+  float softmax_scale;    /* <= 0 selects 1/sqrt(D)                                    */
+} ccg_attn_desc;
+
+/* Bytes of device workspace ccg_attn_fwd (is_bwd = 0) or ccg_attn_bwd
+ * (is_bwd = 1) needs for `desc`; 0 if `desc` is invalid.  The forward
+ * workspace holds the work plan plus CP per-step partial outputs
+ * (CP x T x Hq x D BF16) and their LSE (CP x T x Hq float); the backward
+ * workspace holds the work plan and Delta (T x Hq float). */
+size_t ccg_workspace_size(const ccg_attn_desc* desc, int is_bwd);
+
+/* Forward: O = softmax(scale Q K^T + causal mask) V and its row LSE, computed
+ * as CP emulated ranks do it (TransformerEngine PR, Independent-node
+ * complete-CP evidence; ring exchange as in Related optimization work, P2P):
+ * for ring step s = 0..CP-1 every rank r attends its two query chunks over
+ * the KV chunks of rank (r - s) mod CP, producing a partial (O_s, LSE_s);
+ * the partials are then merged by LSE rescaling in ascending step order.
+ *   q: [G_h][T][Hq/G_h][D] bf16;  k, v: [G_h][T][Hkv/G_h][D] bf16
+ *   o: same layout as q (bf16, written);  lse: [G_h][T][Hq/G_h] float (written,
+ *      natural log)
+ *   workspace: >= ccg_workspace_size(desc, 0) bytes, 256-byte aligned.
+ * Every element of o and lse is written (padding rows 0 / -inf). */
+ccg_status ccg_attn_fwd(const ccg_attn_desc* desc, const void* q, const void* k, const void* v,
+                        const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded,
+                        void* o, float* lse, void* workspace, size_t workspace_bytes,
+                        int32_t* d_status, ccg_stream_t stream);
+
+/* One ring step of the forward, exposed for inspection: the partial
+ * (O_s, LSE_s) of step `step` for all emulated ranks.  Rows that have no
+ * partial at this step (an early chunk whose source rank only holds later
+ * KV, and padding rows) are NOT written.  Same layouts and workspace as
+ * ccg_attn_fwd (the partial buffers inside the workspace are not used). */
+ccg_status ccg_attn_fwd_step(const ccg_attn_desc* desc, int32_t step, const void* q,
+                             const void* k, const void* v, const int32_t* cu_seqlens,
+                             const int32_t* cu_seqlens_padded, void* o_part, float* lse_part,
+                             void* workspace, size_t workspace_bytes, int32_t* d_status,
+                             ccg_stream_t stream);
+
+/* Backward (TransformerEngine PR, Changes and CP8 first-gradient accumulator
+ * reuse): dQ, dK, dV of the forward above given dO, the merged O and LSE.
+ * Delta = rowsum(O * dO) is computed first; dQ of each query chunk sums its
+ * KV contributions in ring-step order; dK/dV of each KV chunk sum the
+ * contributions of ranks src, src+1, ... (ring steps 0..CP-1), query chunk r
+ * before 2CP-1-r, query tile ascending, q head ascending, the FIRST
+ * contribution initialising the accumulator (no zero fill).  The order is
+ * fixed, so results are bitwise repeatable run to run.
+ *   o, dout: layout of q (bf16);  lse: as written by ccg_attn_fwd
+ *   dq: layout of q; dk, dv: layout of k (bf16, all written, padding rows 0)
+ *   workspace: >= ccg_workspace_size(desc, 1) bytes, 256-byte aligned. */
+ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k, const void* v,
+                        const void* o, const void* dout, const float* lse,
+                        const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded,
+                        void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                        int32_t* d_status, ccg_stream_t stream);
+
+/* Load-balanced CP split (TransformerEngine PR, Independent-node complete-CP
+ * evidence: CP8 over packed THD; the 2*CP chunk "reorder"): writes
+ * chunk_table[b][c] = {first physical row, length} for c = 0..2CP-1, with
+ * length P_b / (2CP); chunk c is held by rank c < CP ? c : 2CP-1-c.
+ * Validates the sequence promise on device (status word as above).
+ *   cu_seqlens, cu_seqlens_padded: device int32 [batch+1]
+ *   chunk_table: device int32 [batch][2cp][2], written. */
+ccg_status ccg_cp_split(const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded,
+                        int32_t batch, int64_t total_tokens, int32_t cp, int32_t* chunk_table,
+                        int32_t* d_status, ccg_stream_t stream);
+
+/* K-way LSE merge of partial attention outputs (the CP "LSE correction";
+ * TransformerEngine PR, Description: partial outputs with their Stats):
+ *   M = max_s LSE_s, LSE = M + ln sum_s exp(LSE_s - M),
+ *   O = sum_s exp(LSE_s - LSE) O_s, summed in the given order s = 0..K-1.
+ * A partial whose LSE is -inf is absent for that row (its O is not read).
+ * Rows whose partials are all absent get O = 0, LSE = -inf.
+ *   o_parts, lse_parts: HOST arrays of `nparts` (1..16) DEVICE pointers to
+ *      bf16 [rows][head_dim] and float [rows]
+ *   o: bf16 [rows][head_dim], lse: float [rows], written. */
+ccg_status ccg_cp_lse_merge(int32_t nparts, const void* const* o_parts,
+                            const float* const* lse_parts, int64_t rows, int32_t head_dim,
+                            void* o, float* lse, ccg_stream_t stream);
+
+/* Delta[row] = sum_d O[row][d] * dO[row][d] in float (TransformerEngine PR,
+ * CP8 AllGather composition: the "pitched O/dO dot" helper of the backward).
+ *   o, dout: bf16 [rows][head_dim];  delta: float [rows], written. */
+ccg_status ccg_bwd_dot(const void* o, const void* dout, int64_t rows, int32_t head_dim,
+                       float* delta, ccg_stream_t stream);
+
+/* A2A head-split pack (TransformerEngine PR, Changes: "vectorized A2A layout
+ * copies"): from the rank-major local layout (for rank r, for sequence b:
+ * chunk r then chunk 2CP-1-r; [T][H][D]) to the head-split layout
+ * [CP][T][H/CP][D] in sequence order:
+ *   out[g][t][h'][:] = x[pi(t)][g*H/CP + h'][:],  pi = sequence row -> rank-major row.
+ * Bit-exact copy of 16-bit elements.  H % cp == 0; P_b % 2cp == 0. */
+ccg_status ccg_thd_pack(const void* x_rank_major, const int32_t* cu_seqlens_padded,
+                        int32_t batch, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                        int32_t cp, void* out_head_split, int32_t* d_status, ccg_stream_t stream);
+
+/* Inverse of ccg_thd_pack: head-split [CP][T][H/CP][D] -> rank-major [T][H][D]. */
+ccg_status ccg_thd_unpack(const void* in_head_split, const int32_t* cu_seqlens_padded,
+                          int32_t batch, int64_t total_tokens, int32_t heads, int32_t head_dim,
+                          int32_t cp, void* x_rank_major, int32_t* d_status, ccg_stream_t stream);
+
+/* Synchronises `stream`, reads the device status word and returns it
+ * (CCG_OK, CCG_ERR_SEQLENS or CCG_ERR_TIMEOUT), or CCG_ERR_CUDA if the
+ * synchronisation itself failed. */
+ccg_status ccg_get_status(const int32_t* d_status, ccg_stream_t stream);
+
+/* Static description of a status code. */
+const char* ccg_status_str(ccg_status s);
+
+/* Number of kernel launches the most recent successful ccg_* call on this
+ * host thread issued (for launch accounting by callers). */
+int32_t ccg_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCG_H_ */
