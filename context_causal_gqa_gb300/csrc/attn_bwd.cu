@@ -1,14 +1,807 @@
-// attn_bwd.cu -- placeholder until the backward kernels land.
-#include <cuda.h>
+// attn_bwd.cu -- a6 (dQ pass) and a7 (dK/dV pass) of the CP-emulated causal
+// GQA backward on the 5th-generation tensor cores (sm_103a).
+//
+// TransformerEngine PR "Optimize context parallel attention layouts and
+// gradient accumulation", Changes and CP8 first-gradient accumulator reuse:
+// dK/dV contributions are accumulated in a fixed order and the first
+// contribution is used as the accumulator (no zero-filled buffer, no first
+// add into zero).  Here every output tile is owned by exactly one CTA that
+// walks its contributions in the canonical ring order, and the first MMA of
+// every accumulator runs with accumulation disabled; there are no atomics,
+// so results are bitwise repeatable.
+//
+// dQ pass: one CTA per (128-row query tile, q head).  Q and dO tiles stay in
+//   SMEM; K/V tiles stream through single-tile slots.  Per KV tile:
+//   S = Q K^T, dP = dO V^T (TMEM), then dS = P (dP - Delta) * scale in
+//   registers (P = exp(S*scale - LSE) from the merged LSE), written back to
+//   TMEM as BF16, and dQ += dS K (TMEM accumulator).
+// dK/dV pass: one CTA per (128-row KV tile, kv head).  K and V stay in SMEM;
+//   Q_i / dO_i tiles of every contributing (query chunk, tile, q head)
+//   stream through the slots.  Per contribution: S^T = K Q^T, dP^T = V dO^T,
+//   P^T and dS^T in registers -> TMEM (BF16), dV += P^T dO, dK += dS^T Q.
+//   At D = 256 the two 256-column FP32 accumulators alone fill TMEM, so the
+//   pass runs as two kernels: one accumulating dV, one accumulating dK.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
+#include "ptx.cuh"
+
 namespace ccg {
-int bwd_kv_tile_rows(int D) { return D == 128 ? 128 : 64; }
-int bwd_q_tile_rows(int) { return 128; }
-int bwd_map_rows(int which, int D) { return which < 4 ? 128 : bwd_kv_tile_rows(D); }
-cudaError_t launch_attn_bwd(const CUtensorMap*, const WorkItem*, const WorkItem*, const PlanHeader*,
-                            const int32_t*, const int32_t*, const float*, const float*, void*, void*,
-                            void*, int32_t*, int, int, int, int, int64_t, int, float, int, int, int*,
-                            cudaStream_t) {
-  return cudaErrorNotSupported;
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum class KvMode { kBoth = 0, kDvOnly = 1, kDkOnly = 2 };
+
+struct BwdParams {
+  const WorkItem* items;
+  const PlanHeader* hdr;
+  const int32_t* cu;
+  const int32_t* cu_pad;
+  const float* lse;       // merged LSE, natural log, head-grouped [G_h][T][Hq/G_h]
+  const float* delta;     // rowsum(O * dO), same layout as lse
+  __nv_bfloat16* out0;    // dQ (dQ pass) or dV (dK/dV pass)
+  __nv_bfloat16* out1;    // dK (dK/dV pass)
+  int32_t* status;
+  int cp, hq, hkv, hpg_q, hpg_kv;
+  int64_t T;
+  float scale, scale_log2;
+};
+
+// ---------------------------------------------------------------------------
+// tile configurations
+template <int D>
+struct DqCfg {
+  static constexpr int BM = 128;                 // query rows (MMA M)
+  static constexpr int BN = D == 128 ? 128 : 64; // key rows per tile (MMA N of S, K of dQ)
+  static constexpr int NSLOT = D == 128 ? 4 : 3; // single-tile slots for K_j / V_j
+  static constexpr int RES_BYTES = BM * D * 2;   // Q or dO
+  static constexpr int SLOT_BYTES = BN * D * 2;
+  static constexpr int SMEM_RES = 0;
+  static constexpr int SMEM_SLOT = 2 * RES_BYTES;
+  static constexpr int SMEM_BAR = SMEM_SLOT + NSLOT * SLOT_BYTES;
+  static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
+  static constexpr int T_S = 0, T_DP = BN, T_ACC = 2 * BN;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(2 * BN + D <= 512, "TMEM");
+  static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
+};
+
+template <int D, KvMode M>
+struct KvCfg {
+  static constexpr int BM = 128;                 // key rows (MMA M)
+  static constexpr int BN = D == 128 ? 128 : 64; // query rows per contribution tile
+  static constexpr bool NEED_V = M != KvMode::kDvOnly;
+  static constexpr int NRES = NEED_V ? 2 : 1;
+  static constexpr int NSLOT = (D == 256 && M == KvMode::kDkOnly) ? 3 : 4;
+  static constexpr int RES_BYTES = BM * D * 2;
+  static constexpr int SLOT_BYTES = BN * D * 2;
+  static constexpr int SMEM_RES = 0;
+  static constexpr int SMEM_SLOT = NRES * RES_BYTES;
+  static constexpr int SMEM_VEC = SMEM_SLOT + NSLOT * SLOT_BYTES;   // LSE / Delta, 2 buffers
+  static constexpr int SMEM_BAR = SMEM_VEC + 2 * 2 * BN * 4;
+  static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
+  // TMEM columns: S^T, [dP^T], [dV], [dK]
+  static constexpr int T_S = 0;
+  static constexpr int T_DP = BN;
+  static constexpr int T_DV = M == KvMode::kBoth ? 2 * BN : BN;       // kDvOnly: after S^T
+  static constexpr int T_DK = M == KvMode::kBoth ? 2 * BN + D : 2 * BN;
+  static constexpr int TMEM_COLS = 512;
+  static_assert((M == KvMode::kBoth ? 2 * BN + 2 * D : (M == KvMode::kDvOnly ? BN + D : 2 * BN + D)) <= 512,
+                "TMEM");
+  static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
+};
+
+// ---------------------------------------------------------------------------
+// iteration orders (identical in every role of a CTA)
+
+// KV tiles feeding one query tile's dQ, in ring-step order: steps s ascending,
+// the source rank's visible KV chunks ascending, tiles ascending.
+template <int BN>
+struct DqIter {
+  int cp, r, cq, L, S, q_valid_hi;
+  int s, nv, vi, vis[2], t, ntile, kv_lo, kv_hi;
+  bool diag, done;
+
+  __device__ void load_segment() {
+    const int j = vis[vi];
+    diag = (j == cq);
+    kv_lo = j * L;
+    kv_hi = min((j + 1) * L, S);
+    if (diag) kv_hi = min(kv_hi, q_valid_hi);
+    ntile = kv_hi > kv_lo ? (kv_hi - kv_lo + BN - 1) / BN : 0;
+    t = 0;
+  }
+  __device__ void settle() {
+    // advance to the next non-empty tile from the current (s, vi, t)
+    while (!done) {
+      if (vi < nv && t < ntile) return;
+      if (vi < nv) {
+        ++vi;
+        if (vi < nv) { load_segment(); continue; }
+      }
+      ++s;
+      if (s >= cp) { done = true; return; }
+      nv = visible_kv_chunks(cq, ring_source(r, s, cp), cp, vis);
+      vi = 0;
+      if (nv > 0) load_segment();
+    }
+  }
+  __device__ void init(int cp_, int cq_, int L_, int S_, int q_lo, int q_valid_hi_) {
+    cp = cp_; cq = cq_; r = chunk_owner(cq_, cp_); L = L_; S = S_; q_valid_hi = q_valid_hi_;
+    done = q_valid_hi <= q_lo;       // no real query row in this tile
+    s = 0;
+    nv = visible_kv_chunks(cq, ring_source(r, 0, cp), cp, vis);
+    vi = 0;
+    ntile = 0;
+    t = 0;
+    if (!done && nv > 0) load_segment();
+    settle();
+  }
+  __device__ int k0() const { return kv_lo + t * BN; }
+  __device__ void next() { ++t; settle(); }
+};
+
+// Contributions feeding one KV tile's dK/dV, in the canonical order: ring
+// steps s = 0..CP-1 (rank src+s), query chunk r before 2CP-1-r, query tile
+// ascending, q head of the GQA group ascending.
+template <int BN>
+struct KvIter {
+  int cp, C, j, src, L, S, k_lo, G, g;
+  int s, which, cq, tq, ntq, h, q_valid_hi;
+  bool done;
+
+  __device__ bool load_chunk() {
+    // sets up query tiles of chunk cq; false if none contribute
+    const int r = (src + s) % cp;
+    cq = which == 0 ? r : C - 1 - r;
+    if (j > cq) return false;
+    const int qa = cq * L;
+    q_valid_hi = min((cq + 1) * L, S);
+    if (q_valid_hi <= qa) return false;
+    ntq = (q_valid_hi - qa + BN - 1) / BN;
+    tq = 0;
+    if (cq == j) tq = max(0, (k_lo - qa) / BN);   // diagonal: tiles ending before the KV tile see nothing
+    h = 0;
+    return tq < ntq;
+  }
+  __device__ void settle_chunk() {
+    while (!done) {
+      if (load_chunk()) return;
+      if (++which == 2) {
+        which = 0;
+        if (++s >= cp) { done = true; return; }
+      }
+    }
+  }
+  __device__ void init(int cp_, int j_, int L_, int S_, int k_lo_, int G_, int g_) {
+    cp = cp_; C = 2 * cp_; j = j_; src = chunk_owner(j_, cp_); L = L_; S = S_; k_lo = k_lo_;
+    G = G_; g = g_;
+    s = 0; which = 0;
+    done = k_lo >= S;               // no real key row in this tile
+    settle_chunk();
+  }
+  __device__ int q0() const { return cq * L + tq * BN; }
+  __device__ int head() const { return g * G + h; }
+  __device__ void next() {
+    if (++h < G) return;
+    h = 0;
+    if (++tq < ntq) return;
+    if (++which == 2) {
+      which = 0;
+      if (++s >= cp) { done = true; return; }
+    }
+    settle_chunk();
+  }
+};
+
+struct SeqInfo {
+  int start, S, L;
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const BwdParams& p, int b) {
+  SeqInfo si;
+  si.start = __ldg(p.cu_pad + b);
+  si.S = __ldg(p.cu + b + 1) - __ldg(p.cu + b);
+  si.L = (__ldg(p.cu_pad + b + 1) - si.start) / (2 * p.cp);
+  return si;
 }
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&r)[32], float mul,
+                                               bool zero) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v4 = 0; v4 < 4; ++v4) {
+    uint4 u;
+    if (zero) {
+      u = make_uint4(0, 0, 0, 0);
+    } else {
+      u.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * mul, __uint_as_float(r[8 * v4 + 1]) * mul);
+      u.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * mul, __uint_as_float(r[8 * v4 + 3]) * mul);
+      u.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * mul, __uint_as_float(r[8 * v4 + 5]) * mul);
+      u.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul);
+    }
+    d[v4] = u;
+  }
+}
+
+// Issue the K-major (x) K-major product D[tmem] = A[smem tile, M rows] * B[smem tile, N rows]^T
+// over a contraction of length KD (both tiles TMA SW128 layout, 64-column chunks).
+template <int MROWS, int NROWS, int KD>
+__device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
+  constexpr uint32_t idesc = idesc_bf16_f32(MROWS, NROWS, false, false);
+#pragma unroll
+  for (int k = 0; k < KD / 16; ++k) {
+    const uint32_t a = a_base + (k / 4) * (MROWS * 128) + (k % 4) * 32;
+    const uint32_t b = b_base + (k / 4) * (NROWS * 128) + (k % 4) * 32;
+    umma_ss(d_tmem, smem_desc_sw128(a, 16, 1024), smem_desc_sw128(b, 16, 1024), idesc, k > 0 ? 1u : 0u);
+  }
+}
+
+// D[tmem, M=128 x N=D] (+)= A[tmem bf16, 128 x KROWS] * B[smem tile KROWS rows x D, MN-major]
+template <int KROWS, int D>
+__device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, false, true);
+#pragma unroll
+  for (int k = 0; k < KROWS / 16; ++k) {
+    const uint32_t b = b_base + k * 16 * 128;
+    umma_ts(d_tmem, a_tmem + k * 8, smem_desc_sw128(b, KROWS * 128, 1024), idesc,
+            (accumulate || k > 0) ? 1u : 0u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dQ pass
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const BwdParams p) {
+  using Cfg = DqCfg<D>;
+  constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, KCH = D / 64;
+  const int item_idx = blockIdx.x / p.hq;
+  if (item_idx >= p.hdr->n_dq) return;
+  if (status_bad(p.status)) return;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::SMEM_BAR);
+  uint64_t* res_full = bars;
+  uint64_t* full = bars + 1;              // [NSLOT]
+  uint64_t* empty = full + NSLOT;         // [NSLOT]
+  uint64_t* s_full = empty + NSLOT;
+  uint64_t* ds_full = s_full + 1;
+  uint64_t* acc_done = ds_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WorkItem it = p.items[item_idx];
+  const int h = blockIdx.x % p.hq;
+  const int g = h / (p.hq / p.hkv);
+  const SeqInfo si = seq_info(p, it.b);
+  const int q_lo = it.c * si.L + it.tile * BM;                    // first row (sequence position)
+  const int q_hi = min(q_lo + BM, (it.c + 1) * si.L);              // rows owned by this tile
+  const int q_valid_hi = min(q_hi, si.S);
+
+  if (threadIdx.x == 0) {
+    mbar_init(res_full, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(ds_full, 128);
+    mbar_init(acc_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int kv_group_row = static_cast<int>((g / p.hpg_kv) * p.T) + si.start;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      DqIter<BN> itr;
+      itr.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
+      int issued[NSLOT] = {};
+      bool ok = true;
+      if (!itr.done) {
+        const int row = static_cast<int>((h / p.hpg_q) * p.T) + si.start + q_lo;
+        mbar_arrive_expect_tx(res_full, 2 * Cfg::RES_BYTES);
+        for (int kc = 0; kc < KCH; ++kc) {
+          tma_load_3d(smem + Cfg::SMEM_RES + kc * BM * 128, &tm_q, kc * 64, h % p.hpg_q, row, res_full);
+          tma_load_3d(smem + Cfg::SMEM_RES + Cfg::RES_BYTES + kc * BM * 128, &tm_do, kc * 64, h % p.hpg_q, row,
+                      res_full);
+        }
+        // stream order per KV tile: V_j (released early) then K_j
+        for (int t = 0; !itr.done && ok; ++t) {
+          const int slot = t % NSLOT;
+          if (t >= NSLOT) ok = mbar_wait(empty + slot, ((t / NSLOT) - 1) & 1, abort_flag);
+          if (!ok) break;
+          const bool is_v = (t & 1) == 0;
+          const int k0 = itr.k0();
+          mbar_arrive_expect_tx(full + slot, Cfg::SLOT_BYTES);
+          uint8_t* dst = smem + Cfg::SMEM_SLOT + slot * Cfg::SLOT_BYTES;
+          for (int kc = 0; kc < KCH; ++kc)
+            tma_load_3d(dst + kc * BN * 128, is_v ? &tm_v : &tm_k, kc * 64, g % p.hpg_kv, kv_group_row + k0,
+                        full + slot);
+          issued[slot]++;
+          if (!is_v) itr.next();
+        }
+        if (!ok) {
+          raise_status(p.status, CCG_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        volatile int never = 0;
+        mbar_wait(res_full, 0, &never, 200000000ull);
+        for (int s = 0; s < NSLOT; ++s)
+          if (issued[s] > 0) mbar_wait(full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      DqIter<BN> itr;
+      itr.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
+      bool ok = true;
+      if (!itr.done) {
+        const uint32_t q_base = smem_u32(smem + Cfg::SMEM_RES);
+        const uint32_t do_base = q_base + Cfg::RES_BYTES;
+        const uint32_t slot_base = smem_u32(smem + Cfg::SMEM_SLOT);
+        ok = mbar_wait(res_full, 0, abort_flag);
+        tc_fence_after();
+        for (int j = 0; !itr.done && ok; ++j) {
+          const int tv = 2 * j, tk = 2 * j + 1;
+          const int sv = tv % NSLOT, sk = tk % NSLOT;
+          ok = mbar_wait(full + sk, (tk / NSLOT) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          mma_kk<BM, BN, D>(tmem + Cfg::T_S, q_base, slot_base + sk * Cfg::SLOT_BYTES);
+          ok = mbar_wait(full + sv, (tv / NSLOT) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          mma_kk<BM, BN, D>(tmem + Cfg::T_DP, do_base, slot_base + sv * Cfg::SLOT_BYTES);
+          umma_commit(s_full);
+          umma_commit(empty + sv);
+          ok = mbar_wait(ds_full, j & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          mma_tn<BN, D>(tmem + Cfg::T_ACC, tmem + Cfg::T_S, slot_base + sk * Cfg::SLOT_BYTES, j > 0);
+          umma_commit(empty + sk);
+          itr.next();
+        }
+      }
+      if (!ok) {
+        raise_status(p.status, CCG_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit(acc_done);
+      volatile int never = 0;
+      mbar_wait(acc_done, 0, &never, 200000000ull);
+    }
+  } else if (warp >= 4) {
+    const int row = ((warp & 3) << 5) + lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t0 = tmem + lane_base;
+    const int q_pos = q_lo + row;
+    const bool row_valid = q_pos < q_valid_hi;
+    const int64_t grow = thd_row(si.start + q_pos, h, p.hpg_q, p.T);
+    const float lse2 = row_valid ? __ldg(p.lse + grow) * kLog2e : 0.f;
+    const float dlt = row_valid ? __ldg(p.delta + grow) : 0.f;
+    DqIter<BN> itr;
+    itr.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
+    const bool any = !itr.done;
+    bool ok = true;
+    for (int j = 0; !itr.done; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const int k0 = itr.k0();
+      const int kend = itr.diag ? min(itr.kv_hi, q_pos + 1) : itr.kv_hi;
+      const int nvalid = row_valid ? kend - k0 : 0;
+      uint32_t rs[32], rp[32];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        tmem_ld32(t0 + Cfg::T_S + c * 32, rs);
+        tmem_ld32(t0 + Cfg::T_DP + c * 32, rp);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          float ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = c * 32 + 2 * x + e;
+            const float pv = col < nvalid ? ex2_approx(fmaf(__uint_as_float(rs[2 * x + e]), p.scale_log2, -lse2)) : 0.f;
+            ds[e] = pv * (__uint_as_float(rp[2 * x + e]) - dlt) * p.scale;
+          }
+          pk[x] = pack_bf16x2(ds[0], ds[1]);
+        }
+        tmem_st16(t0 + Cfg::T_S + c * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+      itr.next();
+    }
+    if (ok && any) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
+    if (!ok) {
+      raise_status(p.status, CCG_ERR_TIMEOUT);
+      *abort_flag = 1;
+    } else {
+      // rows of the tile inside this chunk: real rows get dQ, padding rows 0
+      tc_fence_after();
+      const bool own = q_pos < q_hi;
+      __nv_bfloat16* dst = p.out0 + grow * D;
+      uint32_t r[32];
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        if (any) {                        // CTA-uniform: every lane loads
+          tmem_ld32(t0 + Cfg::T_ACC + c * 32, r);
+          tmem_wait_ld();
+        }
+        if (own) store_row_bf16(dst + c * 32, r, 1.f, !any || !row_valid);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// dK/dV pass
+template <int D, KvMode MODE>
+__global__ void __launch_bounds__(256, 1)
+attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const BwdParams p) {
+  using Cfg = KvCfg<D, MODE>;
+  constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, KCH = D / 64;
+  constexpr bool DO_DV = MODE != KvMode::kDkOnly;
+  constexpr bool DO_DK = MODE != KvMode::kDvOnly;
+  const int item_idx = blockIdx.x / p.hkv;
+  if (item_idx >= p.hdr->n_kv) return;
+  if (status_bad(p.status)) return;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::SMEM_BAR);
+  uint64_t* res_full = bars;
+  uint64_t* full = bars + 1;
+  uint64_t* empty = full + NSLOT;
+  uint64_t* s_full = empty + NSLOT;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* acc_done = p_full + 1;
+  uint64_t* vec_ready = acc_done + 1;     // [2]: LSE/Delta buffers written by all 128 threads
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_ready + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* vec = reinterpret_cast<float*>(smem + Cfg::SMEM_VEC);   // [2 buffers][lse2 BN | delta BN]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WorkItem it = p.items[item_idx];
+  const int g = blockIdx.x % p.hkv;
+  const int G = p.hq / p.hkv;
+  const SeqInfo si = seq_info(p, it.b);
+  const int k_lo = it.c * si.L + it.tile * BM;
+  const int k_hi = min(k_lo + BM, (it.c + 1) * si.L);
+  const int k_valid_hi = min(k_hi, si.S);
+
+  if (threadIdx.x == 0) {
+    mbar_init(res_full, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(acc_done, 1);
+    mbar_init(vec_ready + 0, 128);
+    mbar_init(vec_ready + 1, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // streamed tiles per contribution: kBoth: dO_i, Q_i; kDvOnly: Q_i (early), dO_i;
+  // kDkOnly: dO_i (early), Q_i
+  constexpr bool FIRST_IS_Q = MODE == KvMode::kDvOnly;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      KvIter<BN> itr;
+      itr.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
+      int issued[NSLOT] = {};
+      bool ok = true;
+      if (!itr.done) {
+        const int krow = static_cast<int>((g / p.hpg_kv) * p.T) + si.start + k_lo;
+        mbar_arrive_expect_tx(res_full, Cfg::NRES * Cfg::RES_BYTES);
+        for (int kc = 0; kc < KCH; ++kc) {
+          tma_load_3d(smem + Cfg::SMEM_RES + kc * BM * 128, &tm_k, kc * 64, g % p.hpg_kv, krow, res_full);
+          if (Cfg::NEED_V)
+            tma_load_3d(smem + Cfg::SMEM_RES + Cfg::RES_BYTES + kc * BM * 128, &tm_v, kc * 64, g % p.hpg_kv,
+                        krow, res_full);
+        }
+        for (int t = 0; !itr.done && ok; ++t) {
+          const int slot = t % NSLOT;
+          if (t >= NSLOT) ok = mbar_wait(empty + slot, ((t / NSLOT) - 1) & 1, abort_flag);
+          if (!ok) break;
+          const bool first = (t & 1) == 0;
+          const bool is_q = first == FIRST_IS_Q;
+          const int hq = itr.head();
+          const int qrow = static_cast<int>((hq / p.hpg_q) * p.T) + si.start + itr.q0();
+          mbar_arrive_expect_tx(full + slot, Cfg::SLOT_BYTES);
+          uint8_t* dst = smem + Cfg::SMEM_SLOT + slot * Cfg::SLOT_BYTES;
+          for (int kc = 0; kc < KCH; ++kc)
+            tma_load_3d(dst + kc * BN * 128, is_q ? &tm_q : &tm_do, kc * 64, hq % p.hpg_q, qrow, full + slot);
+          issued[slot]++;
+          if (!first) itr.next();
+        }
+        if (!ok) {
+          raise_status(p.status, CCG_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        volatile int never = 0;
+        mbar_wait(res_full, 0, &never, 200000000ull);
+        for (int s = 0; s < NSLOT; ++s)
+          if (issued[s] > 0) mbar_wait(full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      KvIter<BN> itr;
+      itr.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
+      bool ok = true;
+      if (!itr.done) {
+        const uint32_t k_base = smem_u32(smem + Cfg::SMEM_RES);
+        const uint32_t v_base = k_base + Cfg::RES_BYTES;
+        const uint32_t slot_base = smem_u32(smem + Cfg::SMEM_SLOT);
+        ok = mbar_wait(res_full, 0, abort_flag);
+        tc_fence_after();
+        for (int i = 0; !itr.done && ok; ++i) {
+          const int t_first = 2 * i, t_second = 2 * i + 1;
+          const int s_first = t_first % NSLOT, s_second = t_second % NSLOT;
+          const int sq = FIRST_IS_Q ? s_first : s_second;
+          const int sdo = FIRST_IS_Q ? s_second : s_first;
+          const int tq = FIRST_IS_Q ? t_first : t_second;
+          const int tdo = FIRST_IS_Q ? t_second : t_first;
+          ok = mbar_wait(full + sq, (tq / NSLOT) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          mma_kk<BM, BN, D>(tmem + Cfg::T_S, k_base, slot_base + sq * Cfg::SLOT_BYTES);
+          ok = mbar_wait(full + sdo, (tdo / NSLOT) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          if (DO_DK) mma_kk<BM, BN, D>(tmem + Cfg::T_DP, v_base, slot_base + sdo * Cfg::SLOT_BYTES);
+          umma_commit(s_full);
+          if (MODE == KvMode::kDvOnly) umma_commit(empty + sq);     // Q_i done after S^T
+          if (MODE == KvMode::kDkOnly) umma_commit(empty + sdo);    // dO_i done after dP^T
+          ok = mbar_wait(p_full, i & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          if (DO_DV) mma_tn<BN, D>(tmem + Cfg::T_DV, tmem + Cfg::T_S, slot_base + sdo * Cfg::SLOT_BYTES, i > 0);
+          if (DO_DK) mma_tn<BN, D>(tmem + Cfg::T_DK, tmem + Cfg::T_DP, slot_base + sq * Cfg::SLOT_BYTES, i > 0);
+          if (MODE != KvMode::kDkOnly) umma_commit(empty + sdo);
+          if (MODE != KvMode::kDvOnly) umma_commit(empty + sq);
+          itr.next();
+        }
+      }
+      if (!ok) {
+        raise_status(p.status, CCG_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit(acc_done);
+      volatile int never = 0;
+      mbar_wait(acc_done, 0, &never, 200000000ull);
+    }
+  } else if (warp >= 4) {
+    const int row = ((warp & 3) << 5) + lane;       // key row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t0 = tmem + lane_base;
+    const int k_pos = k_lo + row;
+    const bool k_valid = k_pos < k_valid_hi;
+    KvIter<BN> itr;
+    itr.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
+    const bool any = !itr.done;
+    bool ok = true;
+    for (int i = 0; !itr.done; ++i) {
+      // LSE (log2 units) and Delta of this contribution's query rows -> SMEM
+      float* vb = vec + (i & 1) * 2 * BN;
+      if (row < BN) {
+        const int qp = itr.q0() + row;
+        const bool qv = qp < itr.q_valid_hi;
+        const int64_t gr = thd_row(si.start + qp, itr.head(), p.hpg_q, p.T);
+        vb[row] = qv ? __ldg(p.lse + gr) * kLog2e : 0.f;
+        vb[BN + row] = (qv && DO_DK) ? __ldg(p.delta + gr) : 0.f;
+      }
+      mbar_arrive(vec_ready + (i & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(vec_ready + (i & 1), (i >> 1) & 1, abort_flag));
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full, i & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const int q0 = itr.q0();
+      // query column c is visible to this key row iff q0+c >= k_pos and q0+c < q_valid_hi
+      const int c_lo = k_valid ? max(0, k_pos - q0) : BN;
+      const int c_hi = k_valid ? itr.q_valid_hi - q0 : 0;
+      uint32_t rs[32], rp[32];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        tmem_ld32(t0 + Cfg::T_S + c * 32, rs);
+        if (DO_DK) tmem_ld32(t0 + Cfg::T_DP + c * 32, rp);
+        tmem_wait_ld();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          float pv[2], ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = c * 32 + 2 * x + e;
+            const bool vis = col >= c_lo && col < c_hi;
+            pv[e] = vis ? ex2_approx(fmaf(__uint_as_float(rs[2 * x + e]), p.scale_log2, -vb[col])) : 0.f;
+            if (DO_DK) ds[e] = pv[e] * (__uint_as_float(rp[2 * x + e]) - vb[BN + col]) * p.scale;
+          }
+          pk[x] = pack_bf16x2(pv[0], pv[1]);
+          if (DO_DK) dk[x] = pack_bf16x2(ds[0], ds[1]);
+        }
+        if (DO_DV) tmem_st16(t0 + Cfg::T_S + c * 16, pk);
+        if (DO_DK) tmem_st16(t0 + Cfg::T_DP + c * 16, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+      itr.next();
+    }
+    if (ok && any) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
+    if (!ok) {
+      raise_status(p.status, CCG_ERR_TIMEOUT);
+      *abort_flag = 1;
+    } else {
+      tc_fence_after();
+      const bool own = k_pos < k_hi;     // rows of this tile inside the chunk
+      const int64_t grow = thd_row(si.start + k_pos, g, p.hpg_kv, p.T);
+      uint32_t r[32];
+      if (DO_DV) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          if (any) {
+            tmem_ld32(t0 + Cfg::T_DV + c * 32, r);
+            tmem_wait_ld();
+          }
+          if (own) store_row_bf16(p.out0 + grow * D + c * 32, r, 1.f, !any || !k_valid);
+        }
+      }
+      if (DO_DK) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          if (any) {
+            tmem_ld32(t0 + Cfg::T_DK + c * 32, r);
+            tmem_wait_ld();
+          }
+          if (own) store_row_bf16(p.out1 + grow * D + c * 32, r, 1.f, !any || !k_valid);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+}
+
+template <class K>
+cudaError_t set_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D>
+cudaError_t launch_dq(const CUtensorMap* m, const BwdParams& p, int grid_items, cudaStream_t s) {
+  using Cfg = DqCfg<D>;
+  const int smem = Cfg::SMEM_TOTAL + 1024;
+  static bool once = false;
+  if (!once) {
+    cudaError_t e = set_smem(attn_bwd_dq_kernel<D>, smem);
+    if (e != cudaSuccess) return e;
+    once = true;
+  }
+  const int64_t grid = static_cast<int64_t>(grid_items) * p.hq;
+  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  attn_bwd_dq_kernel<D><<<static_cast<unsigned>(grid), 256, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  return cudaGetLastError();
+}
+
+template <int D, KvMode MODE>
+cudaError_t launch_kv(const CUtensorMap* m, const BwdParams& p, int grid_items, cudaStream_t s) {
+  using Cfg = KvCfg<D, MODE>;
+  const int smem = Cfg::SMEM_TOTAL + 1024;
+  static bool once = false;
+  if (!once) {
+    cudaError_t e = set_smem(attn_bwd_kv_kernel<D, MODE>, smem);
+    if (e != cudaSuccess) return e;
+    once = true;
+  }
+  const int64_t grid = static_cast<int64_t>(grid_items) * p.hkv;
+  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  attn_bwd_kv_kernel<D, MODE><<<static_cast<unsigned>(grid), 256, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int bwd_q_tile_rows(int) { return 128; }
+int bwd_kv_tile_rows(int) { return 128; }
+// Box rows of the eight tensor maps: 0..3 = q, k, v, dO for the dQ pass,
+// 4..7 = q, k, v, dO for the dK/dV pass.
+int bwd_map_rows(int which, int D) {
+  const bool kv_pass = which >= 4;
+  const int t = which & 3;
+  const bool is_kv_tensor = (t == 1 || t == 2);
+  if (!kv_pass) return is_kv_tensor ? (D == 128 ? DqCfg<128>::BN : DqCfg<256>::BN) : 128;
+  return is_kv_tensor ? 128 : (D == 128 ? KvCfg<128, KvMode::kBoth>::BN : KvCfg<256, KvMode::kDvOnly>::BN);
+}
+
+cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, const WorkItem* kv_items,
+                            const PlanHeader* hdr, const int32_t* cu, const int32_t* cu_pad, const float* lse,
+                            const float* delta, void* dq, void* dk, void* dv, int32_t* status, int cp, int hq,
+                            int hkv, int head_groups, int64_t T, int D, float scale, int grid_q, int grid_kv,
+                            int* launches, cudaStream_t stream) {
+  BwdParams p;
+  p.hdr = hdr;
+  p.cu = cu;
+  p.cu_pad = cu_pad;
+  p.lse = lse;
+  p.delta = delta;
+  p.status = status;
+  p.cp = cp;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.hpg_q = hq / head_groups;
+  p.hpg_kv = hkv / head_groups;
+  p.T = T;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  cudaError_t e;
+  // dQ pass
+  p.items = dq_items;
+  p.out0 = static_cast<__nv_bfloat16*>(dq);
+  p.out1 = nullptr;
+  e = D == 128 ? launch_dq<128>(maps, p, grid_q, stream) : launch_dq<256>(maps, p, grid_q, stream);
+  if (e != cudaSuccess) return e;
+  ++*launches;
+  // dK/dV pass
+  p.items = kv_items;
+  p.out0 = static_cast<__nv_bfloat16*>(dv);
+  p.out1 = static_cast<__nv_bfloat16*>(dk);
+  if (D == 128) {
+    e = launch_kv<128, KvMode::kBoth>(maps + 4, p, grid_kv, stream);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+  } else {
+    e = launch_kv<256, KvMode::kDvOnly>(maps + 4, p, grid_kv, stream);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    e = launch_kv<256, KvMode::kDkOnly>(maps + 4, p, grid_kv, stream);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace ccg
