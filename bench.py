@@ -1,0 +1,400 @@
+"""Benchmark: causal GQA attention fwd+bwd TFLOP/s on one GB300 through libccg.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ccg|reference] [--workload NAME]
+
+One step = one full pass of the CP-emulated path over the workload (for the
+"large" workload: A2A pack of q/k/v/dO, CP split, 8 ring-step forward
+launches, LSE merge, Delta dot, dQ pass, dV and dK passes, A2A unpack of
+o/dQ/dK/dV).  Inputs are resident in HBM and far larger than L2 (no flush
+needed).  Timing: W warm-up steps, then K steps between CUDA events on the
+launching stream, bracketed by a barrier and synchronize, max over ranks.
+Per-kernel durations come from events the library records around each of its
+launches inside the same timed region.  `e2e` repeats the measurement through
+the same public step API from pinned host buffers (H2D inputs + D2H outputs in
+the timed region).  `cpu_baseline` times the FP64 oracle on a bounded sample
+on this host's cores.  Under torchrun (N > 1) every rank runs an independent
+replica (weak scaling, no data-path collective).
+
+--impl reference times the FP64 CPU oracle instead (one (sequence, q head)
+forward+backward per step), on rank 0 only.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from context_causal_gqa_gb300 import workloads as W  # noqa: E402
+
+METRIC = "causal attention fwd+bwd TFLOP/s on 1 GB300 and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+
+SMALL_NCU = W.custom_workload("ncu_small", [8192] * 2, 32, 8, 256, 8, index=9)
+
+
+def get_workload(name):
+    if name == "ncu_small":
+        return SMALL_NCU
+    return W.WORKLOADS[name]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"bf16_burst": d["bf16_tflops"], "bf16_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "hbm": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ algorithmic work per kernel
+def causal_pairs(w):
+    return sum(s * (s + 1) / 2 for s in w.seqlens)
+
+
+def merge_bytes(w):
+    """Sum over rows of K_row*(2D+4) partial reads + (2D+4) write."""
+    C = 2 * w.cp
+    row = 2 * w.head_dim + 4
+    tot = 0.0
+    for S, P in zip(w.seqlens, w.padded):
+        L = P // C
+        for c in range(C):
+            real = max(0, min(L, S - c * L))
+            K = w.cp if c >= w.cp else c + 1
+            tot += real * (K + 1) * row + (L - real) * row
+    return tot * w.hq
+
+
+def kernel_work(w):
+    """name -> (bound, algorithmic amount per launch [FLOP or byte])."""
+    D, hq, hkv, T = w.head_dim, w.hq, w.hkv, w.total_tokens
+    U = 2.0 * D * hq * causal_pairs(w)           # one D-wide GEMM over all causal pairs
+    tq = T * hq * D * 2
+    tkv = T * hkv * D * 2
+    work = {
+        "attn_fwd_step": ("tensor", 2.0 * U / w.cp),
+        "attn_bwd_dq": ("tensor", 3.0 * U),        # S, dP and dQ
+        "attn_bwd_dv": ("tensor", 1.0 * U),
+        "attn_bwd_dk": ("tensor", 1.0 * U),
+        "attn_bwd_dkdv": ("tensor", 2.0 * U),
+        "lse_merge": ("hbm", merge_bytes(w)),
+        "bwd_dot": ("hbm", 2.0 * tq + T * hq * 4),
+        "thd_pack": ("hbm", (2 * tq + 2 * tkv) / 2.0),      # mean over q, k, v, dO
+        "thd_unpack": ("hbm", (2 * tq + 2 * tkv) / 2.0),    # mean over o, dq, dk, dv
+        "plan": ("hbm", 0.0),
+    }
+    return work
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.uuid and parts[1] != self.uuid:
+                    continue
+                try:
+                    sm.append(float(parts[2].split()[0]))
+                    smax.append(float(parts[3].split()[0]))
+                    power.append(float(parts[4].split()[0]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[6:10]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+def cpu_oracle_units(w, n_units=None, budget_s=12.0, seed=0):
+    """Time the FP64 oracle's forward+backward of whole (sequence, q head)
+    pairs of the workload on this host.  Returns (flops, seconds, units)."""
+    import numpy as np
+    import torch
+    import oracle
+    S = max(w.seqlens)
+    D = w.head_dim
+    g = torch.Generator().manual_seed(w.seed + 17 + seed)
+    flops = 0.0
+    units = 0
+    t0 = time.perf_counter()
+    while True:
+        q, k, v, do = (torch.randn(S, D, generator=g).to(torch.bfloat16).double().numpy() for _ in range(4))
+        oracle.head_backward(q, k, v, do)
+        flops += 3.5 * 4.0 * D * S * (S + 1) / 2
+        units += 1
+        el = time.perf_counter() - t0
+        if (n_units is not None and units >= n_units) or (n_units is None and el >= budget_s):
+            break
+    del np
+    return flops, time.perf_counter() - t0, units
+
+
+def host_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = max((i.get("num_threads", 1) for i in info if i.get("user_api") == "blas"), default=None)
+        if n:
+            return int(n)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ arms
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return rank, local, world, pg
+
+
+def run_reference(args):
+    rank, _, world, pg = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    w = get_workload(args.workload)
+    for _ in range(args.warmup):
+        cpu_oracle_units(w, n_units=1, seed=99)
+    times, fl = [], 0.0
+    for k in range(args.steps):
+        f, t, _ = cpu_oracle_units(w, n_units=1, seed=k)
+        times.append(t)
+        fl = f
+    ms = 1e3 * sum(times) / len(times)
+    value = fl / (ms / 1e3) / 1e12
+    sample = f"one (sequence, q head) forward+backward at S={max(w.seqlens)}, D={w.head_dim} per step (FP64 numpy oracle)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(w.describe(), workload=w.name),
+            "cpu_baseline": {"kind": "oracle", "cores": host_threads(), "sample": sample, "value": value,
+                             "unit": UNIT},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_ccg(args):
+    import torch
+    rank, local, world, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import context_causal_gqa_gb300 as ccg
+    from context_causal_gqa_gb300.pipeline import AttentionStep, profile_begin, profile_end
+    ccg.load()
+    w = get_workload(args.workload)
+    x = W.make_inputs(w, device=dev, seed=w.seed + 1000 * rank)
+    step = AttentionStep(w, x, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize(dev)
+    step.check()
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    def max_over_ranks(v):
+        if pg is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        return float(t.item())
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    per_step = step.launches_per_step
+    profile_begin(per_step * args.steps + 8)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    launches = 0
+    for _ in range(args.steps):
+        launches += step.run()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier()
+    prof = profile_end()
+    step.check()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms)
+    flops = w.flops_fwd_bwd()
+    value = world * flops / (ms_max / 1e3) / 1e12
+
+    # per-kernel attribution inside the timed region
+    work = kernel_work(w)
+    agg = {}
+    for name, t in prof:
+        a = agg.setdefault(name, [0, 0.0])
+        a[0] += 1
+        a[1] += t
+    tot = sum(a[1] for a in agg.values()) or 1.0
+    pk = peaks()
+    kernels = {}
+    for name, (n, t) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
+        bound, amount = work.get(name, ("hbm", 0.0))
+        avg = t / n
+        if bound == "tensor":
+            ach = amount / (avg / 1e3) / 1e12
+            peak = pk["bf16_sustained"]
+        else:
+            ach = amount / (avg / 1e3) / 1e9
+            peak = pk["hbm"]
+        kernels[name] = {"launches_per_step": n / args.steps, "ms_per_launch": round(avg, 4),
+                         "share": round(t / tot, 4), "bound": bound,
+                         "achieved": round(ach, 2), "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+                         "frac": round(ach / peak, 4) if peak else None}
+    dom = max(agg.items(), key=lambda kv: kv[1][1])[0]
+    dk = kernels[dom]
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            tr = json.load(f)
+        ent = tr.get(w.name, {}).get(dom)
+        if ent and ent.get("source_sha") == source_sha(dom):
+            traffic = ent["bytes_per_launch"]
+    roofline = {"bound": dk["bound"], "achieved": dk["achieved"],
+                "peak": pk["bf16_sustained"] if dk["bound"] == "tensor" else pk["hbm"],
+                "unit": dk["unit"], "frac": dk["frac"], "traffic": traffic, "kernel": dom,
+                "peak_source": pk["source"] + (" bf16 sustained (kernel timed inside a long step)"
+                                               if dk["bound"] == "tensor" else " hbm copy")}
+
+    # end to end from pinned host buffers through the same step API
+    e2e = None
+    if not args.no_e2e:
+        h_in, h_out = step.host_buffers()
+        for d, h in zip(step.input_tensors(), h_in):
+            h.copy_(d)
+        bi, bo = step.io_bytes()
+        step.run_from_host(h_in, h_out)
+        torch.cuda.synchronize(dev)
+        ke = max(2, min(args.steps, 5))
+        barrier()
+        e0.record(stream)
+        for _ in range(ke):
+            step.run_from_host(h_in, h_out)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        step.check()
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / ke)
+        e2e = {"value": world * flops / (ms_e2e / 1e3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo, "ms_per_step": ms_e2e, "steps": ke}
+        del h_in, h_out
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        f, t, u = cpu_oracle_units(w, budget_s=args.cpu_seconds)
+        cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+               "sample": f"{u} x one (sequence, q head) forward+backward at S={max(w.seqlens)}, D={w.head_dim} "
+                         f"(FP64 numpy oracle, {t:.1f} s)"}
+
+    if rank == 0:
+        cfg = dict(w.describe())
+        cfg["workload"] = (f"{w.name}: B={w.batch} x S={max(w.seqlens)} packed THD, Hq{w.hq}/Hkv{w.hkv}, "
+                           f"D{w.head_dim}, causal, {w.cp} emulated CP ranks ({2 * w.cp} chunks)"
+                           + (", A2A head-split pack/unpack round trip" if w.pack_roundtrip else ""))
+        cfg["l2"] = "inputs larger than L2, no flush"
+        cfg["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU, CP emulated"
+        line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms_max, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": cfg, "frac_of_peak": round(value / world / pk["bf16_sustained"], 4),
+                "peak_tflops": pk["bf16_sustained"], "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches, "clocks": clk, "kernels": kernels,
+                "peak_mem_gb": round(torch.cuda.max_memory_allocated(dev) / 1e9, 2)}
+        print(json.dumps(line))
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def source_sha(kernel):
+    import hashlib
+    files = {"attn_fwd_step": "attn_fwd.cu", "lse_merge": "elementwise.cu", "bwd_dot": "elementwise.cu",
+             "thd_pack": "elementwise.cu", "thd_unpack": "elementwise.cu"}
+    f = files.get(kernel, "attn_bwd.cu")
+    with open(os.path.join(ROOT, "context_causal_gqa_gb300", "csrc", f), "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ccg", choices=["ccg", "reference"])
+    ap.add_argument("--workload", default="large", choices=list(W.WORKLOADS) + ["ncu_small"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ccg":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ccg(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -32,6 +32,10 @@ SIGNATURES = {
     "ccg_get_status": (ctypes.c_int, [c_vp, c_vp]),
     "ccg_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "ccg_last_launch_count": (c_i32, []),
+    "ccg_profile_begin": (ctypes.c_int, [c_i32]),
+    "ccg_profile_end": (ctypes.c_int, []),
+    "ccg_profile_count": (c_i32, []),
+    "ccg_profile_get": (ctypes.c_int, [c_i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(c_f32)]),
 }
 
 _LIB = None

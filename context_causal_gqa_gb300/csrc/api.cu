@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -40,6 +41,36 @@ int bwd_q_tile_rows(int D);
 int bwd_map_rows(int which, int D);
 
 cudaError_t launch_lse_merge(const MergeArgs& a, int num_sms, cudaStream_t stream);
+
+}  // namespace ccg
+
+namespace {
+
+struct ProfState {
+  bool on = false;
+  std::vector<cudaEvent_t> ev;       // 2 per launch
+  std::vector<const char*> names;
+  int n = 0;
+};
+thread_local ProfState g_prof;
+
+}  // namespace
+
+namespace ccg {
+
+void prof_begin(const char* kernel_name, cudaStream_t stream) {
+  ProfState& p = g_prof;
+  if (!p.on || 2 * (p.n + 1) > static_cast<int>(p.ev.size())) return;
+  p.names[p.n] = kernel_name;
+  cudaEventRecord(p.ev[2 * p.n], stream);
+}
+
+void prof_end(cudaStream_t stream) {
+  ProfState& p = g_prof;
+  if (!p.on || 2 * (p.n + 1) > static_cast<int>(p.ev.size())) return;
+  cudaEventRecord(p.ev[2 * p.n + 1], stream);
+  ++p.n;
+}
 
 }  // namespace ccg
 
@@ -154,9 +185,12 @@ bool make_thd_map(CUtensorMap* m, const void* base, int D, int hpg, int64_t rows
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-#define CCG_CUDA(expr)                       \
+#define CCG_LAUNCH(name, stream, expr)       \
   do {                                       \
-    if ((expr) != cudaSuccess) return CCG_ERR_CUDA; \
+    prof_begin(name, stream);                \
+    const cudaError_t e_ = (expr);           \
+    prof_end(stream);                        \
+    if (e_ != cudaSuccess) return CCG_ERR_CUDA; \
     ++launches;                              \
   } while (0)
 
@@ -198,6 +232,39 @@ const char* ccg_status_str(ccg_status s) {
 
 int32_t ccg_last_launch_count(void) { return g_last_launches; }
 
+ccg_status ccg_profile_begin(int32_t capacity) {
+  ProfState& p = g_prof;
+  if (capacity < 1) return CCG_ERR_INVALID_ARG;
+  for (cudaEvent_t e : p.ev) cudaEventDestroy(e);
+  p.ev.assign(2 * static_cast<size_t>(capacity), nullptr);
+  p.names.assign(capacity, nullptr);
+  for (auto& e : p.ev)
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      p.ev.clear();
+      p.on = false;
+      return CCG_ERR_CUDA;
+    }
+  p.n = 0;
+  p.on = true;
+  return CCG_OK;
+}
+
+ccg_status ccg_profile_end(void) {
+  g_prof.on = false;
+  return CCG_OK;
+}
+
+int32_t ccg_profile_count(void) { return g_prof.n; }
+
+ccg_status ccg_profile_get(int32_t i, const char** kernel_name, float* ms) {
+  ProfState& p = g_prof;
+  if (i < 0 || i >= p.n || !kernel_name || !ms) return CCG_ERR_INVALID_ARG;
+  if (cudaEventSynchronize(p.ev[2 * i + 1]) != cudaSuccess) return CCG_ERR_CUDA;
+  if (cudaEventElapsedTime(ms, p.ev[2 * i], p.ev[2 * i + 1]) != cudaSuccess) return CCG_ERR_CUDA;
+  *kernel_name = p.names[i];
+  return CCG_OK;
+}
+
 ccg_status ccg_get_status(const int32_t* d_status, ccg_stream_t stream) {
   if (d_status == nullptr) return CCG_ERR_INVALID_ARG;
   int32_t h = 0;
@@ -216,8 +283,9 @@ ccg_status ccg_cp_split(const int32_t* cu_seqlens, const int32_t* cu_seqlens_pad
   if (!cu_seqlens || !cu_seqlens_padded || !chunk_table || !d_status) return CCG_ERR_INVALID_ARG;
   if (batch < 1 || total_tokens < 0) return CCG_ERR_INVALID_ARG;
   if (cp < 1 || cp > kMaxCP) return CCG_ERR_UNSUPPORTED;
-  CCG_CUDA(launch_chunk_table(cu_seqlens, cu_seqlens_padded, batch, total_tokens, cp, chunk_table,
-                              d_status, reinterpret_cast<cudaStream_t>(stream)));
+  CCG_LAUNCH("cp_split", reinterpret_cast<cudaStream_t>(stream),
+             launch_chunk_table(cu_seqlens, cu_seqlens_padded, batch, total_tokens, cp, chunk_table, d_status,
+                                reinterpret_cast<cudaStream_t>(stream)));
   g_last_launches = launches;
   return CCG_OK;
 }
@@ -244,7 +312,8 @@ ccg_status ccg_cp_lse_merge(int32_t nparts, const void* const* o_parts, const fl
   a.rows = rows;
   a.D = head_dim;
   a.status = nullptr;
-  CCG_CUDA(launch_lse_merge(a, num_sms_cached(), reinterpret_cast<cudaStream_t>(stream)));
+  CCG_LAUNCH("lse_merge", reinterpret_cast<cudaStream_t>(stream),
+             launch_lse_merge(a, num_sms_cached(), reinterpret_cast<cudaStream_t>(stream)));
   g_last_launches = launches;
   return CCG_OK;
 }
@@ -257,8 +326,9 @@ ccg_status ccg_bwd_dot(const void* o, const void* dout, int64_t rows, int32_t he
   if (head_dim != 128 && head_dim != 256) return CCG_ERR_UNSUPPORTED;
   if (!aligned16(o) || !aligned16(dout)) return CCG_ERR_ALIGNMENT;
   if (rows == 0) return CCG_OK;
-  CCG_CUDA(launch_bwd_dot(o, dout, rows, head_dim, delta, nullptr, num_sms_cached(),
-                          reinterpret_cast<cudaStream_t>(stream)));
+  CCG_LAUNCH("bwd_dot", reinterpret_cast<cudaStream_t>(stream),
+             launch_bwd_dot(o, dout, rows, head_dim, delta, nullptr, num_sms_cached(),
+                            reinterpret_cast<cudaStream_t>(stream)));
   g_last_launches = launches;
   return CCG_OK;
 }
@@ -274,8 +344,9 @@ static ccg_status thd_permute(bool pack, const void* src, const int32_t* cu_pad,
   if ((static_cast<int64_t>(heads / cp) * head_dim) % 8 != 0) return CCG_ERR_UNSUPPORTED;
   if (!aligned16(src) || !aligned16(dst)) return CCG_ERR_ALIGNMENT;
   if (T == 0) return CCG_OK;
-  CCG_CUDA(launch_thd_permute(pack, src, dst, cu_pad, batch, T, heads, head_dim, cp, d_status,
-                              num_sms_cached(), reinterpret_cast<cudaStream_t>(stream)));
+  CCG_LAUNCH(pack ? "thd_pack" : "thd_unpack", reinterpret_cast<cudaStream_t>(stream),
+             launch_thd_permute(pack, src, dst, cu_pad, batch, T, heads, head_dim, cp, d_status,
+                                num_sms_cached(), reinterpret_cast<cudaStream_t>(stream)));
   g_last_launches = launches;
   return CCG_OK;
 }
@@ -302,8 +373,9 @@ static ccg_status fwd_steps(const ccg_attn_desc* d, int first, int last, const v
   auto* base = static_cast<uint8_t*>(workspace);
   auto* hdr = reinterpret_cast<PlanHeader*>(base + L.hdr);
   auto* items = reinterpret_cast<WorkItem*>(base + L.fwd_items);
-  CCG_CUDA(launch_plan(cu, cu_pad, d->batch, d->total_tokens, d->cp, kQTile, kMinKvTile, L.cap_q,
-                       L.cap_kv, 1, hdr, items, nullptr, nullptr, status, s));
+  CCG_LAUNCH("plan", s,
+             launch_plan(cu, cu_pad, d->batch, d->total_tokens, d->cp, kQTile, kMinKvTile, L.cap_q, L.cap_kv, 1,
+                         hdr, items, nullptr, nullptr, status, s));
   const int hg = d->head_groups;
   const int64_t rows = d->total_tokens * hg;
   const int bn = d->head_dim == 128 ? 128 : 64;
@@ -316,9 +388,10 @@ static ccg_status fwd_steps(const ccg_attn_desc* d, int first, int last, const v
   for (int stp = first; stp <= last; ++stp) {
     auto* o_s = static_cast<uint8_t*>(o_part) + size_t(stp - first) * o_stride;
     auto* l_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(lse_part) + size_t(stp - first) * lse_stride);
-    CCG_CUDA(launch_attn_fwd_step(tq, tk, tv, items + size_t(stp) * L.cap_q, hdr, cu, cu_pad, o_s, l_s,
-                                  status, stp, d->cp, d->hq, d->hkv, hg, d->total_tokens, d->head_dim,
-                                  scale, L.cap_q, s));
+    CCG_LAUNCH("attn_fwd_step", s,
+               launch_attn_fwd_step(tq, tk, tv, items + size_t(stp) * L.cap_q, hdr, cu, cu_pad, o_s, l_s, status,
+                                    stp, d->cp, d->hq, d->hkv, hg, d->total_tokens, d->head_dim, scale, L.cap_q,
+                                    s));
   }
   *launches_out = launches;
   return CCG_OK;
@@ -381,7 +454,7 @@ ccg_status ccg_attn_fwd(const ccg_attn_desc* desc, const void* q, const void* k,
   a.rows = static_cast<int64_t>(rows);
   a.D = desc->head_dim;
   a.status = d_status;
-  CCG_CUDA(launch_lse_merge(a, num_sms_cached(), s));
+  CCG_LAUNCH("lse_merge", s, launch_lse_merge(a, num_sms_cached(), s));
   g_last_launches = launches;
   return CCG_OK;
 }
@@ -413,10 +486,12 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
   const int hg = desc->head_groups;
   const int64_t rows = desc->total_tokens * hg;
   int launches = 0;
-  CCG_CUDA(launch_plan(cu_seqlens, cu_seqlens_padded, desc->batch, desc->total_tokens, desc->cp,
-                       bwd_q_tile_rows(D), bwd_kv_tile_rows(D), L.cap_q, L.cap_kv, 2, hdr, nullptr,
-                       dq_items, kv_items, d_status, s));
-  CCG_CUDA(launch_bwd_dot(o, dout, desc->total_tokens * desc->hq, D, delta, d_status, num_sms_cached(), s));
+  CCG_LAUNCH("plan", s,
+             launch_plan(cu_seqlens, cu_seqlens_padded, desc->batch, desc->total_tokens, desc->cp,
+                         bwd_q_tile_rows(D), bwd_kv_tile_rows(D), L.cap_q, L.cap_kv, 2, hdr, nullptr, dq_items,
+                         kv_items, d_status, s));
+  CCG_LAUNCH("bwd_dot", s,
+             launch_bwd_dot(o, dout, desc->total_tokens * desc->hq, D, delta, d_status, num_sms_cached(), s));
   // maps: 0 q, 1 k, 2 v, 3 dO -- row boxes per pass
   CUtensorMap maps[8];
   const int hq_g = desc->hq / hg, hkv_g = desc->hkv / hg;

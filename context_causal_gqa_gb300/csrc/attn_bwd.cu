@@ -782,7 +782,9 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
   p.items = dq_items;
   p.out0 = static_cast<__nv_bfloat16*>(dq);
   p.out1 = nullptr;
+  prof_begin("attn_bwd_dq", stream);
   e = D == 128 ? launch_dq<128>(maps, p, grid_q, stream) : launch_dq<256>(maps, p, grid_q, stream);
+  prof_end(stream);
   if (e != cudaSuccess) return e;
   ++*launches;
   // dK/dV pass
@@ -790,14 +792,20 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
   p.out0 = static_cast<__nv_bfloat16*>(dv);
   p.out1 = static_cast<__nv_bfloat16*>(dk);
   if (D == 128) {
+    prof_begin("attn_bwd_dkdv", stream);
     e = launch_kv<128, KvMode::kBoth>(maps + 4, p, grid_kv, stream);
+    prof_end(stream);
     if (e != cudaSuccess) return e;
     ++*launches;
   } else {
+    prof_begin("attn_bwd_dv", stream);
     e = launch_kv<256, KvMode::kDvOnly>(maps + 4, p, grid_kv, stream);
+    prof_end(stream);
     if (e != cudaSuccess) return e;
     ++*launches;
+    prof_begin("attn_bwd_dk", stream);
     e = launch_kv<256, KvMode::kDkOnly>(maps + 4, p, grid_kv, stream);
+    prof_end(stream);
     if (e != cudaSuccess) return e;
     ++*launches;
   }

@@ -88,6 +88,11 @@ __device__ __forceinline__ int find_sequence(const int32_t* __restrict__ cu_pad,
   return lo;
 }
 
+// Launch timing hooks (defined in api.cu): no-ops unless a profile is open
+// on the calling host thread.
+void prof_begin(const char* kernel_name, cudaStream_t stream);
+void prof_end(cudaStream_t stream);
+
 __device__ __forceinline__ bool status_bad(const int32_t* status) {
   return *reinterpret_cast<const volatile int32_t*>(status) != 0;
 }

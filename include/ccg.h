@@ -193,6 +193,21 @@ const char* ccg_status_str(ccg_status s);
  * host thread issued (for launch accounting by callers). */
 int32_t ccg_last_launch_count(void);
 
+/* Launch timing for callers that measure the library.  Between
+ * ccg_profile_begin and ccg_profile_end, every kernel the library launches
+ * from the calling host thread is bracketed by two CUDA events recorded on
+ * the stream it is launched on.  `capacity` event pairs are created by
+ * ccg_profile_begin (host-side CUDA events; no device memory is allocated);
+ * launches beyond the capacity are not timed.  Returns CCG_ERR_CUDA if the
+ * events cannot be created. */
+ccg_status ccg_profile_begin(int32_t capacity);
+ccg_status ccg_profile_end(void);
+/* Number of launches timed by the last profile. */
+int32_t ccg_profile_count(void);
+/* Kernel name (static string) and elapsed milliseconds of the i-th timed
+ * launch; waits for that launch's end event. */
+ccg_status ccg_profile_get(int32_t i, const char** kernel_name, float* ms);
+
 #ifdef __cplusplus
 }
 #endif
