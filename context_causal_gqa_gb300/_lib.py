@@ -23,6 +23,8 @@ SIGNATURES = {
                                          c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "ccg_attn_bwd": (ctypes.c_int, [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                     c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "ccg_attn_bwd_noalloc": (ctypes.c_int, [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                            c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "ccg_cp_split": (ctypes.c_int, [c_vp, c_vp, c_i32, c_i64, c_i32, c_vp, c_vp, c_vp]),
     "ccg_cp_lse_merge": (ctypes.c_int, [c_i32, ctypes.POINTER(c_vp), ctypes.POINTER(c_vp), c_i64, c_i32,
                                         c_vp, c_vp, c_vp]),

@@ -136,6 +136,34 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
                         void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                         int32_t* d_status, ccg_stream_t stream);
 
+/* Allocation-free variant of ccg_attn_bwd, for callers that cannot allocate
+ * device memory (for example a plugin whose host framework owns all device
+ * memory and hands it only input and output pointers, or code that must not
+ * call cudaMalloc once it is running).  It computes exactly what
+ * ccg_attn_bwd computes, with the same arguments minus the workspace: its
+ * scratch (work plan and Delta) is a fixed 16 MiB array in the library's
+ * device image, held by every GPU that loads the library until the process
+ * exits.  This entry point has no counterpart in the TransformerEngine pull
+ * request the rest of this header follows.
+ *   Limit: ccg_workspace_size(desc, 1) must be at most 16,776,960 bytes
+ *   (16 MiB - 256); larger problems return CCG_ERR_WORKSPACE and launch
+ *   nothing.  The library itself allocates nothing here (no cudaMalloc,
+ *   no cudaFree).
+ *   d_status: the caller's status word, as in ccg_attn_bwd; NULL selects a
+ *   status word inside the fixed scratch that is cleared at the start of
+ *   every call and cannot be read back.
+ *   The first call on a device looks up the array's device address on that
+ *   device (cudaGetSymbolAddress, with the device current); make that first
+ *   call before any stream capture.  All calls on a device share the one
+ *   array, which keeps the previous call's contents (every call rewrites
+ *   the plan and Delta before reading them): calls whose execution overlaps
+ *   on the GPU race on it and must not be issued. */
+ccg_status ccg_attn_bwd_noalloc(const ccg_attn_desc* desc, const void* q, const void* k,
+                                const void* v, const void* o, const void* dout, const float* lse,
+                                const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded,
+                                void* dq, void* dk, void* dv, int32_t* d_status,
+                                ccg_stream_t stream);
+
 /* Load-balanced CP split (TransformerEngine PR, Independent-node complete-CP
  * evidence: CP8 over packed THD; the 2*CP chunk "reorder"): writes
  * chunk_table[b][c] = {first physical row, length} for c = 0..2CP-1, with
