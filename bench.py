@@ -36,13 +36,16 @@ from context_causal_gqa_gb300 import workloads as W  # noqa: E402
 METRIC = "causal attention fwd+bwd TFLOP/s on 1 GB300 and % of dense BF16 tensor peak"
 UNIT = "TFLOP/s"
 
-SMALL_NCU = W.custom_workload("ncu_small", [8192] * 2, 32, 8, 256, 8, index=9)
+# extra shapes for profiling and the D=128 companion measurement (not bench defaults)
+EXTRA = {
+    "ncu_small": W.custom_workload("ncu_small", [8192] * 2, 32, 8, 256, 8, index=9),
+    "ncu_small_d128": W.custom_workload("ncu_small_d128", [8192] * 2, 32, 8, 128, 8, index=10),
+    "large_d128": W.custom_workload("large_d128", [8192] * 64, 32, 8, 128, 8, index=11, pack_roundtrip=True),
+}
 
 
 def get_workload(name):
-    if name == "ncu_small":
-        return SMALL_NCU
-    return W.WORKLOADS[name]
+    return EXTRA[name] if name in EXTRA else W.WORKLOADS[name]
 
 
 def peaks():
@@ -384,7 +387,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ccg", choices=["ccg", "reference"])
-    ap.add_argument("--workload", default="large", choices=list(W.WORKLOADS) + ["ncu_small"])
+    ap.add_argument("--workload", default="large", choices=list(W.WORKLOADS) + list(EXTRA))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -49,9 +49,9 @@ def up_to_date():
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src, verbose):
+def _compile(src, verbose, extra=()):
     obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc()] + flags() + ["-c", src, "-o", obj]
+    cmd = [nvcc()] + flags() + list(extra) + ["-c", src, "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -60,14 +60,16 @@ def _compile(src, verbose):
     return obj, r.stderr
 
 
-def build(force=False, verbose=False):
-    """Compile csrc/*.cu and link _build/libccg.so; returns the library path."""
-    if not force and up_to_date():
+def build(force=False, verbose=False, extra=()):
+    """Compile csrc/*.cu and link _build/libccg.so; returns the library path.
+
+    `extra` are additional nvcc flags (e.g. -D tile-shape overrides)."""
+    if not force and not extra and up_to_date():
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
     srcs = sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(lambda s: _compile(s, verbose), srcs))
+        results = list(ex.map(lambda s: _compile(s, verbose, extra), srcs))
     if verbose:
         for _, log in results:
             if log.strip():

@@ -492,16 +492,13 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
                          kv_items, d_status, s));
   CCG_LAUNCH("bwd_dot", s,
              launch_bwd_dot(o, dout, desc->total_tokens * desc->hq, D, delta, d_status, num_sms_cached(), s));
-  // maps: 0 q, 1 k, 2 v, 3 dO -- row boxes per pass
-  CUtensorMap maps[8];
+  // maps: q, k, v, dO for each of the three backward kernels (row boxes differ)
+  CUtensorMap maps[12];
   const int hq_g = desc->hq / hg, hkv_g = desc->hkv / hg;
   const void* bases[4] = {q, k, v, dout};
   const int hpgs[4] = {hq_g, hkv_g, hkv_g, hq_g};
-  for (int i = 0; i < 4; ++i) {
-    if (!make_thd_map(&maps[i], bases[i], D, hpgs[i], rows, bwd_map_rows(i, D)) ||
-        !make_thd_map(&maps[4 + i], bases[i], D, hpgs[i], rows, bwd_map_rows(4 + i, D)))
-      return CCG_ERR_CUDA;
-  }
+  for (int i = 0; i < 12; ++i)
+    if (!make_thd_map(&maps[i], bases[i % 4], D, hpgs[i % 4], rows, bwd_map_rows(i, D))) return CCG_ERR_CUDA;
   int kl = 0;
   if (launch_attn_bwd(maps, dq_items, kv_items, hdr, cu_seqlens, cu_seqlens_padded, lse, delta, dq, dk, dv,
                       d_status, desc->cp, desc->hq, desc->hkv, hg, desc->total_tokens, D,

@@ -51,45 +51,71 @@ struct BwdParams {
 
 // ---------------------------------------------------------------------------
 // tile configurations
-template <int D>
+//
+// Both passes keep two S/dP tile buffers in TMEM and run two softmax
+// warpgroups: tile (or contribution) j is formed by warpgroup j % 2 in
+// buffer j % 2 while the tensor core computes the neighbouring tile, since
+// with the final LSE every tile's P is independent of the others.
+constexpr int kThreads = 384;    // warp 0 TMA, 1 MMA, 2 TMEM alloc, 3 idle, 4-11 two softmax warpgroups
+
+template <int D, int BN_, int NSLOT_, int NBUF_>
 struct DqCfg {
   static constexpr int BM = 128;                 // query rows (MMA M)
-  static constexpr int BN = D == 128 ? 128 : 64; // key rows per tile (MMA N of S, K of dQ)
-  static constexpr int NSLOT = D == 128 ? 4 : 3; // single-tile slots for K_j / V_j
+  static constexpr int BN = BN_;                 // key rows per tile (MMA N of S, K of dQ)
+  static constexpr int NSLOT = NSLOT_;           // single-tile slots for K_j / V_j
+  // NBUF = 2: tiles alternate between two TMEM buffers and the two softmax
+  // warpgroups (the tensor core works on the next tile meanwhile); NBUF = 1:
+  // one buffer, both warpgroups split every tile's columns (for shapes whose
+  // shared memory leaves too few slots to keep two tiles in flight).
+  static constexpr int NBUF = NBUF_;
+  static constexpr bool SPLIT = NBUF == 1;
   static constexpr int RES_BYTES = BM * D * 2;   // Q or dO
   static constexpr int SLOT_BYTES = BN * D * 2;
   static constexpr int SMEM_RES = 0;
   static constexpr int SMEM_SLOT = 2 * RES_BYTES;
   static constexpr int SMEM_BAR = SMEM_SLOT + NSLOT * SLOT_BYTES;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
-  static constexpr int T_S = 0, T_DP = BN, T_ACC = 2 * BN;
+  static constexpr int T_BUF = 2 * BN;           // buffer b: S at b*T_BUF, dP at b*T_BUF + BN
+  static constexpr int T_ACC = NBUF * T_BUF;
+  // dS (BF16, the A operand of dQ += dS K): packed in place over S when one
+  // warpgroup owns the whole tile; with split columns it goes to its own
+  // region, since the other warpgroup may still be reading S there
+  static constexpr int T_A = SPLIT ? T_ACC + D : -1;
   static constexpr int TMEM_COLS = 512;
-  static_assert(2 * BN + D <= 512, "TMEM");
+  static_assert(NBUF * 2 * BN + D + (SPLIT ? BN / 2 : 0) <= 512, "TMEM");
+  static_assert((SPLIT ? BN / 2 : BN) % 32 == 0, "softmax chunking");
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
 };
 
-template <int D, KvMode M>
+template <int D, KvMode M, int BN_, int NSLOT_, int NBUF_>
 struct KvCfg {
   static constexpr int BM = 128;                 // key rows (MMA M)
-  static constexpr int BN = D == 128 ? 128 : 64; // query rows per contribution tile
+  static constexpr int BN = BN_;                 // query rows per contribution tile
+  static constexpr int NBUF = NBUF_;             // as in DqCfg
+  static constexpr bool SPLIT = NBUF == 1;
   static constexpr bool NEED_V = M != KvMode::kDvOnly;
+  static constexpr bool HAS_DP = M != KvMode::kDvOnly;
   static constexpr int NRES = NEED_V ? 2 : 1;
-  static constexpr int NSLOT = (D == 256 && M == KvMode::kDkOnly) ? 3 : 4;
+  static constexpr int NSLOT = NSLOT_;
   static constexpr int RES_BYTES = BM * D * 2;
   static constexpr int SLOT_BYTES = BN * D * 2;
   static constexpr int SMEM_RES = 0;
   static constexpr int SMEM_SLOT = NRES * RES_BYTES;
-  static constexpr int SMEM_VEC = SMEM_SLOT + NSLOT * SLOT_BYTES;   // LSE / Delta, 2 buffers
+  static constexpr int SMEM_VEC = SMEM_SLOT + NSLOT * SLOT_BYTES;   // [WG][lse2 BN | delta BN]
   static constexpr int SMEM_BAR = SMEM_VEC + 2 * 2 * BN * 4;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
-  // TMEM columns: S^T, [dP^T], [dV], [dK]
-  static constexpr int T_S = 0;
-  static constexpr int T_DP = BN;
-  static constexpr int T_DV = M == KvMode::kBoth ? 2 * BN : BN;       // kDvOnly: after S^T
-  static constexpr int T_DK = M == KvMode::kBoth ? 2 * BN + D : 2 * BN;
+  // TMEM: buffer b holds S^T at b*T_BUF and (if HAS_DP) dP^T at b*T_BUF + BN
+  static constexpr int T_BUF = HAS_DP ? 2 * BN : BN;
+  static constexpr int T_DV = NBUF * T_BUF;
+  static constexpr int T_DK = M == KvMode::kBoth ? NBUF * T_BUF + D : NBUF * T_BUF;
+  static constexpr int ACC_END = NBUF * T_BUF + (M == KvMode::kBoth ? 2 * D : D);
+  // P^T / dS^T (BF16 A operands): in place over S^T / dP^T when one warpgroup
+  // owns the whole tile, in their own regions when the columns are split
+  static constexpr int T_AP = SPLIT ? ACC_END : -1;
+  static constexpr int T_AD = SPLIT ? ACC_END + (M == KvMode::kDkOnly ? 0 : BN / 2) : -1;
   static constexpr int TMEM_COLS = 512;
-  static_assert((M == KvMode::kBoth ? 2 * BN + 2 * D : (M == KvMode::kDvOnly ? BN + D : 2 * BN + D)) <= 512,
-                "TMEM");
+  static_assert(ACC_END + (SPLIT ? (M == KvMode::kBoth ? BN : BN / 2) : 0) <= 512, "TMEM");
+  static_assert((SPLIT ? BN / 2 : BN) % 32 == 0, "softmax chunking");
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
 };
 
@@ -227,38 +253,33 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
 }
 
 // Issue the K-major (x) K-major product D[tmem] = A[smem tile, M rows] * B[smem tile, N rows]^T
-// over a contraction of length KD (both tiles TMA SW128 layout, 64-column chunks).
+// over a contraction of length KD (both tiles TMA SW128 layout, 64-column chunks);
+// a_desc / b_desc are the tiles' base descriptors.
 template <int MROWS, int NROWS, int KD>
-__device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
+__device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
   constexpr uint32_t idesc = idesc_bf16_f32(MROWS, NROWS, false, false);
 #pragma unroll
-  for (int k = 0; k < KD / 16; ++k) {
-    const uint32_t a = a_base + (k / 4) * (MROWS * 128) + (k % 4) * 32;
-    const uint32_t b = b_base + (k / 4) * (NROWS * 128) + (k % 4) * 32;
-    umma_ss(d_tmem, smem_desc_sw128(a, 16, 1024), smem_desc_sw128(b, 16, 1024), idesc, k > 0 ? 1u : 0u);
-  }
+  for (int k = 0; k < KD / 16; ++k)
+    umma_ss(d_tmem, a_desc + kmajor_step(MROWS, k), b_desc + kmajor_step(NROWS, k), idesc, k > 0 ? 1u : 0u);
 }
 
-// D[tmem, M=128 x N=D] (+)= A[tmem bf16, 128 x KROWS] * B[smem tile KROWS rows x D, MN-major]
+// D[tmem, M=128 x N=D] (+)= A[tmem bf16, 128 x KROWS] * B[smem tile KROWS rows x D, MN-major];
+// b_desc is the base descriptor of B built with LBO = KROWS*128.
 template <int KROWS, int D>
-__device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, bool accumulate) {
+__device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, D, false, true);
 #pragma unroll
-  for (int k = 0; k < KROWS / 16; ++k) {
-    const uint32_t b = b_base + k * 16 * 128;
-    umma_ts(d_tmem, a_tmem + k * 8, smem_desc_sw128(b, KROWS * 128, 1024), idesc,
-            (accumulate || k > 0) ? 1u : 0u);
-  }
+  for (int k = 0; k < KROWS / 16; ++k)
+    umma_ts(d_tmem, a_tmem + k * 8, b_desc + mnmajor_step(k), idesc, (accumulate || k > 0) ? 1u : 0u);
 }
 
 // ---------------------------------------------------------------------------
 // dQ pass
-template <int D>
-__global__ void __launch_bounds__(256, 1)
+template <class Cfg, int D>
+__global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const BwdParams p) {
-  using Cfg = DqCfg<D>;
   constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, KCH = D / 64;
   const int item_idx = blockIdx.x / p.hq;
   if (item_idx >= p.hdr->n_dq) return;
@@ -271,9 +292,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   uint64_t* res_full = bars;
   uint64_t* full = bars + 1;              // [NSLOT]
   uint64_t* empty = full + NSLOT;         // [NSLOT]
-  uint64_t* s_full = empty + NSLOT;
-  uint64_t* ds_full = s_full + 1;
-  uint64_t* acc_done = ds_full + 1;
+  uint64_t* s_full = empty + NSLOT;       // [2]
+  uint64_t* ds_full = s_full + 2;         // [2]
+  uint64_t* acc_done = ds_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -292,8 +313,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(ds_full, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(ds_full + b, Cfg::SPLIT ? 256 : 128);
+    }
     mbar_init(acc_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -312,7 +335,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (lane == 0) {
       DqIter<BN> itr;
       itr.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
-      int issued[NSLOT] = {};
+      int issued[NSLOT];
+      for (int s = 0; s < NSLOT; ++s) issued[s] = 0;
       bool ok = true;
       if (!itr.done) {
         const int row = static_cast<int>((h / p.hpg_q) * p.T) + si.start + q_lo;
@@ -322,7 +346,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tma_load_3d(smem + Cfg::SMEM_RES + Cfg::RES_BYTES + kc * BM * 128, &tm_do, kc * 64, h % p.hpg_q, row,
                       res_full);
         }
-        // stream order per KV tile: V_j (released early) then K_j
+        // stream order per KV tile: V_j (released after dP) then K_j (released after dQ)
         for (int t = 0; !itr.done && ok; ++t) {
           const int slot = t % NSLOT;
           if (t >= NSLOT) ok = mbar_wait(empty + slot, ((t / NSLOT) - 1) & 1, abort_flag);
@@ -349,34 +373,57 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      DqIter<BN> itr;
-      itr.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
+      DqIter<BN> ahead;
+      ahead.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
       bool ok = true;
-      if (!itr.done) {
+      if (!ahead.done) {
         const uint32_t q_base = smem_u32(smem + Cfg::SMEM_RES);
-        const uint32_t do_base = q_base + Cfg::RES_BYTES;
+        const uint64_t q_desc = smem_desc_sw128(q_base, 16, 1024);
+        const uint64_t do_desc = smem_desc_sw128(q_base + Cfg::RES_BYTES, 16, 1024);
         const uint32_t slot_base = smem_u32(smem + Cfg::SMEM_SLOT);
+        // per slot: K-major (S, dP) and MN-major (dQ) base descriptors
+        uint64_t slot_k[NSLOT], slot_mn[NSLOT];
+#pragma unroll
+        for (int s2 = 0; s2 < NSLOT; ++s2) {
+          slot_k[s2] = smem_desc_sw128(slot_base + s2 * Cfg::SLOT_BYTES, 16, 1024);
+          slot_mn[s2] = smem_desc_sw128(slot_base + s2 * Cfg::SLOT_BYTES, BN * 128, 1024);
+        }
         ok = mbar_wait(res_full, 0, abort_flag);
         tc_fence_after();
-        for (int j = 0; !itr.done && ok; ++j) {
+        // S and dP of tile j into buffer j % 2
+        auto issue_sp = [&](int j) -> bool {
           const int tv = 2 * j, tk = 2 * j + 1;
           const int sv = tv % NSLOT, sk = tk % NSLOT;
-          ok = mbar_wait(full + sk, (tk / NSLOT) & 1, abort_flag);
-          if (!ok) break;
+          const int b = j % Cfg::NBUF;
+          const uint32_t buf = tmem + b * Cfg::T_BUF;
+          if (!mbar_wait(full + sk, (tk / NSLOT) & 1, abort_flag)) return false;
           tc_fence_after();
-          mma_kk<BM, BN, D>(tmem + Cfg::T_S, q_base, slot_base + sk * Cfg::SLOT_BYTES);
-          ok = mbar_wait(full + sv, (tv / NSLOT) & 1, abort_flag);
-          if (!ok) break;
+          mma_kk<BM, BN, D>(buf, q_desc, slot_k[sk]);
+          if (!mbar_wait(full + sv, (tv / NSLOT) & 1, abort_flag)) return false;
           tc_fence_after();
-          mma_kk<BM, BN, D>(tmem + Cfg::T_DP, do_base, slot_base + sv * Cfg::SLOT_BYTES);
-          umma_commit(s_full);
+          mma_kk<BM, BN, D>(buf + BN, do_desc, slot_k[sv]);
+          umma_commit(s_full + b);
           umma_commit(empty + sv);
-          ok = mbar_wait(ds_full, j & 1, abort_flag);
+          return true;
+        };
+        int j_sp = 0;
+        while (ok && !ahead.done && j_sp < Cfg::NBUF) {
+          ok = issue_sp(j_sp++);
+          ahead.next();
+        }
+        for (int j = 0; ok && j < j_sp; ++j) {
+          const int b = j % Cfg::NBUF;
+          ok = mbar_wait(ds_full + b, (j / Cfg::NBUF) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          mma_tn<BN, D>(tmem + Cfg::T_ACC, tmem + Cfg::T_S, slot_base + sk * Cfg::SLOT_BYTES, j > 0);
+          const int sk = (2 * j + 1) % NSLOT;
+          const uint32_t a_op = Cfg::SPLIT ? tmem + Cfg::T_A : tmem + b * Cfg::T_BUF;
+          mma_tn<BN, D>(tmem + Cfg::T_ACC, a_op, slot_mn[sk], j > 0);
           umma_commit(empty + sk);
-          itr.next();
+          if (!ahead.done) {
+            ok = issue_sp(j_sp++);
+            ahead.next();
+          }
         }
       }
       if (!ok) {
@@ -388,9 +435,12 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_wait(acc_done, 0, &never, 200000000ull);
     }
   } else if (warp >= 4) {
+    const int wg = (warp - 4) >> 2;   // softmax warpgroup: tiles j % 2 == wg, or half the columns (SPLIT)
     const int row = ((warp & 3) << 5) + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t0 = tmem + lane_base;
+    constexpr int NC = Cfg::SPLIT ? BN / 64 : BN / 32;   // 32-column chunks per warpgroup
+    const int c_first = Cfg::SPLIT ? wg * NC : 0;
     const int q_pos = q_lo + row;
     const bool row_valid = q_pos < q_valid_hi;
     const int64_t grow = thd_row(si.start + q_pos, h, p.hpg_q, p.T);
@@ -400,8 +450,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     itr.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
     const bool any = !itr.done;
     bool ok = true;
-    for (int j = 0; !itr.done; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag));
+    for (int j = 0; !itr.done; ++j, itr.next()) {
+      if (!Cfg::SPLIT && (j & 1) != wg) continue;
+      const int b = j % Cfg::NBUF;
+      const uint32_t tb = t0 + b * Cfg::T_BUF;
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j / Cfg::NBUF) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       const int k0 = itr.k0();
@@ -409,9 +462,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const int nvalid = row_valid ? kend - k0 : 0;
       uint32_t rs[32], rp[32];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        tmem_ld32(t0 + Cfg::T_S + c * 32, rs);
-        tmem_ld32(t0 + Cfg::T_DP + c * 32, rp);
+      for (int c = c_first; c < c_first + NC; ++c) {
+        tmem_ld32(tb + c * 32, rs);
+        tmem_ld32(tb + BN + c * 32, rp);
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
@@ -425,25 +478,25 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           }
           pk[x] = pack_bf16x2(ds[0], ds[1]);
         }
-        tmem_st16(t0 + Cfg::T_S + c * 16, pk);
+        tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_A : tb) + c * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(ds_full);
-      itr.next();
+      mbar_arrive(ds_full + b);
     }
     if (ok && any) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
     if (!ok) {
       raise_status(p.status, CCG_ERR_TIMEOUT);
       *abort_flag = 1;
     } else {
-      // rows of the tile inside this chunk: real rows get dQ, padding rows 0
+      // each warpgroup writes half of the columns of the tile's rows in this
+      // chunk: real rows get dQ, padding rows 0
       tc_fence_after();
       const bool own = q_pos < q_hi;
       __nv_bfloat16* dst = p.out0 + grow * D;
       uint32_t r[32];
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
         if (any) {                        // CTA-uniform: every lane loads
           tmem_ld32(t0 + Cfg::T_ACC + c * 32, r);
           tmem_wait_ld();
@@ -460,12 +513,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
 // ---------------------------------------------------------------------------
 // dK/dV pass
-template <int D, KvMode MODE>
-__global__ void __launch_bounds__(256, 1)
+template <class Cfg, int D, KvMode MODE>
+__global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const BwdParams p) {
-  using Cfg = KvCfg<D, MODE>;
   constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, KCH = D / 64;
   constexpr bool DO_DV = MODE != KvMode::kDkOnly;
   constexpr bool DO_DK = MODE != KvMode::kDvOnly;
@@ -480,13 +532,14 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   uint64_t* res_full = bars;
   uint64_t* full = bars + 1;
   uint64_t* empty = full + NSLOT;
-  uint64_t* s_full = empty + NSLOT;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* acc_done = p_full + 1;
-  uint64_t* vec_ready = acc_done + 1;     // [2]: LSE/Delta buffers written by all 128 threads
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_ready + 2);
+  uint64_t* s_full = empty + NSLOT;       // [2]
+  uint64_t* p_full = s_full + 2;          // [2]
+  uint64_t* acc_done = p_full + 2;
+  uint64_t* vec_ready = acc_done + 1;     // [2 WG]: LSE/Delta of the next contribution staged
+  uint64_t* vec_free = vec_ready + 2;     // [2 WG]: every thread finished reading them
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_free + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* vec = reinterpret_cast<float*>(smem + Cfg::SMEM_VEC);   // [2 buffers][lse2 BN | delta BN]
+  float* vec = reinterpret_cast<float*>(smem + Cfg::SMEM_VEC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WorkItem it = p.items[item_idx];
@@ -503,11 +556,15 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(p_full + b, Cfg::SPLIT ? 256 : 128);
+    }
     mbar_init(acc_done, 1);
-    mbar_init(vec_ready + 0, 128);
-    mbar_init(vec_ready + 1, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(vec_ready + b, 128);
+      mbar_init(vec_free + b, 128);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -528,7 +585,8 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (lane == 0) {
       KvIter<BN> itr;
       itr.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
-      int issued[NSLOT] = {};
+      int issued[NSLOT];
+      for (int s = 0; s < NSLOT; ++s) issued[s] = 0;
       bool ok = true;
       if (!itr.done) {
         const int krow = static_cast<int>((g / p.hpg_kv) * p.T) + si.start + k_lo;
@@ -566,41 +624,70 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      KvIter<BN> itr;
-      itr.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
+      KvIter<BN> ahead;
+      ahead.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
       bool ok = true;
-      if (!itr.done) {
+      if (!ahead.done) {
         const uint32_t k_base = smem_u32(smem + Cfg::SMEM_RES);
-        const uint32_t v_base = k_base + Cfg::RES_BYTES;
+        const uint64_t k_desc = smem_desc_sw128(k_base, 16, 1024);
+        const uint64_t v_desc = smem_desc_sw128(k_base + Cfg::RES_BYTES, 16, 1024);
         const uint32_t slot_base = smem_u32(smem + Cfg::SMEM_SLOT);
+        uint64_t slot_k[NSLOT], slot_mn[NSLOT];
+#pragma unroll
+        for (int s2 = 0; s2 < NSLOT; ++s2) {
+          slot_k[s2] = smem_desc_sw128(slot_base + s2 * Cfg::SLOT_BYTES, 16, 1024);
+          slot_mn[s2] = smem_desc_sw128(slot_base + s2 * Cfg::SLOT_BYTES, BN * 128, 1024);
+        }
         ok = mbar_wait(res_full, 0, abort_flag);
         tc_fence_after();
-        for (int i = 0; !itr.done && ok; ++i) {
-          const int t_first = 2 * i, t_second = 2 * i + 1;
-          const int s_first = t_first % NSLOT, s_second = t_second % NSLOT;
-          const int sq = FIRST_IS_Q ? s_first : s_second;
-          const int sdo = FIRST_IS_Q ? s_second : s_first;
-          const int tq = FIRST_IS_Q ? t_first : t_second;
-          const int tdo = FIRST_IS_Q ? t_second : t_first;
-          ok = mbar_wait(full + sq, (tq / NSLOT) & 1, abort_flag);
-          if (!ok) break;
+        auto slot_q = [&](int j) { return (FIRST_IS_Q ? 2 * j : 2 * j + 1); };
+        auto slot_do = [&](int j) { return (FIRST_IS_Q ? 2 * j + 1 : 2 * j); };
+        // S^T (and dP^T) of contribution j into buffer j % 2
+        auto issue_sp = [&](int j) -> bool {
+          const int tq = slot_q(j), tdo = slot_do(j);
+          const int sq = tq % NSLOT, sdo = tdo % NSLOT;
+          const int b = j % Cfg::NBUF;
+          const uint32_t buf = tmem + b * Cfg::T_BUF;
+          if (!mbar_wait(full + sq, (tq / NSLOT) & 1, abort_flag)) return false;
           tc_fence_after();
-          mma_kk<BM, BN, D>(tmem + Cfg::T_S, k_base, slot_base + sq * Cfg::SLOT_BYTES);
-          ok = mbar_wait(full + sdo, (tdo / NSLOT) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          if (DO_DK) mma_kk<BM, BN, D>(tmem + Cfg::T_DP, v_base, slot_base + sdo * Cfg::SLOT_BYTES);
-          umma_commit(s_full);
+          mma_kk<BM, BN, D>(buf, k_desc, slot_k[sq]);
+          if (DO_DK) {
+            if (!mbar_wait(full + sdo, (tdo / NSLOT) & 1, abort_flag)) return false;
+            tc_fence_after();
+            mma_kk<BM, BN, D>(buf + BN, v_desc, slot_k[sdo]);
+          }
+          umma_commit(s_full + b);
           if (MODE == KvMode::kDvOnly) umma_commit(empty + sq);     // Q_i done after S^T
           if (MODE == KvMode::kDkOnly) umma_commit(empty + sdo);    // dO_i done after dP^T
-          ok = mbar_wait(p_full, i & 1, abort_flag);
+          return true;
+        };
+        int j_sp = 0;
+        while (ok && !ahead.done && j_sp < Cfg::NBUF) {
+          ok = issue_sp(j_sp++);
+          ahead.next();
+        }
+        for (int j = 0; ok && j < j_sp; ++j) {
+          const int tq = slot_q(j), tdo = slot_do(j);
+          const int sq = tq % NSLOT, sdo = tdo % NSLOT;
+          const int b = j % Cfg::NBUF;
+          const uint32_t buf = tmem + b * Cfg::T_BUF;
+          ok = mbar_wait(p_full + b, (j / Cfg::NBUF) & 1, abort_flag);
           if (!ok) break;
+          if (MODE == KvMode::kDvOnly) {
+            ok = mbar_wait(full + sdo, (tdo / NSLOT) & 1, abort_flag);
+            if (!ok) break;
+          }
           tc_fence_after();
-          if (DO_DV) mma_tn<BN, D>(tmem + Cfg::T_DV, tmem + Cfg::T_S, slot_base + sdo * Cfg::SLOT_BYTES, i > 0);
-          if (DO_DK) mma_tn<BN, D>(tmem + Cfg::T_DK, tmem + Cfg::T_DP, slot_base + sq * Cfg::SLOT_BYTES, i > 0);
+          const uint32_t a_p = Cfg::SPLIT ? tmem + Cfg::T_AP : buf;
+          const uint32_t a_d = Cfg::SPLIT ? tmem + Cfg::T_AD : buf + BN;
+          if (DO_DV) mma_tn<BN, D>(tmem + Cfg::T_DV, a_p, slot_mn[sdo], j > 0);
+          if (DO_DK) mma_tn<BN, D>(tmem + Cfg::T_DK, a_d, slot_mn[sq], j > 0);
           if (MODE != KvMode::kDkOnly) umma_commit(empty + sdo);
           if (MODE != KvMode::kDvOnly) umma_commit(empty + sq);
-          itr.next();
+          if (!ahead.done) {
+            ok = issue_sp(j_sp++);
+            ahead.next();
+          }
         }
       }
       if (!ok) {
@@ -612,29 +699,43 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_wait(acc_done, 0, &never, 200000000ull);
     }
   } else if (warp >= 4) {
-    const int row = ((warp & 3) << 5) + lane;       // key row of the tile
+    const int wg = (warp - 4) >> 2;   // contributions j % 2 == wg, or half the columns (SPLIT)
+    const int row = ((warp & 3) << 5) + lane;        // key row of the tile
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t0 = tmem + lane_base;
+    constexpr int NC = Cfg::SPLIT ? BN / 64 : BN / 32;
+    const int c_first = Cfg::SPLIT ? wg * NC : 0;
+    constexpr int VEC_N = Cfg::SPLIT ? BN / 2 : BN;  // query rows whose LSE/Delta this warpgroup stages
     const int k_pos = k_lo + row;
     const bool k_valid = k_pos < k_valid_hi;
     KvIter<BN> itr;
     itr.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
     const bool any = !itr.done;
     bool ok = true;
-    for (int i = 0; !itr.done; ++i) {
+    int k = 0;                                       // this warpgroup's contribution count
+    for (int j = 0; !itr.done; ++j, itr.next()) {
+      if (!Cfg::SPLIT && (j & 1) != wg) continue;
+      const int b = j % Cfg::NBUF;
+      const uint32_t tb = t0 + b * Cfg::T_BUF;
       // LSE (log2 units) and Delta of this contribution's query rows -> SMEM
-      float* vb = vec + (i & 1) * 2 * BN;
-      if (row < BN) {
-        const int qp = itr.q0() + row;
+      float* vb = vec + wg * 2 * BN;
+      if (k > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(vec_free + wg, (k - 1) & 1, abort_flag));
+        if (!ok) break;
+      }
+      if (row < VEC_N) {
+        const int col = c_first * 32 + row;
+        const int qp = itr.q0() + col;
         const bool qv = qp < itr.q_valid_hi;
         const int64_t gr = thd_row(si.start + qp, itr.head(), p.hpg_q, p.T);
-        vb[row] = qv ? __ldg(p.lse + gr) * kLog2e : 0.f;
-        vb[BN + row] = (qv && DO_DK) ? __ldg(p.delta + gr) : 0.f;
+        vb[col] = qv ? __ldg(p.lse + gr) * kLog2e : 0.f;
+        vb[BN + col] = (qv && DO_DK) ? __ldg(p.delta + gr) : 0.f;
       }
-      mbar_arrive(vec_ready + (i & 1));
-      ok = __all_sync(0xffffffffu, mbar_wait(vec_ready + (i & 1), (i >> 1) & 1, abort_flag));
+      mbar_arrive(vec_ready + wg);
+      ok = __all_sync(0xffffffffu, mbar_wait(vec_ready + wg, k & 1, abort_flag));
       if (!ok) break;
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full, i & 1, abort_flag));
+      ++k;
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j / Cfg::NBUF) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       const int q0 = itr.q0();
@@ -643,9 +744,9 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const int c_hi = k_valid ? itr.q_valid_hi - q0 : 0;
       uint32_t rs[32], rp[32];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        tmem_ld32(t0 + Cfg::T_S + c * 32, rs);
-        if (DO_DK) tmem_ld32(t0 + Cfg::T_DP + c * 32, rp);
+      for (int c = c_first; c < c_first + NC; ++c) {
+        tmem_ld32(tb + c * 32, rs);
+        if (DO_DK) tmem_ld32(tb + BN + c * 32, rp);
         tmem_wait_ld();
         uint32_t pk[16], dk[16];
 #pragma unroll
@@ -661,13 +762,13 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           pk[x] = pack_bf16x2(pv[0], pv[1]);
           if (DO_DK) dk[x] = pack_bf16x2(ds[0], ds[1]);
         }
-        if (DO_DV) tmem_st16(t0 + Cfg::T_S + c * 16, pk);
-        if (DO_DK) tmem_st16(t0 + Cfg::T_DP + c * 16, dk);
+        if (DO_DV) tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_AP : tb) + c * 16, pk);
+        if (DO_DK) tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_AD : tb + BN) + c * 16, dk);
       }
+      mbar_arrive(vec_free + wg);          // done reading this contribution's LSE/Delta
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full);
-      itr.next();
+      mbar_arrive(p_full + b);
     }
     if (ok && any) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
     if (!ok) {
@@ -678,9 +779,14 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const bool own = k_pos < k_hi;     // rows of this tile inside the chunk
       const int64_t grow = thd_row(si.start + k_pos, g, p.hpg_kv, p.T);
       uint32_t r[32];
-      if (DO_DV) {
+      // kBoth: warpgroup 0 writes dV, warpgroup 1 dK; single-output modes split the columns
+      const bool write_dv = DO_DV && (MODE != KvMode::kBoth || wg == 0);
+      const bool write_dk = DO_DK && (MODE != KvMode::kBoth || wg == 1);
+      const int c_begin = MODE == KvMode::kBoth ? 0 : wg * (D / 64);
+      const int c_end = MODE == KvMode::kBoth ? D / 32 : (wg + 1) * (D / 64);
+      if (write_dv) {
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
           if (any) {
             tmem_ld32(t0 + Cfg::T_DV + c * 32, r);
             tmem_wait_ld();
@@ -688,9 +794,9 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           if (own) store_row_bf16(p.out0 + grow * D + c * 32, r, 1.f, !any || !k_valid);
         }
       }
-      if (DO_DK) {
+      if (write_dk) {
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
           if (any) {
             tmem_ld32(t0 + Cfg::T_DK + c * 32, r);
             tmem_wait_ld();
@@ -711,50 +817,66 @@ cudaError_t set_smem(K kern, int bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int D>
+template <class Cfg, int D>
 cudaError_t launch_dq(const CUtensorMap* m, const BwdParams& p, int grid_items, cudaStream_t s) {
-  using Cfg = DqCfg<D>;
   const int smem = Cfg::SMEM_TOTAL + 1024;
   static bool once = false;
   if (!once) {
-    cudaError_t e = set_smem(attn_bwd_dq_kernel<D>, smem);
+    cudaError_t e = set_smem(attn_bwd_dq_kernel<Cfg, D>, smem);
     if (e != cudaSuccess) return e;
     once = true;
   }
   const int64_t grid = static_cast<int64_t>(grid_items) * p.hq;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  attn_bwd_dq_kernel<D><<<static_cast<unsigned>(grid), 256, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  attn_bwd_dq_kernel<Cfg, D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(m[0], m[1], m[2], m[3], p);
   return cudaGetLastError();
 }
 
-template <int D, KvMode MODE>
+template <class Cfg, int D, KvMode MODE>
 cudaError_t launch_kv(const CUtensorMap* m, const BwdParams& p, int grid_items, cudaStream_t s) {
-  using Cfg = KvCfg<D, MODE>;
   const int smem = Cfg::SMEM_TOTAL + 1024;
   static bool once = false;
   if (!once) {
-    cudaError_t e = set_smem(attn_bwd_kv_kernel<D, MODE>, smem);
+    cudaError_t e = set_smem(attn_bwd_kv_kernel<Cfg, D, MODE>, smem);
     if (e != cudaSuccess) return e;
     once = true;
   }
   const int64_t grid = static_cast<int64_t>(grid_items) * p.hkv;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  attn_bwd_kv_kernel<D, MODE><<<static_cast<unsigned>(grid), 256, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  attn_bwd_kv_kernel<Cfg, D, MODE><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(m[0], m[1], m[2], m[3], p);
   return cudaGetLastError();
 }
+
+// Tile shapes.  D = 256 is limited by shared memory: the resident 128-row
+// tiles take 128 KB (Q, dO) or 128 KB (K, V), so streamed tiles are 32 rows.
+#ifndef CCG_BWD256_BN
+#define CCG_BWD256_BN 64
+#endif
+using Dq128 = DqCfg<128, 64, 8, 2>;
+#ifndef CCG_BWD256_KBN
+#define CCG_BWD256_KBN CCG_BWD256_BN
+#endif
+#ifndef CCG_BWD256_NBUF
+#define CCG_BWD256_NBUF 1
+#endif
+using Dq256 = DqCfg<256, CCG_BWD256_BN, (CCG_BWD256_BN == 32 ? 6 : 3), CCG_BWD256_NBUF>;
+using Kv128 = KvCfg<128, KvMode::kBoth, 64, 8, 2>;
+using Kv256V = KvCfg<256, KvMode::kDvOnly, CCG_BWD256_KBN, (CCG_BWD256_KBN == 32 ? 8 : 4), 2>;
+using Kv256K = KvCfg<256, KvMode::kDkOnly, CCG_BWD256_KBN, (CCG_BWD256_KBN == 32 ? 6 : 3), CCG_BWD256_NBUF>;
 
 }  // namespace
 
 int bwd_q_tile_rows(int) { return 128; }
 int bwd_kv_tile_rows(int) { return 128; }
-// Box rows of the eight tensor maps: 0..3 = q, k, v, dO for the dQ pass,
-// 4..7 = q, k, v, dO for the dK/dV pass.
+// Box rows of the twelve tensor maps: 0..3 = q, k, v, dO for the dQ pass,
+// 4..7 = the same for the first dK/dV kernel, 8..11 for the second (D = 256).
 int bwd_map_rows(int which, int D) {
-  const bool kv_pass = which >= 4;
-  const int t = which & 3;
+  const int pass = which / 4, t = which % 4;
   const bool is_kv_tensor = (t == 1 || t == 2);
-  if (!kv_pass) return is_kv_tensor ? (D == 128 ? DqCfg<128>::BN : DqCfg<256>::BN) : 128;
-  return is_kv_tensor ? 128 : (D == 128 ? KvCfg<128, KvMode::kBoth>::BN : KvCfg<256, KvMode::kDvOnly>::BN);
+  if (pass == 0) return is_kv_tensor ? (D == 128 ? Dq128::BN : Dq256::BN) : 128;
+  if (is_kv_tensor) return 128;
+  if (D == 128) return Kv128::BN;
+  return pass == 1 ? Kv256V::BN : Kv256K::BN;
 }
 
 cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, const WorkItem* kv_items,
@@ -783,7 +905,7 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
   p.out0 = static_cast<__nv_bfloat16*>(dq);
   p.out1 = nullptr;
   prof_begin("attn_bwd_dq", stream);
-  e = D == 128 ? launch_dq<128>(maps, p, grid_q, stream) : launch_dq<256>(maps, p, grid_q, stream);
+  e = D == 128 ? launch_dq<Dq128, 128>(maps, p, grid_q, stream) : launch_dq<Dq256, 256>(maps, p, grid_q, stream);
   prof_end(stream);
   if (e != cudaSuccess) return e;
   ++*launches;
@@ -793,18 +915,18 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
   p.out1 = static_cast<__nv_bfloat16*>(dk);
   if (D == 128) {
     prof_begin("attn_bwd_dkdv", stream);
-    e = launch_kv<128, KvMode::kBoth>(maps + 4, p, grid_kv, stream);
+    e = launch_kv<Kv128, 128, KvMode::kBoth>(maps + 4, p, grid_kv, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
     ++*launches;
   } else {
     prof_begin("attn_bwd_dv", stream);
-    e = launch_kv<256, KvMode::kDvOnly>(maps + 4, p, grid_kv, stream);
+    e = launch_kv<Kv256V, 256, KvMode::kDvOnly>(maps + 4, p, grid_kv, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
     ++*launches;
     prof_begin("attn_bwd_dk", stream);
-    e = launch_kv<256, KvMode::kDkOnly>(maps + 4, p, grid_kv, stream);
+    e = launch_kv<Kv256K, 256, KvMode::kDkOnly>(maps + 8, p, grid_kv, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
     ++*launches;

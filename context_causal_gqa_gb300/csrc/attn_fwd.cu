@@ -234,18 +234,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint32_t q_base = smem_u32(smem + Cfg::SMEM_Q);
       const uint32_t k_base = smem_u32(smem + Cfg::SMEM_K);
       const uint32_t v_base = smem_u32(smem + Cfg::SMEM_V);
+      uint64_t q_desc[NH], k_desc[NSTAGE], v_desc[NSTAGE];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) q_desc[h] = smem_desc_sw128(q_base + h * Cfg::Q_BYTES, 16, 1024);
+#pragma unroll
+      for (int st = 0; st < NSTAGE; ++st) {
+        k_desc[st] = smem_desc_sw128(k_base + st * Cfg::KV_BYTES, 16, 1024);
+        v_desc[st] = smem_desc_sw128(v_base + st * Cfg::KV_BYTES, BN * 128, 1024);
+      }
       bool ok = mbar_wait(q_full, 0, abort_flag);
       tc_fence_after();
       auto issue_s = [&](int h, int j) {
         const int st = j % NSTAGE, buf = j % SBUF;
         const uint32_t d_tmem = tmem + h * Cfg::TMEM_HEAD + buf * BN;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t a = q_base + h * Cfg::Q_BYTES + (k / 4) * (kBM * 128) + (k % 4) * 32;
-          const uint32_t b = k_base + st * Cfg::KV_BYTES + (k / 4) * (BN * 128) + (k % 4) * 32;
-          umma_ss(d_tmem, smem_desc_sw128(a, 16, 1024), smem_desc_sw128(b, 16, 1024), idesc_s,
+        for (int k = 0; k < D / 16; ++k)
+          umma_ss(d_tmem, q_desc[h] + kmajor_step(kBM, k), k_desc[st] + kmajor_step(BN, k), idesc_s,
                   k > 0 ? 1u : 0u);
-        }
         umma_commit(s_full + h * SBUF + buf);
       };
       auto issue_pv = [&](int h, int j) {
@@ -253,11 +258,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t d_tmem = tmem + h * Cfg::TMEM_HEAD + SBUF * BN;
         const uint32_t p_tmem = tmem + h * Cfg::TMEM_HEAD + buf * BN;
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint32_t b = v_base + st * Cfg::KV_BYTES + k * 16 * 128;
-          umma_ts(d_tmem, p_tmem + k * 8, smem_desc_sw128(b, BN * 128, 1024), idesc_o,
-                  (j > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < BN / 16; ++k)
+          umma_ts(d_tmem, p_tmem + k * 8, v_desc[st] + mnmajor_step(k), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
         umma_commit(o_done + h);
       };
       if (ok && n > 0) {

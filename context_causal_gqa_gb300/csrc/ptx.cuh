@@ -122,6 +122,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Offset, in descriptor units (16 bytes), of the k-th 16-element K step of a
+// K-major 128-byte-swizzled tile with `rows` rows stored as 64-column chunks
+// of rows*128 bytes: added to the tile's base descriptor.  The start address
+// is the descriptor's low field, so adding keeps the other fields intact as
+// long as the address stays inside shared memory.
+__host__ __device__ constexpr uint32_t kmajor_step(int rows, int k) {
+  return static_cast<uint32_t>(((k / 4) * (rows * 128) + (k % 4) * 32) >> 4);
+}
+// ... and of the k-th 16-row K step of an MN-major tile (16 rows x 128 bytes).
+__host__ __device__ constexpr uint32_t mnmajor_step(int k) { return static_cast<uint32_t>((k * 16 * 128) >> 4); }
+
 // Instruction descriptor, kind::f16 with BF16 A/B and FP32 accumulator.
 //   [4,6) D fmt (1 = f32)  [7,10) A fmt (1 = bf16)  [10,13) B fmt (1 = bf16)
 //   [15] A major (0 = K)   [16] B major (1 = MN)     [17,23) N >> 3   [24,29) M >> 4

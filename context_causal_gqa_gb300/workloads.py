@@ -87,9 +87,10 @@ WORKLOADS = {
 }
 
 
-def custom_workload(name, seqlens, hq, hkv, head_dim, cp, pad_to=1, padded=None, index=0):
+def custom_workload(name, seqlens, hq, hkv, head_dim, cp, pad_to=1, padded=None, index=0,
+                    pack_roundtrip=False):
     return Workload(name, index, list(seqlens), hq, hkv, head_dim, cp, pad_to=pad_to,
-                    padded=list(padded) if padded is not None else [])
+                    pack_roundtrip=pack_roundtrip, padded=list(padded) if padded is not None else [])
 
 
 def _randn_bf16(shape, gen, device):
