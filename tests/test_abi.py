@@ -1,0 +1,88 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/ccg.h declares, and rejects bad arguments on the host before any CUDA
+call (fail-closed error convention)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import context_causal_gqa_gb300 as ccg
+from context_causal_gqa_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ccg.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()            # no-op when up to date; nvcc cross-compiles without a GPU
+    return ccg.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ccg_\w+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 15
+    lib = ctypes.CDLL(B.LIB)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in ccg.h but not exported"
+    # and the binding declares a prototype for each of them
+    from context_causal_gqa_gb300._lib import SIGNATURES
+    assert set(names) <= set(SIGNATURES), set(names) - set(SIGNATURES)
+
+
+def test_status_strings(L):
+    for code in range(8):
+        assert len(ccg.status_str(code)) >= 2
+    assert ccg.status_str(99) == "unknown status"
+
+
+def _desc(**kw):
+    d = dict(batch=1, hq=4, hkv=1, head_dim=128, cp=2, total_tokens=512)
+    d.update(kw)
+    return ccg.make_desc(**d)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=64), 2), (dict(head_dim=192), 2), (dict(hq=6, hkv=4), 2), (dict(cp=0), 2),
+    (dict(cp=17), 2), (dict(total_tokens=510), 2), (dict(batch=0), 1), (dict(total_tokens=-4), 1),
+])
+def test_workspace_size_rejects_bad_descriptors(L, kw, code):
+    assert ccg.workspace_size(_desc(**kw), False) == 0
+    assert ccg.workspace_size(_desc(**kw), True) == 0
+
+
+def test_workspace_size_grows_with_problem(L):
+    small, big = _desc(), _desc(total_tokens=4096)
+    assert 0 < ccg.workspace_size(small, False) < ccg.workspace_size(big, False)
+    # forward workspace holds CP partials of O (bf16) and LSE (fp32)
+    assert ccg.workspace_size(big, False) >= 2 * 4096 * 4 * (128 * 2 + 4)
+    assert ccg.workspace_size(big, True) >= 4096 * 4 * 4
+
+
+def _call_fwd(L, desc, ptr=0x10000, ws=1 << 30, wsp=0x100000):
+    p = ctypes.c_void_p(ptr)
+    return L.ccg_attn_fwd(ctypes.byref(desc), p, p, p, p, p, p, p, ctypes.c_void_p(wsp), ws, p, None)
+
+
+def test_host_side_rejections_need_no_gpu(L):
+    assert L.ccg_attn_fwd(None, *([None] * 8), 0, None, None) == 1          # null descriptor
+    assert _call_fwd(L, _desc(head_dim=64)) == 2                             # unsupported D
+    assert _call_fwd(L, _desc(hq=5, hkv=2)) == 2                             # Hq % Hkv
+    assert _call_fwd(L, _desc(), ptr=0x10008) == 3                           # misaligned tensor
+    assert _call_fwd(L, _desc(), ws=16) == 4                                 # workspace too small
+    assert _call_fwd(L, _desc(), wsp=0) == 4                                 # no workspace
+    assert _call_fwd(L, _desc(), wsp=0x100010) == 3                          # workspace not 256-aligned
+    null = ctypes.c_void_p(0)
+    assert L.ccg_cp_lse_merge(0, None, None, 10, 128, null, null, None) == 1
+    assert L.ccg_bwd_dot(null, null, 10, 128, null, None) == 1
+    assert L.ccg_thd_pack(ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1000), 1, 64, 6, 128, 4,
+                          ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1000), None) == 2   # H % cp
+    big = _desc(hq=32, hkv=8, total_tokens=1 << 20, cp=1)
+    assert L.ccg_attn_bwd_noalloc(ctypes.byref(big), *([null] * 12), null) == 4

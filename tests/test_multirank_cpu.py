@@ -1,0 +1,48 @@
+"""The bench's multi-rank path on CPU with gloo (world size 2): each rank
+runs its own replica, the slowest rank's time sets the job time, and the
+job throughput sums the ranks' work (weak scaling, no data-path
+collective)."""
+
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = [12.0, 30.0][rank]                     # rank 1 is the slow one
+    ms_max = bench.reduce_max(dist, ms, "cpu")
+    out[rank] = (ms_max, bench.job_throughput(1e12, world, ms_max))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_and_weak_scaling_aggregate():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    assert res[0] == res[1]
+    ms_max, tput = res[0]
+    assert ms_max == 30.0
+    assert tput == pytest.approx(2 * 1e12 / 0.030 / 1e12)
+
+
+def test_single_process_identity():
+    import bench
+    assert bench.reduce_max(None, 7.5) == 7.5
+    assert bench.job_throughput(2e12, 1, 1000.0) == pytest.approx(2.0)
