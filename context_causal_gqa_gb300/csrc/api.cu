@@ -15,7 +15,7 @@ namespace ccg {
 
 
 cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp, int bm,
-                        int bn, int cap_q, int cap_kv, int want, PlanHeader* hdr,
+                        int bn, int cap_q, int cap_kv, int want, int step_only, PlanHeader* hdr,
                         WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items,
                         int32_t* status, cudaStream_t stream);
 cudaError_t launch_chunk_table(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp,
@@ -25,11 +25,11 @@ cudaError_t launch_bwd_dot(const void* o, const void* dout, int64_t rows, int D,
 cudaError_t launch_thd_permute(bool pack, const void* src, void* dst, const int32_t* cu_pad, int B,
                                int64_t T, int H, int D, int cp, int32_t* status, int num_sms,
                                cudaStream_t stream);
-cudaError_t launch_attn_fwd_step(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                 const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
-                                 const int32_t* cu_pad, void* o, float* lse, int32_t* status,
-                                 int step, int cp, int hq, int hkv, int head_groups, int64_t T,
-                                 int D, float scale, int grid_x, cudaStream_t stream);
+cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
+                            const int32_t* cu_pad, void* o, float* lse, int64_t o_slab, int64_t lse_slab,
+                            int32_t* status, int cp, int hq, int hkv, int head_groups, int64_t T, int D,
+                            float scale, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items,
                             const WorkItem* kv_items, const PlanHeader* hdr, const int32_t* cu,
                             const int32_t* cu_pad, const float* lse, const float* delta, void* dq,
@@ -365,17 +365,19 @@ ccg_status ccg_thd_unpack(const void* in_head_split, const int32_t* cu_seqlens_p
                      x_rank_major, d_status, stream);
 }
 
-static ccg_status fwd_steps(const ccg_attn_desc* d, int first, int last, const void* q, const void* k,
-                            const void* v, const int32_t* cu, const int32_t* cu_pad, void* o_part,
-                            size_t o_stride, float* lse_part, size_t lse_stride, void* workspace,
-                            const Layout& L, int32_t* status, cudaStream_t s, int* launches_out) {
+// Plans and launches the ring-step partials: all steps (step_only < 0) into
+// consecutive slabs of o_part / lse_part, or one step into o_part / lse_part.
+static ccg_status fwd_partials(const ccg_attn_desc* d, int step_only, const void* q, const void* k,
+                               const void* v, const int32_t* cu, const int32_t* cu_pad, void* o_part,
+                               int64_t o_slab, float* lse_part, int64_t lse_slab, void* workspace,
+                               const Layout& L, int32_t* status, cudaStream_t s, int* launches_out) {
   int launches = *launches_out;
   auto* base = static_cast<uint8_t*>(workspace);
   auto* hdr = reinterpret_cast<PlanHeader*>(base + L.hdr);
   auto* items = reinterpret_cast<WorkItem*>(base + L.fwd_items);
   CCG_LAUNCH("plan", s,
              launch_plan(cu, cu_pad, d->batch, d->total_tokens, d->cp, kQTile, kMinKvTile, L.cap_q, L.cap_kv, 1,
-                         hdr, items, nullptr, nullptr, status, s));
+                         step_only, hdr, items, nullptr, nullptr, status, s));
   const int hg = d->head_groups;
   const int64_t rows = d->total_tokens * hg;
   const int bn = d->head_dim == 128 ? 128 : 64;
@@ -384,15 +386,10 @@ static ccg_status fwd_steps(const ccg_attn_desc* d, int first, int last, const v
       !make_thd_map(&tk, k, d->head_dim, d->hkv / hg, rows, bn) ||
       !make_thd_map(&tv, v, d->head_dim, d->hkv / hg, rows, bn))
     return CCG_ERR_CUDA;
-  const float scale = softmax_scale(d);
-  for (int stp = first; stp <= last; ++stp) {
-    auto* o_s = static_cast<uint8_t*>(o_part) + size_t(stp - first) * o_stride;
-    auto* l_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(lse_part) + size_t(stp - first) * lse_stride);
-    CCG_LAUNCH("attn_fwd_step", s,
-               launch_attn_fwd_step(tq, tk, tv, items + size_t(stp) * L.cap_q, hdr, cu, cu_pad, o_s, l_s, status,
-                                    stp, d->cp, d->hq, d->hkv, hg, d->total_tokens, d->head_dim, scale, L.cap_q,
-                                    s));
-  }
+  CCG_LAUNCH("attn_fwd", s,
+             launch_attn_fwd(tq, tk, tv, items, hdr, cu, cu_pad, o_part, lse_part, o_slab, lse_slab, status, d->cp,
+                             d->hq, d->hkv, hg, d->total_tokens, d->head_dim, softmax_scale(d), num_sms_cached(),
+                             s));
   *launches_out = launches;
   return CCG_OK;
 }
@@ -411,8 +408,8 @@ ccg_status ccg_attn_fwd_step(const ccg_attn_desc* desc, int32_t step, const void
   if (!aligned16(o_part)) return CCG_ERR_ALIGNMENT;
   if (desc->total_tokens == 0) return CCG_OK;
   int launches = 0;
-  st = fwd_steps(desc, step, step, q, k, v, cu_seqlens, cu_seqlens_padded, o_part, 0, lse_part, 0,
-                 workspace, L, d_status, reinterpret_cast<cudaStream_t>(stream), &launches);
+  st = fwd_partials(desc, step, q, k, v, cu_seqlens, cu_seqlens_padded, o_part, 0, lse_part, 0, workspace, L,
+                    d_status, reinterpret_cast<cudaStream_t>(stream), &launches);
   g_last_launches = launches;
   return st;
 }
@@ -433,9 +430,9 @@ ccg_status ccg_attn_fwd(const ccg_attn_desc* desc, const void* q, const void* k,
   const size_t rows = size_t(desc->total_tokens) * desc->hq;
   const size_t o_stride = rows * desc->head_dim * 2, l_stride = rows * 4;
   int launches = 0;
-  st = fwd_steps(desc, 0, desc->cp - 1, q, k, v, cu_seqlens, cu_seqlens_padded, base + L.o_parts,
-                 o_stride, reinterpret_cast<float*>(base + L.lse_parts), l_stride, workspace, L, d_status,
-                 s, &launches);
+  st = fwd_partials(desc, -1, q, k, v, cu_seqlens, cu_seqlens_padded, base + L.o_parts,
+                    static_cast<int64_t>(rows * desc->head_dim), reinterpret_cast<float*>(base + L.lse_parts),
+                    static_cast<int64_t>(rows), workspace, L, d_status, s, &launches);
   if (st != CCG_OK) return st;
   MergeArgs a{};
   for (int p = 0; p < desc->cp; ++p) {
@@ -488,7 +485,7 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
   int launches = 0;
   CCG_LAUNCH("plan", s,
              launch_plan(cu_seqlens, cu_seqlens_padded, desc->batch, desc->total_tokens, desc->cp,
-                         bwd_q_tile_rows(D), bwd_kv_tile_rows(D), L.cap_q, L.cap_kv, 2, hdr, nullptr, dq_items,
+                         bwd_q_tile_rows(D), bwd_kv_tile_rows(D), L.cap_q, L.cap_kv, 2, -1, hdr, nullptr, dq_items,
                          kv_items, d_status, s));
   CCG_LAUNCH("bwd_dot", s,
              launch_bwd_dot(o, dout, desc->total_tokens * desc->hq, D, delta, d_status, num_sms_cached(), s));

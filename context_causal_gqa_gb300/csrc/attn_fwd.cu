@@ -1,16 +1,22 @@
-// attn_fwd.cu -- a3: one ring step of the CP-emulated causal GQA forward on
-// the 5th-generation tensor cores (sm_103a).
+// attn_fwd.cu -- a3: the ring-step partials of the CP-emulated causal GQA
+// forward on the 5th-generation tensor cores (sm_103a).
 //
 // TransformerEngine PR "Optimize context parallel attention layouts and
 // gradient accumulation", Independent-node complete-CP evidence: each CP
-// rank attends its two query chunks against the KV it holds at a ring
-// step and keeps the partial output with its LSE ("Stats") for the merge.
+// rank attends its two query chunks against the KV it holds at a ring step
+// and keeps the partial output with its LSE ("Stats") for the merge.
 //
-// One CTA = one 128-row query tile of NH q heads that share one kv head
-// (GQA K/V reuse: every K/V tile is loaded once for the NH heads), looping
-// over the visible KV tiles of the step (causal block skipping: KV tiles past
-// the tile's last row are never loaded).  Roles:
-//   warp 0     TMA producer: Q once, then K/V tiles through an NSTAGE ring
+// One persistent launch covers every ring step: the work list holds one item
+// per (ring step, query chunk, 128-row query tile), heaviest first, and each
+// item is computed for NH q heads that share one kv head (GQA K/V reuse:
+// every K/V tile is loaded once for the NH heads).  An item attends its query
+// tile over the KV chunks of the step's source rank that it can see (causal
+// block skipping: KV tiles past the tile's last row are never loaded) with a
+// fresh online softmax, and writes the step's partial (O_s, LSE_s).  CTAs
+// stride through the list, so the next item's Q load and first S = Q K^T
+// products overlap the current item's last P V product and its epilogue.
+// Roles:
+//   warp 0     TMA producer: Q per item, K/V tiles through an NSTAGE ring
 //   warp 1     MMA issuer (one thread): S = Q K^T (SMEM x SMEM -> TMEM),
 //              O += P V (P from TMEM, V from SMEM -> TMEM)
 //   warp 2     TMEM allocator
@@ -52,14 +58,15 @@ struct FwdCfg {
 };
 
 struct FwdParams {
-  const WorkItem* items;        // this step's items
+  const WorkItem* items;        // combined work list (all planned steps)
   const PlanHeader* hdr;
   const int32_t* cu;
   const int32_t* cu_pad;
-  __nv_bfloat16* o;             // partial O of this step, head-grouped THD
-  float* lse;                   // partial LSE of this step
+  __nv_bfloat16* o;             // partial O of step s at o + s * o_slab (head-grouped THD)
+  float* lse;                   // partial LSE of step s at lse + s * lse_slab
+  int64_t o_slab, lse_slab;     // elements between consecutive steps' partials (0: one step)
   int32_t* status;
-  int step, cp, hq, hkv, hpg_q, hpg_kv;
+  int cp, hq, hkv, hpg_q, hpg_kv;
   int64_t T;
   float scale_log2;
 };
@@ -86,7 +93,7 @@ __device__ __forceinline__ TilePlan make_tile_plan(const FwdParams& p, const Wor
   tp.q_lo = it.c * L + it.tile * kBM;
   tp.q_hi = min(min(tp.q_lo + kBM, (it.c + 1) * L), S);
   int vis[2];
-  const int src = ring_source(chunk_owner(it.c, p.cp), p.step, p.cp);
+  const int src = ring_source(chunk_owner(it.c, p.cp), it.step, p.cp);
   tp.nseg = visible_kv_chunks(it.c, src, p.cp, vis);
   tp.ntiles = 0;
   for (int i = 0; i < 2; ++i) {
@@ -131,8 +138,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   constexpr int BN = Cfg::BN, SBUF = Cfg::SBUF, NSTAGE = Cfg::NSTAGE, KCH = Cfg::KCH;
 
   const int nhg = p.hq / NH;                           // head groups per item
-  const int item_idx = blockIdx.x / nhg;
-  if (item_idx >= p.hdr->n_fwd[p.step]) return;
+  const int64_t n_work = static_cast<int64_t>(p.hdr->n_fwd_all) * nhg;
+  if (static_cast<int64_t>(blockIdx.x) >= n_work) return;
   if (status_bad(p.status)) return;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -140,23 +147,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::SMEM_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;                        // [NSTAGE]
+  uint64_t* q_free = bars + 1;                         // last S of the item done: Q may be reloaded
+  uint64_t* kv_full = bars + 2;                        // [NSTAGE]
   uint64_t* kv_empty = kv_full + NSTAGE;               // [NSTAGE]
   uint64_t* s_full = kv_empty + NSTAGE;                // [NH][SBUF]
   uint64_t* p_full = s_full + NH * SBUF;               // [NH][SBUF]
-  uint64_t* o_done = p_full + NH * SBUF;               // [NH]
-  uint64_t* mma_done = o_done + NH;
+  uint64_t* o_done = p_full + NH * SBUF;               // [NH]: one phase per P V product
+  uint64_t* o_free = o_done + NH;                      // [NH]: the item's O has been read out
+  uint64_t* mma_done = o_free + NH;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const WorkItem it = p.items[item_idx];
-  const TilePlan tp = make_tile_plan<BN>(p, it);
-  const int h0 = (blockIdx.x % nhg) * NH;              // first q head of this CTA
-  const int g = h0 / (p.hq / p.hkv);                   // shared kv head
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_free, 1);
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(kv_full + s, 1);
       mbar_init(kv_empty + s, 1);
@@ -165,7 +171,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(s_full + i, 1);
       mbar_init(p_full + i, 128);
     }
-    for (int h = 0; h < NH; ++h) mbar_init(o_done + h, 1);
+    for (int h = 0; h < NH; ++h) {
+      mbar_init(o_done + h, 1);
+      mbar_init(o_free + h, 128);
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -178,7 +187,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n = tp.ntiles;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -186,45 +194,57 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int qrow_base = tp.seq_start + tp.q_lo;
-      mbar_arrive_expect_tx(q_full, NH * Cfg::Q_BYTES);
-      for (int h = 0; h < NH; ++h) {
-        const int hq = h0 + h;
-        const int row = static_cast<int>((hq / p.hpg_q) * p.T) + qrow_base;
-        for (int kc = 0; kc < KCH; ++kc)
-          tma_load_3d(smem + Cfg::SMEM_Q + h * Cfg::Q_BYTES + kc * kBM * 128, &tm_q, kc * 64,
-                      hq % p.hpg_q, row, q_full);
-      }
-      const int kv_group_row = static_cast<int>((g / p.hpg_kv) * p.T) + tp.seq_start;
-      int issued[NSTAGE] = {};
+      int issued[NSTAGE];
+      for (int s = 0; s < NSTAGE; ++s) issued[s] = 0;
+      int q_loads = 0;
       bool ok = true;
-      for (int j = 0; j < n && ok; ++j) {
-        const int st = j % NSTAGE;
-        if (j >= NSTAGE) ok = mbar_wait(kv_empty + st, ((j / NSTAGE) - 1) & 1, abort_flag);
+      int64_t gkv = 0;                                 // K/V tiles loaded so far by this CTA
+      int item_k = 0;
+      for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item_k) {
+        const WorkItem it = p.items[w / nhg];
+        const int h0 = static_cast<int>(w % nhg) * NH;
+        const int g = h0 / (p.hq / p.hkv);
+        const TilePlan tp = make_tile_plan<BN>(p, it);
+        if (item_k > 0) ok = mbar_wait(q_free, (item_k - 1) & 1, abort_flag);
         if (!ok) break;
-        int k0, khi;
-        bool diag;
-        tile_of<BN>(tp, j, &k0, &khi, &diag);
-        mbar_arrive_expect_tx(kv_full + st, 2 * Cfg::KV_BYTES);
-        for (int kc = 0; kc < KCH; ++kc) {
-          tma_load_3d(smem + Cfg::SMEM_K + st * Cfg::KV_BYTES + kc * BN * 128, &tm_k, kc * 64,
-                      g % p.hpg_kv, kv_group_row + k0, kv_full + st);
-          tma_load_3d(smem + Cfg::SMEM_V + st * Cfg::KV_BYTES + kc * BN * 128, &tm_v, kc * 64,
-                      g % p.hpg_kv, kv_group_row + k0, kv_full + st);
+        const int qrow_base = tp.seq_start + tp.q_lo;
+        mbar_arrive_expect_tx(q_full, NH * Cfg::Q_BYTES);
+        for (int h = 0; h < NH; ++h) {
+          const int hq = h0 + h;
+          const int row = static_cast<int>((hq / p.hpg_q) * p.T) + qrow_base;
+          for (int kc = 0; kc < KCH; ++kc)
+            tma_load_3d(smem + Cfg::SMEM_Q + h * Cfg::Q_BYTES + kc * kBM * 128, &tm_q, kc * 64,
+                        hq % p.hpg_q, row, q_full);
         }
-        issued[st]++;
+        ++q_loads;
+        const int kv_group_row = static_cast<int>((g / p.hpg_kv) * p.T) + tp.seq_start;
+        for (int j = 0; j < tp.ntiles; ++j, ++gkv) {
+          const int st = static_cast<int>(gkv % NSTAGE);
+          if (gkv >= NSTAGE)
+            ok = mbar_wait(kv_empty + st, static_cast<uint32_t>((gkv / NSTAGE) - 1) & 1, abort_flag);
+          if (!ok) break;
+          int k0, khi;
+          bool diag;
+          tile_of<BN>(tp, j, &k0, &khi, &diag);
+          mbar_arrive_expect_tx(kv_full + st, 2 * Cfg::KV_BYTES);
+          for (int kc = 0; kc < KCH; ++kc) {
+            tma_load_3d(smem + Cfg::SMEM_K + st * Cfg::KV_BYTES + kc * BN * 128, &tm_k, kc * 64,
+                        g % p.hpg_kv, kv_group_row + k0, kv_full + st);
+            tma_load_3d(smem + Cfg::SMEM_V + st * Cfg::KV_BYTES + kc * BN * 128, &tm_v, kc * 64,
+                        g % p.hpg_kv, kv_group_row + k0, kv_full + st);
+          }
+          issued[st]++;
+        }
       }
       if (!ok) {
         raise_status(p.status, CCG_ERR_TIMEOUT);
         *abort_flag = 1;
       }
       // never leave a copy in flight into shared memory we are about to release
-      mbar_wait(q_full, 0, abort_flag, 200000000ull);
+      volatile int never = 0;
+      if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, &never, 200000000ull);
       for (int s = 0; s < NSTAGE; ++s)
-        if (issued[s] > 0) {
-          volatile int never = 0;
-          mbar_wait(kv_full + s, (issued[s] - 1) & 1, &never, 200000000ull);
-        }
+        if (issued[s] > 0) mbar_wait(kv_full + s, (issued[s] - 1) & 1, &never, 200000000ull);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -242,10 +262,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         k_desc[st] = smem_desc_sw128(k_base + st * Cfg::KV_BYTES, 16, 1024);
         v_desc[st] = smem_desc_sw128(v_base + st * Cfg::KV_BYTES, BN * 128, 1024);
       }
-      bool ok = mbar_wait(q_full, 0, abort_flag);
-      tc_fence_after();
-      auto issue_s = [&](int h, int j) {
-        const int st = j % NSTAGE, buf = j % SBUF;
+      int64_t gkv = 0;   // K/V tiles consumed (stage ring)
+      int64_t gs = 0;    // S tiles computed (S buffers, P and O barriers)
+      bool ok = true;
+      // S_h of the tile with global index t (K/V in stage st) -> buffer t % SBUF
+      auto issue_s = [&](int h, int64_t t, int st) {
+        const int buf = static_cast<int>(t % SBUF);
         const uint32_t d_tmem = tmem + h * Cfg::TMEM_HEAD + buf * BN;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
@@ -253,49 +275,69 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                   k > 0 ? 1u : 0u);
         umma_commit(s_full + h * SBUF + buf);
       };
-      auto issue_pv = [&](int h, int j) {
-        const int st = j % NSTAGE, buf = j % SBUF;
+      auto issue_pv = [&](int h, int64_t t, int st, bool first) {
+        const int buf = static_cast<int>(t % SBUF);
         const uint32_t d_tmem = tmem + h * Cfg::TMEM_HEAD + SBUF * BN;
         const uint32_t p_tmem = tmem + h * Cfg::TMEM_HEAD + buf * BN;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          umma_ts(d_tmem, p_tmem + k * 8, v_desc[st] + mnmajor_step(k), idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+          umma_ts(d_tmem, p_tmem + k * 8, v_desc[st] + mnmajor_step(k), idesc_o, (!first || k > 0) ? 1u : 0u);
         umma_commit(o_done + h);
       };
-      if (ok && n > 0) {
-        ok = mbar_wait(kv_full + 0, 0, abort_flag);
+      auto wait_kv = [&](int64_t t) -> bool {
+        const bool r = mbar_wait(kv_full + (t % NSTAGE), static_cast<uint32_t>(t / NSTAGE) & 1, abort_flag);
         tc_fence_after();
-        if (ok)
-          for (int h = 0; h < NH; ++h) issue_s(h, 0);
-      }
-      for (int j = 0; j < n && ok; ++j) {
-        const int st = j % NSTAGE;
-        const bool has_next = j + 1 < n;
-        bool next_ready = false;
-        if (SBUF == 2 && has_next) {
-          ok = mbar_wait(kv_full + (j + 1) % NSTAGE, ((j + 1) / NSTAGE) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          next_ready = true;
-          issue_s(0, j + 1);
-        }
-        for (int h = 0; h < NH && ok; ++h) {
-          const int buf = j % SBUF;
-          ok = mbar_wait(p_full + h * SBUF + buf, (j / SBUF) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(h, j);
-          if (SBUF == 1 && has_next) {
-            if (!next_ready) {
-              ok = mbar_wait(kv_full + (j + 1) % NSTAGE, ((j + 1) / NSTAGE) & 1, abort_flag);
-              if (!ok) break;
-              tc_fence_after();
-              next_ready = true;
-            }
-            issue_s(h, j + 1);
+        return r;
+      };
+      int item_k = 0;
+      for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item_k) {
+        const TilePlan tp = make_tile_plan<BN>(p, p.items[w / nhg]);
+        const int n = tp.ntiles;
+        ok = mbar_wait(q_full, item_k & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        // first S of the item
+        ok = wait_kv(gkv);
+        if (!ok) break;
+        for (int h = 0; h < NH; ++h) issue_s(h, gs, static_cast<int>(gkv % NSTAGE));
+        if (n == 1) umma_commit(q_free);
+        for (int j = 0; j < n && ok; ++j) {
+          const int64_t t = gs + j, kt = gkv + j;
+          const int st = static_cast<int>(kt % NSTAGE);
+          const bool has_next = j + 1 < n;
+          bool next_ready = false;
+          if (SBUF == 2 && has_next) {
+            ok = wait_kv(kt + 1);
+            if (!ok) break;
+            next_ready = true;
+            issue_s(0, t + 1, static_cast<int>((kt + 1) % NSTAGE));
+            if (j + 2 == n) umma_commit(q_free);            // that was the item's last S
           }
+          for (int h = 0; h < NH && ok; ++h) {
+            const int buf = static_cast<int>(t % SBUF);
+            ok = mbar_wait(p_full + h * SBUF + buf, static_cast<uint32_t>(t / SBUF) & 1, abort_flag);
+            if (!ok) break;
+            if (j == 0 && item_k > 0) {
+              // the previous item's O must have been read out before it is overwritten
+              ok = mbar_wait(o_free + h, (item_k - 1) & 1, abort_flag);
+              if (!ok) break;
+            }
+            tc_fence_after();
+            issue_pv(h, t, st, j == 0);
+            if (SBUF == 1 && has_next) {
+              if (!next_ready) {
+                ok = wait_kv(kt + 1);
+                if (!ok) break;
+                next_ready = true;
+              }
+              issue_s(h, t + 1, static_cast<int>((kt + 1) % NSTAGE));
+              if (j + 2 == n && h == NH - 1) umma_commit(q_free);
+            }
+          }
+          umma_commit(kv_empty + st);
         }
-        umma_commit(kv_empty + st);
+        gs += n;
+        gkv += n;
       }
       if (!ok) {
         raise_status(p.status, CCG_ERR_TIMEOUT);
@@ -312,99 +354,124 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_head = tmem + lane_base + h * Cfg::TMEM_HEAD;
     const uint32_t t_o = t_head + SBUF * BN;
-    const int q_pos = tp.q_lo + row;
-    float m = -INFINITY, l = 0.f;
+    int64_t gs = 0;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int buf = j % SBUF;
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full + h * SBUF + buf, (j / SBUF) & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      int k0, khi;
-      bool diag;
-      tile_of<BN>(tp, j, &k0, &khi, &diag);
-      // keys visible to this row: k < kend (segment end, and k <= q_pos on the diagonal chunk)
-      const int kend = diag ? min(khi, q_pos + 1) : khi;
-      const int nvalid = kend - k0;                     // may be <= 0 or >= BN
-      const uint32_t t_s = t_head + buf * BN;
-      uint32_t r[32];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        tmem_ld32(t_s + c * 32, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          const float sv = __uint_as_float(r[x]) * p.scale_log2;
-          mx = (c * 32 + x < nvalid) ? fmaxf(mx, sv) : mx;
-        }
-      }
-      float alpha = 1.f;
-      if (mx > m) {
-        if (m == -INFINITY) {
-          m = mx;
-        } else if (mx > m + kRescaleThreshold) {
-          alpha = ex2_approx(m - mx);
-          m = mx;
-        }
-      }
-      const float m_use = (m == -INFINITY) ? 0.f : m;
-      float psum = 0.f;
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        tmem_ld32(t_s + c * 32, r);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int c0 = c * 32 + 2 * x;
-          const float p0 = (c0 < nvalid) ? ex2_approx(__uint_as_float(r[2 * x]) * p.scale_log2 - m_use) : 0.f;
-          const float p1 = (c0 + 1 < nvalid) ? ex2_approx(__uint_as_float(r[2 * x + 1]) * p.scale_log2 - m_use) : 0.f;
-          psum += p0 + p1;
-          pk[x] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(t_s + c * 16, pk);
-      }
-      tmem_wait_st();
-      l = l * alpha + psum;
-      // consume the previous P V product's completion (every phase, in order,
-      // so that parity waits stay unambiguous); it is needed before O may be
-      // rescaled and costs nothing when it has already landed
-      if (j > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(o_done + h, (j - 1) & 1, abort_flag));
+    for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+      const WorkItem it = p.items[w / nhg];
+      const int h0 = static_cast<int>(w % nhg) * NH;
+      const TilePlan tp = make_tile_plan<BN>(p, it);
+      const int n = tp.ntiles;
+      const int q_pos = tp.q_lo + row;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        const int64_t t = gs + j;
+        const int buf = static_cast<int>(t % SBUF);
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(s_full + h * SBUF + buf, static_cast<uint32_t>(t / SBUF) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
-      }
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          tmem_ld32(t_o + c * 32, r);
+        int k0, khi;
+        bool diag;
+        tile_of<BN>(tp, j, &k0, &khi, &diag);
+        // keys visible to this row: k < kend (segment end, and k <= q_pos on the diagonal chunk)
+        const int kend = diag ? min(khi, q_pos + 1) : khi;
+        const int nvalid = kend - k0;                     // may be <= 0 or >= BN
+        const uint32_t t_s = t_head + buf * BN;
+        // S row columns held in registers at once: the whole row when the
+        // register budget allows (one TMEM round trip), else halves
+        constexpr int HOLD = (NH == 1) ? BN : 64;
+        uint32_t sr[HOLD];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int g0 = 0; g0 < BN; g0 += HOLD) {
+#pragma unroll
+          for (int c = 0; c < HOLD / 32; ++c)
+            tmem_ld32(t_s + g0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
           tmem_wait_ld();
 #pragma unroll
-          for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
-          tmem_st32(t_o + c * 32, r);
+          for (int x = 0; x < HOLD; ++x) {
+            const float sv = __uint_as_float(sr[x]) * p.scale_log2;
+            mx = (g0 + x < nvalid) ? fmaxf(mx, sv) : mx;
+          }
+        }
+        float alpha = 1.f;
+        if (mx > m) {
+          if (m == -INFINITY) {
+            m = mx;
+          } else if (mx > m + kRescaleThreshold) {
+            alpha = ex2_approx(m - mx);
+            m = mx;
+          }
+        }
+        const float m_use = (m == -INFINITY) ? 0.f : m;
+        float psum = 0.f;
+#pragma unroll
+        for (int g0 = 0; g0 < BN; g0 += HOLD) {
+          if (HOLD < BN) {
+#pragma unroll
+            for (int c = 0; c < HOLD / 32; ++c)
+              tmem_ld32(t_s + g0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
+            tmem_wait_ld();
+          }
+#pragma unroll
+          for (int c = 0; c < HOLD / 32; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              const int cl = c * 32 + 2 * x, c0 = g0 + cl;
+              const float p0 = (c0 < nvalid) ? ex2_approx(fmaf(__uint_as_float(sr[cl]), p.scale_log2, -m_use)) : 0.f;
+              const float p1 =
+                  (c0 + 1 < nvalid) ? ex2_approx(fmaf(__uint_as_float(sr[cl + 1]), p.scale_log2, -m_use)) : 0.f;
+              psum += p0 + p1;
+              pk[x] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(t_s + (g0 + c * 32) / 2, pk);
+          }
         }
         tmem_wait_st();
+        l = l * alpha + psum;
+        // consume the previous P V product's completion (every phase, in order,
+        // so that parity waits stay unambiguous); it is needed before O may be
+        // rescaled and costs nothing when it has already landed
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(o_done + h, static_cast<uint32_t>(t - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          uint32_t r[32];
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            tmem_ld32(t_o + c * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+            tmem_st32(t_o + c * 32, r);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(p_full + h * SBUF + buf);
       }
-      tc_fence_before();
-      mbar_arrive(p_full + h * SBUF + buf);
-    }
-    if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done + h, (n - 1) & 1, abort_flag));
-    if (!ok) {
-      raise_status(p.status, CCG_ERR_TIMEOUT);
-      *abort_flag = 1;
-    } else if (n > 0) {
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(o_done + h, static_cast<uint32_t>(gs + n - 1) & 1, abort_flag));
+      if (!ok) break;
       tc_fence_after();
+      // read O out of TMEM, then release it for the next item's first P V
       const bool valid = q_pos < tp.q_hi;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const int hq = h0 + h;
       const int64_t orow = thd_row(tp.seq_start + q_pos, hq, p.hpg_q, p.T);
-      uint4* dst = reinterpret_cast<uint4*>(p.o + orow * D);
+      uint4* dst = reinterpret_cast<uint4*>(p.o + it.step * p.o_slab + orow * D);
       uint32_t r[32];
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         tmem_ld32(t_o + c * 32, r);
         tmem_wait_ld();
+        if (c == D / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(o_free + h);
+        }
         if (valid) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
@@ -417,7 +484,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
       }
-      if (valid) p.lse[orow] = (m + __log2f(l)) * kLn2;
+      if (valid) p.lse[it.step * p.lse_slab + orow] = (m + __log2f(l)) * kLn2;
+      gs += n;
+    }
+    if (!ok) {
+      raise_status(p.status, CCG_ERR_TIMEOUT);
+      *abort_flag = 1;
     }
   }
   tc_fence_before();
@@ -428,7 +500,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 template <int D, int NH>
 cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FwdParams& p, int grid_x, cudaStream_t stream) {
+                            const FwdParams& p, int grid, cudaStream_t stream) {
   using Cfg = FwdCfg<D, NH>;
   auto kern = attn_fwd_kernel<D, NH>;
   static bool attr_set = false;
@@ -438,11 +510,7 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  // consecutive CTAs share one item (same K/V tiles, different heads): the
-  // K/V tiles they read stay hot in L2
-  const int64_t grid = static_cast<int64_t>(grid_x) * (p.hq / NH);
-  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), Cfg::THREADS, smem, stream>>>(tq, tk, tv, p);
+  kern<<<grid, Cfg::THREADS, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -451,11 +519,13 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
 int fwd_kv_tile_rows(int D) { return D == 128 ? FwdCfg<128, 2>::BN : FwdCfg<256, 1>::BN; }
 int fwd_heads_per_cta(int D, int group) { return (D == 128 && group % 2 == 0) ? 2 : 1; }
 
-cudaError_t launch_attn_fwd_step(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                 const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
-                                 const int32_t* cu_pad, void* o, float* lse, int32_t* status,
-                                 int step, int cp, int hq, int hkv, int head_groups, int64_t T,
-                                 int D, float scale, int grid_x, cudaStream_t stream) {
+// Persistent launch over the combined work list: one CTA per SM (the work
+// count is only known on the device; CTAs with nothing to do exit at once).
+cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
+                            const int32_t* cu_pad, void* o, float* lse, int64_t o_slab, int64_t lse_slab,
+                            int32_t* status, int cp, int hq, int hkv, int head_groups, int64_t T, int D,
+                            float scale, int num_sms, cudaStream_t stream) {
   FwdParams p;
   p.items = items;
   p.hdr = hdr;
@@ -463,8 +533,9 @@ cudaError_t launch_attn_fwd_step(const CUtensorMap& tq, const CUtensorMap& tk, c
   p.cu_pad = cu_pad;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
+  p.o_slab = o_slab;
+  p.lse_slab = lse_slab;
   p.status = status;
-  p.step = step;
   p.cp = cp;
   p.hq = hq;
   p.hkv = hkv;
@@ -473,9 +544,9 @@ cudaError_t launch_attn_fwd_step(const CUtensorMap& tq, const CUtensorMap& tk, c
   p.T = T;
   p.scale_log2 = scale * 1.4426950408889634f;
   const int nh = fwd_heads_per_cta(D, hq / hkv);
-  if (D == 128 && nh == 2) return launch_fwd_impl<128, 2>(tq, tk, tv, p, grid_x, stream);
-  if (D == 128) return launch_fwd_impl<128, 1>(tq, tk, tv, p, grid_x, stream);
-  if (D == 256) return launch_fwd_impl<256, 1>(tq, tk, tv, p, grid_x, stream);
+  if (D == 128 && nh == 2) return launch_fwd_impl<128, 2>(tq, tk, tv, p, num_sms, stream);
+  if (D == 128) return launch_fwd_impl<128, 1>(tq, tk, tv, p, num_sms, stream);
+  if (D == 256) return launch_fwd_impl<256, 1>(tq, tk, tv, p, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 

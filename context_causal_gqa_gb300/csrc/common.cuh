@@ -19,13 +19,15 @@ struct PlanHeader {
   int32_t n_dq;            // dQ-pass items
   int32_t n_kv;            // dK/dV-pass items
   int32_t valid;           // 1 when the sequence promise held
-  int32_t pad[64 - kMaxCP - 3];
+  int32_t n_fwd_all;       // forward items of all planned steps (one combined list)
+  int32_t pad[64 - kMaxCP - 4];
 };
 static_assert(sizeof(PlanHeader) == kPlanHeaderBytes, "plan header size");
 
-// One unit of work: sequence b, chunk c, tile index inside the chunk.
+// One unit of work: sequence b, chunk c, tile index inside the chunk; for
+// forward items `step` is the ring step (0 in the backward lists).
 struct WorkItem {
-  int32_t b, c, tile, cost;
+  int32_t b, c, tile, step;
 };
 
 // Arguments of the K-way LSE merge (a4).  CP-aware mode when cu_pad is

@@ -63,7 +63,7 @@ __device__ int block_emit(int n, int base, CountF count, WriteF write) {
 
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, int B, int64_t T,
-            int cp, int bm, int bn, int cap_q, int cap_kv, int want, PlanHeader* hdr,
+            int cp, int bm, int bn, int cap_q, int cap_kv, int want, int step_only, PlanHeader* hdr,
             WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items, int32_t* status) {
   __shared__ int bad;
   const int C = 2 * cp;
@@ -82,6 +82,7 @@ plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, 
     if (threadIdx.x == 0) {
       raise_status(status, CCG_ERR_SEQLENS);
       for (int s = 0; s < kMaxCP; ++s) hdr->n_fwd[s] = 0;
+      hdr->n_fwd_all = 0;
       hdr->n_dq = 0;
       hdr->n_kv = 0;
       hdr->valid = 0;
@@ -101,12 +102,14 @@ plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, 
 
   int overflow = 0;
   if (want & 1) {
-    for (int s = 0; s < cp; ++s) {
-      WorkItem* out = fwd_items + static_cast<int64_t>(s) * cap_q;
-      int slot = 0;
-      // heavy items first: two visible KV chunks, then one full chunk, then
-      // the diagonal chunk alone
-      for (int cls = 0; cls < 3; ++cls) {
+    // one combined list over the planned ring steps (all, or only `step_only`),
+    // heavy items first: two visible KV chunks, then one full chunk, then the
+    // diagonal chunk alone; inside a class by step, sequence, chunk, tile
+    int slot = 0;
+    const int cap_all = cp * cap_q;
+    for (int cls = 0; cls < 3; ++cls) {
+      for (int s = 0; s < cp; ++s) {
+        if (step_only >= 0 && s != step_only) continue;
         auto count = [&](int i) {
           const int b = i / C, c = i % C;
           int vis[2];
@@ -116,15 +119,16 @@ plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, 
         };
         auto write = [&](int i, int first, int n) {
           const int b = i / C, c = i % C;
-          for (int t = 0; t < n && first + t < cap_q; ++t) out[first + t] = WorkItem{b, c, t, cls};
+          for (int t = 0; t < n && first + t < cap_all; ++t) fwd_items[first + t] = WorkItem{b, c, t, s};
         };
         slot = block_emit(npairs, slot, count, write);
       }
-      if (slot > cap_q) overflow = 1;
-      if (threadIdx.x == 0) hdr->n_fwd[s] = min(slot, cap_q);
     }
-    if (threadIdx.x == 0)
-      for (int s = cp; s < kMaxCP; ++s) hdr->n_fwd[s] = 0;
+    if (slot > cap_all) overflow = 1;
+    if (threadIdx.x == 0) {
+      hdr->n_fwd_all = min(slot, cap_all);
+      for (int s = 0; s < kMaxCP; ++s) hdr->n_fwd[s] = 0;
+    }
   }
   if (want & 2) {
     // dQ pass: later query chunks see more keys, so they go first
@@ -175,10 +179,10 @@ __global__ void chunk_table_kernel(const int32_t* __restrict__ cu, const int32_t
 }  // namespace
 
 cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp, int bm,
-                        int bn, int cap_q, int cap_kv, int want, PlanHeader* hdr,
+                        int bn, int cap_q, int cap_kv, int want, int step_only, PlanHeader* hdr,
                         WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items,
                         int32_t* status, cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(cu, cu_pad, B, T, cp, bm, bn, cap_q, cap_kv, want,
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(cu, cu_pad, B, T, cp, bm, bn, cap_q, cap_kv, want, step_only,
                                                hdr, fwd_items, dq_items, kv_items, status);
   return cudaGetLastError();
 }
