@@ -381,13 +381,12 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const uint64_t q_desc = smem_desc_sw128(q_base, 16, 1024);
         const uint64_t do_desc = smem_desc_sw128(q_base + Cfg::RES_BYTES, 16, 1024);
         const uint32_t slot_base = smem_u32(smem + Cfg::SMEM_SLOT);
-        // per slot: K-major (S, dP) and MN-major (dQ) base descriptors
-        uint64_t slot_k[NSLOT], slot_mn[NSLOT];
-#pragma unroll
-        for (int s2 = 0; s2 < NSLOT; ++s2) {
-          slot_k[s2] = smem_desc_sw128(slot_base + s2 * Cfg::SLOT_BYTES, 16, 1024);
-          slot_mn[s2] = smem_desc_sw128(slot_base + s2 * Cfg::SLOT_BYTES, BN * 128, 1024);
-        }
+        // slot s: K-major (S, dP) and MN-major (dQ) descriptors = base + s * SLOT_BYTES/16
+        const uint64_t slot_k0 = smem_desc_sw128(slot_base, 16, 1024);
+        const uint64_t slot_mn0 = smem_desc_sw128(slot_base, BN * 128, 1024);
+        constexpr uint32_t kSlotStep = Cfg::SLOT_BYTES >> 4;
+        auto slot_k = [&](int s2) { return slot_k0 + s2 * kSlotStep; };
+        auto slot_mn = [&](int s2) { return slot_mn0 + s2 * kSlotStep; };
         ok = mbar_wait(res_full, 0, abort_flag);
         tc_fence_after();
         // S and dP of tile j into buffer j % 2
@@ -398,10 +397,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           const uint32_t buf = tmem + b * Cfg::T_BUF;
           if (!mbar_wait(full + sk, (tk / NSLOT) & 1, abort_flag)) return false;
           tc_fence_after();
-          mma_kk<BM, BN, D>(buf, q_desc, slot_k[sk]);
+          mma_kk<BM, BN, D>(buf, q_desc, slot_k(sk));
           if (!mbar_wait(full + sv, (tv / NSLOT) & 1, abort_flag)) return false;
           tc_fence_after();
-          mma_kk<BM, BN, D>(buf + BN, do_desc, slot_k[sv]);
+          mma_kk<BM, BN, D>(buf + BN, do_desc, slot_k(sv));
           umma_commit(s_full + b);
           umma_commit(empty + sv);
           return true;
@@ -418,7 +417,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tc_fence_after();
           const int sk = (2 * j + 1) % NSLOT;
           const uint32_t a_op = Cfg::SPLIT ? tmem + Cfg::T_A : tmem + b * Cfg::T_BUF;
-          mma_tn<BN, D>(tmem + Cfg::T_ACC, a_op, slot_mn[sk], j > 0);
+          mma_tn<BN, D>(tmem + Cfg::T_ACC, a_op, slot_mn(sk), j > 0);
           umma_commit(empty + sk);
           if (!ahead.done) {
             ok = issue_sp(j_sp++);
@@ -632,12 +631,11 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const uint64_t k_desc = smem_desc_sw128(k_base, 16, 1024);
         const uint64_t v_desc = smem_desc_sw128(k_base + Cfg::RES_BYTES, 16, 1024);
         const uint32_t slot_base = smem_u32(smem + Cfg::SMEM_SLOT);
-        uint64_t slot_k[NSLOT], slot_mn[NSLOT];
-#pragma unroll
-        for (int s2 = 0; s2 < NSLOT; ++s2) {
-          slot_k[s2] = smem_desc_sw128(slot_base + s2 * Cfg::SLOT_BYTES, 16, 1024);
-          slot_mn[s2] = smem_desc_sw128(slot_base + s2 * Cfg::SLOT_BYTES, BN * 128, 1024);
-        }
+        const uint64_t slot_k0 = smem_desc_sw128(slot_base, 16, 1024);
+        const uint64_t slot_mn0 = smem_desc_sw128(slot_base, BN * 128, 1024);
+        constexpr uint32_t kSlotStep = Cfg::SLOT_BYTES >> 4;
+        auto slot_k = [&](int s2) { return slot_k0 + s2 * kSlotStep; };
+        auto slot_mn = [&](int s2) { return slot_mn0 + s2 * kSlotStep; };
         ok = mbar_wait(res_full, 0, abort_flag);
         tc_fence_after();
         auto slot_q = [&](int j) { return (FIRST_IS_Q ? 2 * j : 2 * j + 1); };
@@ -650,11 +648,11 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           const uint32_t buf = tmem + b * Cfg::T_BUF;
           if (!mbar_wait(full + sq, (tq / NSLOT) & 1, abort_flag)) return false;
           tc_fence_after();
-          mma_kk<BM, BN, D>(buf, k_desc, slot_k[sq]);
+          mma_kk<BM, BN, D>(buf, k_desc, slot_k(sq));
           if (DO_DK) {
             if (!mbar_wait(full + sdo, (tdo / NSLOT) & 1, abort_flag)) return false;
             tc_fence_after();
-            mma_kk<BM, BN, D>(buf + BN, v_desc, slot_k[sdo]);
+            mma_kk<BM, BN, D>(buf + BN, v_desc, slot_k(sdo));
           }
           umma_commit(s_full + b);
           if (MODE == KvMode::kDvOnly) umma_commit(empty + sq);     // Q_i done after S^T
@@ -680,8 +678,8 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tc_fence_after();
           const uint32_t a_p = Cfg::SPLIT ? tmem + Cfg::T_AP : buf;
           const uint32_t a_d = Cfg::SPLIT ? tmem + Cfg::T_AD : buf + BN;
-          if (DO_DV) mma_tn<BN, D>(tmem + Cfg::T_DV, a_p, slot_mn[sdo], j > 0);
-          if (DO_DK) mma_tn<BN, D>(tmem + Cfg::T_DK, a_d, slot_mn[sq], j > 0);
+          if (DO_DV) mma_tn<BN, D>(tmem + Cfg::T_DV, a_p, slot_mn(sdo), j > 0);
+          if (DO_DK) mma_tn<BN, D>(tmem + Cfg::T_DK, a_d, slot_mn(sq), j > 0);
           if (MODE != KvMode::kDkOnly) umma_commit(empty + sdo);
           if (MODE != KvMode::kDvOnly) umma_commit(empty + sq);
           if (!ahead.done) {

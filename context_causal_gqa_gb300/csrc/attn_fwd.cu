@@ -16,7 +16,7 @@
 // stride through the list, so the next item's Q load and first S = Q K^T
 // products overlap the current item's last P V product and its epilogue.
 // Roles:
-//   warp 0     TMA producer: Q per item, K/V tiles through an NSTAGE ring
+//   warp 0     TMA producer: Q per item, K and V tiles through single-tile slots
 //   warp 1     MMA issuer (one thread): S = Q K^T (SMEM x SMEM -> TMEM),
 //              O += P V (P from TMEM, V from SMEM -> TMEM)
 //   warp 2     TMEM allocator
@@ -40,19 +40,23 @@ template <int D, int NH>
 struct FwdCfg {
   static constexpr int BN = D == 128 ? 128 : 64;
   static constexpr int SBUF = NH == 1 ? 2 : 1;
-  static constexpr int NSTAGE = 2;
   static constexpr int KCH = D / 64;                       // 64-wide (128-byte) column chunks
   static constexpr int Q_BYTES = kBM * D * 2;              // one head
   static constexpr int KV_BYTES = BN * D * 2;              // one K (or V) tile
+  // K and V tiles stream through NSLOT single-tile slots (K_j at position 2j,
+  // V_j at 2j+1): K_j is released when S_j is done and V_j when P_j V_j is,
+  // so the loads of the next tiles start one iteration earlier than with
+  // paired K/V stages.
+  static constexpr int NSLOT = (227 * 1024 - 2048 - NH * Q_BYTES) / KV_BYTES;
   static constexpr int SMEM_Q = 0;
-  static constexpr int SMEM_K = SMEM_Q + NH * Q_BYTES;
-  static constexpr int SMEM_V = SMEM_K + NSTAGE * KV_BYTES;
-  static constexpr int SMEM_BAR = SMEM_V + NSTAGE * KV_BYTES;
+  static constexpr int SMEM_KV = SMEM_Q + NH * Q_BYTES;
+  static constexpr int SMEM_BAR = SMEM_KV + NSLOT * KV_BYTES;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
   static constexpr int TMEM_HEAD = SBUF * BN + D;
   static constexpr int TMEM_USED = NH * TMEM_HEAD;
   static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : (TMEM_USED <= 256 ? 256 : 512);
   static constexpr int THREADS = 128 + 128 * NH;
+  static_assert(NSLOT >= 4, "at least two tiles in flight");
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM budget");
 };
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using Cfg = FwdCfg<D, NH>;
-  constexpr int BN = Cfg::BN, SBUF = Cfg::SBUF, NSTAGE = Cfg::NSTAGE, KCH = Cfg::KCH;
+  constexpr int BN = Cfg::BN, SBUF = Cfg::SBUF, NSLOT = Cfg::NSLOT, KCH = Cfg::KCH;
 
   const int nhg = p.hq / NH;                           // head groups per item
   const int64_t n_work = static_cast<int64_t>(p.hdr->n_fwd_all) * nhg;
@@ -148,9 +152,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::SMEM_BAR);
   uint64_t* q_full = bars + 0;
   uint64_t* q_free = bars + 1;                         // last S of the item done: Q may be reloaded
-  uint64_t* kv_full = bars + 2;                        // [NSTAGE]
-  uint64_t* kv_empty = kv_full + NSTAGE;               // [NSTAGE]
-  uint64_t* s_full = kv_empty + NSTAGE;                // [NH][SBUF]
+  uint64_t* kv_full = bars + 2;                        // [NSLOT]
+  uint64_t* kv_empty = kv_full + NSLOT;                // [NSLOT]
+  uint64_t* s_full = kv_empty + NSLOT;                 // [NH][SBUF]
   uint64_t* p_full = s_full + NH * SBUF;               // [NH][SBUF]
   uint64_t* o_done = p_full + NH * SBUF;               // [NH]: one phase per P V product
   uint64_t* o_free = o_done + NH;                      // [NH]: the item's O has been read out
@@ -163,7 +167,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_free, 1);
-    for (int s = 0; s < NSTAGE; ++s) {
+    for (int s = 0; s < NSLOT; ++s) {
       mbar_init(kv_full + s, 1);
       mbar_init(kv_empty + s, 1);
     }
@@ -194,11 +198,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int issued[NSTAGE];
-      for (int s = 0; s < NSTAGE; ++s) issued[s] = 0;
+      int issued[NSLOT];
+      for (int s = 0; s < NSLOT; ++s) issued[s] = 0;
       int q_loads = 0;
       bool ok = true;
-      int64_t gkv = 0;                                 // K/V tiles loaded so far by this CTA
+      int64_t u = 0;                                   // K/V tile positions streamed by this CTA
       int item_k = 0;
       for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item_k) {
         const WorkItem it = p.items[w / nhg];
@@ -218,22 +222,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         ++q_loads;
         const int kv_group_row = static_cast<int>((g / p.hpg_kv) * p.T) + tp.seq_start;
-        for (int j = 0; j < tp.ntiles; ++j, ++gkv) {
-          const int st = static_cast<int>(gkv % NSTAGE);
-          if (gkv >= NSTAGE)
-            ok = mbar_wait(kv_empty + st, static_cast<uint32_t>((gkv / NSTAGE) - 1) & 1, abort_flag);
-          if (!ok) break;
+        for (int j = 0; j < tp.ntiles && ok; ++j) {
           int k0, khi;
           bool diag;
           tile_of<BN>(tp, j, &k0, &khi, &diag);
-          mbar_arrive_expect_tx(kv_full + st, 2 * Cfg::KV_BYTES);
-          for (int kc = 0; kc < KCH; ++kc) {
-            tma_load_3d(smem + Cfg::SMEM_K + st * Cfg::KV_BYTES + kc * BN * 128, &tm_k, kc * 64,
-                        g % p.hpg_kv, kv_group_row + k0, kv_full + st);
-            tma_load_3d(smem + Cfg::SMEM_V + st * Cfg::KV_BYTES + kc * BN * 128, &tm_v, kc * 64,
-                        g % p.hpg_kv, kv_group_row + k0, kv_full + st);
+          for (int which = 0; which < 2; ++which, ++u) {          // K_j then V_j
+            const int sl = static_cast<int>(u % NSLOT);
+            if (u >= NSLOT) ok = mbar_wait(kv_empty + sl, static_cast<uint32_t>((u / NSLOT) - 1) & 1, abort_flag);
+            if (!ok) break;
+            mbar_arrive_expect_tx(kv_full + sl, Cfg::KV_BYTES);
+            uint8_t* dst = smem + Cfg::SMEM_KV + sl * Cfg::KV_BYTES;
+            for (int kc = 0; kc < KCH; ++kc)
+              tma_load_3d(dst + kc * BN * 128, which == 0 ? &tm_k : &tm_v, kc * 64, g % p.hpg_kv,
+                          kv_group_row + k0, kv_full + sl);
+            issued[sl]++;
           }
-          issued[st]++;
         }
       }
       if (!ok) {
@@ -243,7 +246,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // never leave a copy in flight into shared memory we are about to release
       volatile int never = 0;
       if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, &never, 200000000ull);
-      for (int s = 0; s < NSTAGE; ++s)
+      for (int s = 0; s < NSLOT; ++s)
         if (issued[s] > 0) mbar_wait(kv_full + s, (issued[s] - 1) & 1, &never, 200000000ull);
     }
   } else if (warp == 1) {
@@ -252,42 +255,48 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
       const uint32_t q_base = smem_u32(smem + Cfg::SMEM_Q);
-      const uint32_t k_base = smem_u32(smem + Cfg::SMEM_K);
-      const uint32_t v_base = smem_u32(smem + Cfg::SMEM_V);
-      uint64_t q_desc[NH], k_desc[NSTAGE], v_desc[NSTAGE];
-#pragma unroll
-      for (int h = 0; h < NH; ++h) q_desc[h] = smem_desc_sw128(q_base + h * Cfg::Q_BYTES, 16, 1024);
-#pragma unroll
-      for (int st = 0; st < NSTAGE; ++st) {
-        k_desc[st] = smem_desc_sw128(k_base + st * Cfg::KV_BYTES, 16, 1024);
-        v_desc[st] = smem_desc_sw128(v_base + st * Cfg::KV_BYTES, BN * 128, 1024);
-      }
-      int64_t gkv = 0;   // K/V tiles consumed (stage ring)
+      const uint32_t kv_base = smem_u32(smem + Cfg::SMEM_KV);
+      // base descriptors in registers; head h / slot sl are constant offsets
+      const uint64_t q_desc0 = smem_desc_sw128(q_base, 16, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(kv_base, 16, 1024);
+      const uint64_t v_desc0 = smem_desc_sw128(kv_base, BN * 128, 1024);
+      constexpr uint32_t kQStep = Cfg::Q_BYTES >> 4, kKVStep = Cfg::KV_BYTES >> 4;
+      int64_t gkv = 0;   // K/V tiles consumed (tile t uses positions 2t and 2t+1)
       int64_t gs = 0;    // S tiles computed (S buffers, P and O barriers)
       bool ok = true;
-      // S_h of the tile with global index t (K/V in stage st) -> buffer t % SBUF
-      auto issue_s = [&](int h, int64_t t, int st) {
+      auto kslot = [&](int64_t kt) { return static_cast<int>((2 * kt) % NSLOT); };
+      auto vslot = [&](int64_t kt) { return static_cast<int>((2 * kt + 1) % NSLOT); };
+      auto wait_slot = [&](int64_t pos) -> bool {
+        const bool r = mbar_wait(kv_full + (pos % NSLOT), static_cast<uint32_t>(pos / NSLOT) & 1, abort_flag);
+        tc_fence_after();
+        return r;
+      };
+      // S_h of the tile with global index t (K in slot sl) -> buffer t % SBUF
+      auto issue_s = [&](int h, int64_t t, int sl) {
         const int buf = static_cast<int>(t % SBUF);
         const uint32_t d_tmem = tmem + h * Cfg::TMEM_HEAD + buf * BN;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          umma_ss(d_tmem, q_desc[h] + kmajor_step(kBM, k), k_desc[st] + kmajor_step(BN, k), idesc_s,
-                  k > 0 ? 1u : 0u);
+          umma_ss(d_tmem, q_desc0 + h * kQStep + kmajor_step(kBM, k), k_desc0 + sl * kKVStep + kmajor_step(BN, k),
+                  idesc_s, k > 0 ? 1u : 0u);
         umma_commit(s_full + h * SBUF + buf);
       };
-      auto issue_pv = [&](int h, int64_t t, int st, bool first) {
+      auto issue_pv = [&](int h, int64_t t, int sl, bool first) {
         const int buf = static_cast<int>(t % SBUF);
         const uint32_t d_tmem = tmem + h * Cfg::TMEM_HEAD + SBUF * BN;
         const uint32_t p_tmem = tmem + h * Cfg::TMEM_HEAD + buf * BN;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          umma_ts(d_tmem, p_tmem + k * 8, v_desc[st] + mnmajor_step(k), idesc_o, (!first || k > 0) ? 1u : 0u);
+          umma_ts(d_tmem, p_tmem + k * 8, v_desc0 + sl * kKVStep + mnmajor_step(k), idesc_o,
+                  (!first || k > 0) ? 1u : 0u);
         umma_commit(o_done + h);
       };
-      auto wait_kv = [&](int64_t t) -> bool {
-        const bool r = mbar_wait(kv_full + (t % NSTAGE), static_cast<uint32_t>(t / NSTAGE) & 1, abort_flag);
-        tc_fence_after();
-        return r;
+      // all NH heads' S of K/V tile kt (global S index t); then K_kt is free
+      auto issue_s_all = [&](int64_t t, int64_t kt) -> bool {
+        if (!wait_slot(2 * kt)) return false;
+        for (int h = 0; h < NH; ++h) issue_s(h, t, kslot(kt));
+        umma_commit(kv_empty + kslot(kt));
+        return true;
       };
       int item_k = 0;
       for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item_k) {
@@ -296,22 +305,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ok = mbar_wait(q_full, item_k & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        // first S of the item
-        ok = wait_kv(gkv);
+        ok = issue_s_all(gs, gkv);                      // first S of the item
         if (!ok) break;
-        for (int h = 0; h < NH; ++h) issue_s(h, gs, static_cast<int>(gkv % NSTAGE));
         if (n == 1) umma_commit(q_free);
         for (int j = 0; j < n && ok; ++j) {
           const int64_t t = gs + j, kt = gkv + j;
-          const int st = static_cast<int>(kt % NSTAGE);
           const bool has_next = j + 1 < n;
-          bool next_ready = false;
           if (SBUF == 2 && has_next) {
-            ok = wait_kv(kt + 1);
+            ok = issue_s_all(t + 1, kt + 1);            // S of the next tile ahead of this P V
             if (!ok) break;
-            next_ready = true;
-            issue_s(0, t + 1, static_cast<int>((kt + 1) % NSTAGE));
-            if (j + 2 == n) umma_commit(q_free);            // that was the item's last S
+            if (j + 2 == n) umma_commit(q_free);        // that was the item's last S
+          }
+          ok = wait_slot(2 * kt + 1);                    // V_kt
+          if (!ok) break;
+          if (SBUF == 1 && has_next) {
+            ok = wait_slot(2 * (kt + 1));                // K of the next tile
+            if (!ok) break;
           }
           for (int h = 0; h < NH && ok; ++h) {
             const int buf = static_cast<int>(t % SBUF);
@@ -323,18 +332,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               if (!ok) break;
             }
             tc_fence_after();
-            issue_pv(h, t, st, j == 0);
-            if (SBUF == 1 && has_next) {
-              if (!next_ready) {
-                ok = wait_kv(kt + 1);
-                if (!ok) break;
-                next_ready = true;
-              }
-              issue_s(h, t + 1, static_cast<int>((kt + 1) % NSTAGE));
-              if (j + 2 == n && h == NH - 1) umma_commit(q_free);
-            }
+            issue_pv(h, t, vslot(kt), j == 0);
+            // one buffer per head: this head's next S goes right behind its P V,
+            // while the other head's softmax keeps the tensor core busy
+            if (SBUF == 1 && has_next) issue_s(h, t + 1, kslot(kt + 1));
           }
-          umma_commit(kv_empty + st);
+          if (!ok) break;
+          umma_commit(kv_empty + vslot(kt));
+          if (SBUF == 1 && has_next) {
+            umma_commit(kv_empty + kslot(kt + 1));
+            if (j + 2 == n) umma_commit(q_free);
+          }
         }
         gs += n;
         gkv += n;
