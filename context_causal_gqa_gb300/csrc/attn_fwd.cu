@@ -39,20 +39,23 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale only past 2^8
 template <int D, int NH>
 struct FwdCfg {
   static constexpr int BN = D == 128 ? 128 : 64;
-  static constexpr int SBUF = NH == 1 ? 2 : 1;
+  // One head per CTA: three S buffers, so S of tile t+2 is issued before the
+  // MMA warp waits for P of tile t (lookahead LA = 2).  Two heads per CTA:
+  // one S buffer per head, the heads' MMAs and softmaxes interleave (LA = 1).
+  static constexpr int SBUF = NH == 1 ? 3 : 1;
+  static constexpr int LA = NH == 1 ? 2 : 1;
   static constexpr int KCH = D / 64;                       // 64-wide (128-byte) column chunks
   static constexpr int Q_BYTES = kBM * D * 2;              // one head
   static constexpr int KV_BYTES = BN * D * 2;              // one K (or V) tile
-  // K and V tiles stream through NSLOT single-tile slots (K_j at position 2j,
-  // V_j at 2j+1): K_j is released when S_j is done and V_j when P_j V_j is,
-  // so the loads of the next tiles start one iteration earlier than with
-  // paired K/V stages.
+  // K and V tiles stream through NSLOT single-tile slots in the order the MMA
+  // warp consumes them (per item: K_0..K_{LA-1}, then K_{j+LA} and V_j for
+  // j = 0, 1, ...); a slot is released when its S or P V product is done.
   static constexpr int NSLOT = (227 * 1024 - 2048 - NH * Q_BYTES) / KV_BYTES;
   static constexpr int SMEM_Q = 0;
   static constexpr int SMEM_KV = SMEM_Q + NH * Q_BYTES;
   static constexpr int SMEM_BAR = SMEM_KV + NSLOT * KV_BYTES;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
-  static constexpr int TMEM_HEAD = SBUF * BN + D;
+  static constexpr int TMEM_HEAD = SBUF * BN + D;  // S buffers, then O
   static constexpr int TMEM_USED = NH * TMEM_HEAD;
   static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : (TMEM_USED <= 256 ? 256 : 512);
   static constexpr int THREADS = 128 + 128 * NH;
@@ -156,8 +159,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   uint64_t* kv_empty = kv_full + NSLOT;                // [NSLOT]
   uint64_t* s_full = kv_empty + NSLOT;                 // [NH][SBUF]
   uint64_t* p_full = s_full + NH * SBUF;               // [NH][SBUF]
-  uint64_t* o_done = p_full + NH * SBUF;               // [NH]: one phase per P V product
-  uint64_t* o_free = o_done + NH;                      // [NH]: the item's O has been read out
+  // [NH][4]: P V product of tile t completes on o_done[h][t % 4].  A wait for
+  // PV(t) is then unambiguous without consuming every phase: when S(t) is
+  // complete, PV(t-3) is too (S is issued at most two tiles ahead of P V), so
+  // the barrier's previous phase (PV(t-4)) has completed and PV(t+4) cannot
+  // have been issued.  The softmax waits only when it must rescale O, and
+  // once per item before reading O out.
+  uint64_t* o_done = p_full + NH * SBUF;
+  uint64_t* o_free = o_done + NH * 4;                  // [NH]: the item's O has been read out
   uint64_t* mma_done = o_free + NH;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -176,7 +185,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(p_full + i, 128);
     }
     for (int h = 0; h < NH; ++h) {
-      mbar_init(o_done + h, 1);
+      for (int i = 0; i < 4; ++i) mbar_init(o_done + h * 4 + i, 1);
       mbar_init(o_free + h, 128);
     }
     mbar_init(mma_done, 1);
@@ -222,21 +231,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         ++q_loads;
         const int kv_group_row = static_cast<int>((g / p.hpg_kv) * p.T) + tp.seq_start;
-        for (int j = 0; j < tp.ntiles && ok; ++j) {
+        auto load = [&](int which, int j) -> bool {          // which: 0 = K_j, 1 = V_j
           int k0, khi;
           bool diag;
           tile_of<BN>(tp, j, &k0, &khi, &diag);
-          for (int which = 0; which < 2; ++which, ++u) {          // K_j then V_j
-            const int sl = static_cast<int>(u % NSLOT);
-            if (u >= NSLOT) ok = mbar_wait(kv_empty + sl, static_cast<uint32_t>((u / NSLOT) - 1) & 1, abort_flag);
-            if (!ok) break;
-            mbar_arrive_expect_tx(kv_full + sl, Cfg::KV_BYTES);
-            uint8_t* dst = smem + Cfg::SMEM_KV + sl * Cfg::KV_BYTES;
-            for (int kc = 0; kc < KCH; ++kc)
-              tma_load_3d(dst + kc * BN * 128, which == 0 ? &tm_k : &tm_v, kc * 64, g % p.hpg_kv,
-                          kv_group_row + k0, kv_full + sl);
-            issued[sl]++;
-          }
+          const int sl = static_cast<int>(u % NSLOT);
+          if (u >= NSLOT && !mbar_wait(kv_empty + sl, static_cast<uint32_t>((u / NSLOT) - 1) & 1, abort_flag))
+            return false;
+          mbar_arrive_expect_tx(kv_full + sl, Cfg::KV_BYTES);
+          uint8_t* dst = smem + Cfg::SMEM_KV + sl * Cfg::KV_BYTES;
+          for (int kc = 0; kc < KCH; ++kc)
+            tma_load_3d(dst + kc * BN * 128, which == 0 ? &tm_k : &tm_v, kc * 64, g % p.hpg_kv,
+                        kv_group_row + k0, kv_full + sl);
+          issued[sl]++;
+          ++u;
+          return true;
+        };
+        const int n = tp.ntiles;
+        for (int j = 0; j < min(Cfg::LA, n) && ok; ++j) ok = load(0, j);
+        for (int j = 0; j < n && ok; ++j) {
+          if (j + Cfg::LA < n) ok = load(0, j + Cfg::LA);
+          if (ok) ok = load(1, j);
         }
       }
       if (!ok) {
@@ -261,12 +276,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint64_t k_desc0 = smem_desc_sw128(kv_base, 16, 1024);
       const uint64_t v_desc0 = smem_desc_sw128(kv_base, BN * 128, 1024);
       constexpr uint32_t kQStep = Cfg::Q_BYTES >> 4, kKVStep = Cfg::KV_BYTES >> 4;
-      int64_t gkv = 0;   // K/V tiles consumed (tile t uses positions 2t and 2t+1)
+      int64_t u = 0;     // K/V stream positions consumed (same order as the producer's)
       int64_t gs = 0;    // S tiles computed (S buffers, P and O barriers)
       bool ok = true;
-      auto kslot = [&](int64_t kt) { return static_cast<int>((2 * kt) % NSLOT); };
-      auto vslot = [&](int64_t kt) { return static_cast<int>((2 * kt + 1) % NSLOT); };
-      auto wait_slot = [&](int64_t pos) -> bool {
+      auto wait_pos = [&](int64_t pos) -> bool {
         const bool r = mbar_wait(kv_full + (pos % NSLOT), static_cast<uint32_t>(pos / NSLOT) & 1, abort_flag);
         tc_fence_after();
         return r;
@@ -289,13 +302,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int k = 0; k < BN / 16; ++k)
           umma_ts(d_tmem, p_tmem + k * 8, v_desc0 + sl * kKVStep + mnmajor_step(k), idesc_o,
                   (!first || k > 0) ? 1u : 0u);
-        umma_commit(o_done + h);
+        umma_commit(o_done + h * 4 + static_cast<int>(t % 4));
       };
-      // all NH heads' S of K/V tile kt (global S index t); then K_kt is free
-      auto issue_s_all = [&](int64_t t, int64_t kt) -> bool {
-        if (!wait_slot(2 * kt)) return false;
-        for (int h = 0; h < NH; ++h) issue_s(h, t, kslot(kt));
-        umma_commit(kv_empty + kslot(kt));
+      // all NH heads' S of tile t, K at the next stream position; then K is free
+      auto issue_s_all = [&](int64_t t) -> bool {
+        if (!wait_pos(u)) return false;
+        const int sl = static_cast<int>(u % NSLOT);
+        for (int h = 0; h < NH; ++h) issue_s(h, t, sl);
+        umma_commit(kv_empty + sl);
+        ++u;
         return true;
       };
       int item_k = 0;
@@ -305,23 +320,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ok = mbar_wait(q_full, item_k & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        ok = issue_s_all(gs, gkv);                      // first S of the item
+        const int a = min(Cfg::LA, n);
+        for (int j = 0; j < a && ok; ++j) ok = issue_s_all(gs + j);
         if (!ok) break;
-        if (n == 1) umma_commit(q_free);
+        if (n <= Cfg::LA) umma_commit(q_free);          // every S of the item issued
         for (int j = 0; j < n && ok; ++j) {
-          const int64_t t = gs + j, kt = gkv + j;
-          const bool has_next = j + 1 < n;
-          if (SBUF == 2 && has_next) {
-            ok = issue_s_all(t + 1, kt + 1);            // S of the next tile ahead of this P V
+          const int64_t t = gs + j;
+          const bool ahead = j + Cfg::LA < n;
+          if (SBUF > 1 && ahead) {
+            ok = issue_s_all(t + Cfg::LA);               // S LA tiles ahead of this P V
             if (!ok) break;
-            if (j + 2 == n) umma_commit(q_free);        // that was the item's last S
+            if (j + Cfg::LA == n - 1) umma_commit(q_free);
           }
-          ok = wait_slot(2 * kt + 1);                    // V_kt
+          int64_t k_next = -1;                           // NH = 2: K of the next tile
+          if (SBUF == 1 && ahead) {
+            k_next = u++;
+            ok = wait_pos(k_next);
+            if (!ok) break;
+          }
+          const int64_t vpos = u++;                      // V_j
+          ok = wait_pos(vpos);
           if (!ok) break;
-          if (SBUF == 1 && has_next) {
-            ok = wait_slot(2 * (kt + 1));                // K of the next tile
-            if (!ok) break;
-          }
+          const int vsl = static_cast<int>(vpos % NSLOT);
           for (int h = 0; h < NH && ok; ++h) {
             const int buf = static_cast<int>(t % SBUF);
             ok = mbar_wait(p_full + h * SBUF + buf, static_cast<uint32_t>(t / SBUF) & 1, abort_flag);
@@ -332,20 +352,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               if (!ok) break;
             }
             tc_fence_after();
-            issue_pv(h, t, vslot(kt), j == 0);
+            issue_pv(h, t, vsl, j == 0);
             // one buffer per head: this head's next S goes right behind its P V,
             // while the other head's softmax keeps the tensor core busy
-            if (SBUF == 1 && has_next) issue_s(h, t + 1, kslot(kt + 1));
+            if (SBUF == 1 && ahead) issue_s(h, t + 1, static_cast<int>(k_next % NSLOT));
           }
           if (!ok) break;
-          umma_commit(kv_empty + vslot(kt));
-          if (SBUF == 1 && has_next) {
-            umma_commit(kv_empty + kslot(kt + 1));
+          umma_commit(kv_empty + vsl);
+          if (SBUF == 1 && ahead) {
+            umma_commit(kv_empty + static_cast<int>(k_next % NSLOT));
             if (j + 2 == n) umma_commit(q_free);
           }
         }
         gs += n;
-        gkv += n;
       }
       if (!ok) {
         raise_status(p.status, CCG_ERR_TIMEOUT);
@@ -438,15 +457,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         tmem_wait_st();
         l = l * alpha + psum;
-        // consume the previous P V product's completion (every phase, in order,
-        // so that parity waits stay unambiguous); it is needed before O may be
-        // rescaled and costs nothing when it has already landed
-        if (j > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(o_done + h, static_cast<uint32_t>(t - 1) & 1, abort_flag));
+        // rescale the running O (rare: the reference max grew past the
+        // threshold) once the previous P V product has landed
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const int64_t tp1 = t - 1;                     // alpha != 1 implies j > 0
+          ok = __all_sync(0xffffffffu, mbar_wait(o_done + h * 4 + static_cast<int>(tp1 % 4),
+                                                 static_cast<uint32_t>(tp1 / 4) & 1, abort_flag));
           if (!ok) break;
           tc_fence_after();
-        }
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
           uint32_t r[32];
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
@@ -462,7 +480,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_arrive(p_full + h * SBUF + buf);
       }
       if (!ok) break;
-      ok = __all_sync(0xffffffffu, mbar_wait(o_done + h, static_cast<uint32_t>(gs + n - 1) & 1, abort_flag));
+      const int64_t t_last = gs + n - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(o_done + h * 4 + static_cast<int>(t_last % 4),
+                                             static_cast<uint32_t>(t_last / 4) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       // read O out of TMEM, then release it for the next item's first P V

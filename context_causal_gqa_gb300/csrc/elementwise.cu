@@ -24,22 +24,41 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
   }
 }
 
+// Cached lookup of the sequence holding physical row t: rows handled by one
+// thread are ascending, so the binary search runs only when t leaves the
+// cached sequence.
+struct SeqCache {
+  int64_t lo = 1, hi = 0;   // empty
+  int b = 0;
+  __device__ __forceinline__ int get(const int32_t* cu_pad, int B, int64_t t) {
+    if (t < lo || t >= hi) {
+      b = find_sequence(cu_pad, B, t);
+      lo = __ldg(cu_pad + b);
+      hi = __ldg(cu_pad + b + 1);
+    }
+    return b;
+  }
+};
+
+// Each block merges a contiguous range of rows (better DRAM locality and a
+// cached sequence lookup); TPR threads per row, 16 bytes each.
 template <int TPR>
-__global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a) {
+__global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a, int64_t rows_per_block) {
   if (a.status != nullptr && status_bad(a.status)) return;
   const int sub = threadIdx.x % TPR;
-  const int64_t rows_per_block = 256 / TPR;
-  const int64_t row0 = blockIdx.x * rows_per_block + threadIdx.x / TPR;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * rows_per_block;
-  for (int64_t r = row0; r < a.rows; r += stride) {
+  constexpr int kRowsPerPass = 256 / TPR;
+  const int64_t r_begin = blockIdx.x * rows_per_block;
+  const int64_t r_end = min(a.rows, r_begin + rows_per_block);
+  SeqCache sc;
+  for (int64_t r = r_begin + threadIdx.x / TPR; r < r_end; r += kRowsPerPass) {
     int K = a.nparts;
     bool valid = true;
     if (a.cu_pad != nullptr) {
       const int64_t t = (r / a.hpg) % a.T;
-      const int b = find_sequence(a.cu_pad, a.B, t);
-      const int start = __ldg(a.cu_pad + b);
+      const int b = sc.get(a.cu_pad, a.B, t);
+      const int start = static_cast<int>(sc.lo);
       const int pos = static_cast<int>(t - start);
-      const int L = (__ldg(a.cu_pad + b + 1) - start) / (2 * a.cp);
+      const int L = (static_cast<int>(sc.hi) - start) / (2 * a.cp);
       const int S = __ldg(a.cu + b + 1) - __ldg(a.cu + b);
       valid = pos < S;
       const int c = L > 0 ? pos / L : 0;
@@ -59,6 +78,12 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a) {
       outv = make_uint4(0, 0, 0, 0);
       lse_out = -INFINITY;
     } else {
+      // issue every partial's load before using any of them
+      uint4 u[kMaxCP];
+#pragma unroll
+      for (int s = 0; s < kMaxCP; ++s)
+        if (s < K && l[s] != -INFINITY)
+          u[s] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o_parts[s]) + off));
       float sigma = 0.f;
 #pragma unroll
       for (int s = 0; s < kMaxCP; ++s)
@@ -69,9 +94,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a) {
       for (int s = 0; s < kMaxCP; ++s) {
         if (s < K && l[s] != -INFINITY) {
           const float w = ex2_approx((l[s] - lse_out) * kLog2e);
-          const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o_parts[s]) + off));
           float f[8];
-          bf16x8_to_f32(u, f);
+          bf16x8_to_f32(u[s], f);
 #pragma unroll
           for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
         }
@@ -109,48 +133,41 @@ bwd_dot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restr
   }
 }
 
-// Rank-major row of sequence-order physical row t (load-balanced split).
-__device__ __forceinline__ int64_t rank_major_row(const int32_t* cu_pad, int B, int64_t T, int cp,
-                                                  int64_t t, bool* ok) {
-  const int C = 2 * cp;
-  const int b = find_sequence(cu_pad, B, t);
-  const int start = __ldg(cu_pad + b);
-  const int P = __ldg(cu_pad + b + 1) - start;
-  if (P % C != 0 || P <= 0) {
-    *ok = false;
-    return 0;
-  }
-  const int L = P / C;
-  const int pos = static_cast<int>(t - start);
-  const int c = pos / L, i = pos % L;
-  const int r = chunk_owner(c, cp);
-  *ok = true;
-  return static_cast<int64_t>(r) * (T / cp) + start / cp + (c == r ? 0 : L) + i;
-}
-
-// One warp per (head group g, sequence row t): copies hpg*D contiguous
-// 16-bit elements between the rank-major row and the head-split row.
+// One warp per (head group g, sequence row t), each warp walking a contiguous
+// range of such rows: copies hpg*D contiguous 16-bit elements between the
+// rank-major row and the head-split row.  Rank-major row of sequence row t:
+// rank r = owner of t's chunk; r*T/CP + start_b/CP + (chunk is r ? 0 : L_b) + i.
 template <bool kPack>
 __global__ void __launch_bounds__(256)
 thd_permute_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                    const int32_t* __restrict__ cu_pad, int B, int64_t T, int H, int D, int cp,
-                   int32_t* status) {
+                   int64_t rows_per_warp, int32_t* status) {
   if (status_bad(status)) return;
   const int lane = threadIdx.x & 31;
+  const int C = 2 * cp;
   const int hpg = H / cp;
   const int64_t w16 = static_cast<int64_t>(hpg) * D / 8;   // uint4 per head-split row
   const int64_t row_w16 = static_cast<int64_t>(H) * D / 8;  // uint4 per rank-major row
   const int64_t nrows = static_cast<int64_t>(cp) * T;
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < nrows; w += warps) {
+  const int64_t warp_id = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t w_begin = warp_id * rows_per_warp;
+  const int64_t w_end = min(nrows, w_begin + rows_per_warp);
+  SeqCache sc;
+  for (int64_t w = w_begin; w < w_end; ++w) {
     const int g = static_cast<int>(w / T);
     const int64_t t = w % T;
-    bool ok;
-    const int64_t pr = rank_major_row(cu_pad, B, T, cp, t, &ok);
-    if (!ok) {
+    sc.get(cu_pad, B, t);
+    const int start = static_cast<int>(sc.lo);
+    const int P = static_cast<int>(sc.hi) - start;
+    if (P % C != 0 || P <= 0) {
       if (lane == 0) raise_status(status, CCG_ERR_SEQLENS);
       return;
     }
+    const int L = P / C;
+    const int pos = static_cast<int>(t - start);
+    const int c = pos / L, i = pos % L;
+    const int r = chunk_owner(c, cp);
+    const int64_t pr = static_cast<int64_t>(r) * (T / cp) + start / cp + (c == r ? 0 : L) + i;
     const uint4* s;
     uint4* d;
     if (kPack) {
@@ -160,7 +177,15 @@ thd_permute_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
       s = src + w * w16;
       d = dst + pr * row_w16 + static_cast<int64_t>(g) * w16;
     }
-    for (int64_t u = lane; u < w16; u += 32) d[u] = __ldg(s + u);
+    int64_t u = lane;
+    for (; u + 96 < w16; u += 128) {             // four 16-byte loads in flight per lane
+      const uint4 x0 = __ldg(s + u), x1 = __ldg(s + u + 32), x2 = __ldg(s + u + 64), x3 = __ldg(s + u + 96);
+      d[u] = x0;
+      d[u + 32] = x1;
+      d[u + 64] = x2;
+      d[u + 96] = x3;
+    }
+    for (; u < w16; u += 32) d[u] = __ldg(s + u);
   }
 }
 
@@ -176,8 +201,9 @@ int grid_for(int64_t units, int per_block, int max_blocks) {
 cudaError_t launch_lse_merge(const MergeArgs& a, int num_sms, cudaStream_t stream) {
   const int tpr = a.D / 8;
   const int grid = grid_for(a.rows, 256 / tpr, num_sms * 16);
-  if (tpr == 16) lse_merge_kernel<16><<<grid, 256, 0, stream>>>(a);
-  else if (tpr == 32) lse_merge_kernel<32><<<grid, 256, 0, stream>>>(a);
+  const int64_t rpb = (a.rows + grid - 1) / grid;
+  if (tpr == 16) lse_merge_kernel<16><<<grid, 256, 0, stream>>>(a, rpb);
+  else if (tpr == 32) lse_merge_kernel<32><<<grid, 256, 0, stream>>>(a, rpb);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
@@ -199,10 +225,12 @@ cudaError_t launch_thd_permute(bool pack, const void* src, void* dst, const int3
                                cudaStream_t stream) {
   const int64_t nrows = static_cast<int64_t>(cp) * T;
   const int grid = grid_for(nrows, 8, num_sms * 16);
+  const int64_t warps = static_cast<int64_t>(grid) * 8;
+  const int64_t rpw = (nrows + warps - 1) / warps;
   auto* s = static_cast<const uint4*>(src);
   auto* d = static_cast<uint4*>(dst);
-  if (pack) thd_permute_kernel<true><<<grid, 256, 0, stream>>>(s, d, cu_pad, B, T, H, D, cp, status);
-  else thd_permute_kernel<false><<<grid, 256, 0, stream>>>(s, d, cu_pad, B, T, H, D, cp, status);
+  if (pack) thd_permute_kernel<true><<<grid, 256, 0, stream>>>(s, d, cu_pad, B, T, H, D, cp, rpw, status);
+  else thd_permute_kernel<false><<<grid, 256, 0, stream>>>(s, d, cu_pad, B, T, H, D, cp, rpw, status);
   return cudaGetLastError();
 }
 
