@@ -84,7 +84,8 @@ def kernel_work(w):
     tq = T * hq * D * 2
     tkv = T * hkv * D * 2
     work = {
-        "attn_fwd": ("tensor", 2.0 * U),            # all ring-step partials, one launch
+        "attn_fwd": ("tensor", 2.0 * U),            # all ring-step partials (or fused), one launch
+        "pad_rows": ("hbm", 0.0),
         "attn_bwd_dq": ("tensor", 3.0 * U),        # S, dP and dQ
         "attn_bwd_dv": ("tensor", 1.0 * U),
         "attn_bwd_dk": ("tensor", 1.0 * U),
@@ -254,7 +255,7 @@ def run_ccg(args):
     ccg.load()
     w = get_workload(args.workload)
     x = W.make_inputs(w, device=dev, seed=w.seed + 1000 * rank)
-    step = AttentionStep(w, x, device=dev)
+    step = AttentionStep(w, x, device=dev, schedule=args.schedule, fused=args.fwd == "fused")
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         step.run()
@@ -371,6 +372,8 @@ def run_ccg(args):
                            f"D{w.head_dim}, causal, {w.cp} emulated CP ranks ({2 * w.cp} chunks)"
                            + (", A2A head-split pack/unpack round trip" if w.pack_roundtrip else ""))
         cfg["l2"] = "inputs larger than L2, no flush"
+        cfg["schedule"] = args.schedule
+        cfg["forward"] = "fused online softmax" if step.fused else "ring-step partials + LSE merge"
         cfg["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU, CP emulated"
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(ms_max, 3), "higher_is_better": True,
@@ -401,6 +404,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ccg", choices=["ccg", "reference"])
     ap.add_argument("--workload", default="large", choices=list(W.WORKLOADS) + list(EXTRA))
+    ap.add_argument("--schedule", default="ring", choices=["ring", "a2a"],
+                    help="ring: CP-emulated ring (the measured path); a2a: A2A head-split schedule")
+    ap.add_argument("--fwd", default="partials", choices=["partials", "fused"],
+                    help="partials: ring-step partials + LSE merge (the measured path); fused: one online softmax")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -53,8 +53,9 @@ def make_desc(batch, hq, hkv, head_dim, cp, total_tokens, head_groups=1, scale=0
                     head_groups=head_groups, reserved=0, total_tokens=total_tokens, softmax_scale=scale)
 
 
-def workspace_size(desc, is_bwd):
-    return int(load().ccg_workspace_size(ctypes.byref(desc), 1 if is_bwd else 0))
+def workspace_size(desc, kind):
+    """kind: 0 / False forward, 1 / True backward, 2 fused forward."""
+    return int(load().ccg_workspace_size(ctypes.byref(desc), int(kind)))
 
 
 class Workspace:
@@ -91,19 +92,20 @@ def _desc_for(q, k, cu_seqlens, cp, head_groups, scale):
 
 
 def attn_fwd(q, k, v, cu_seqlens, cu_seqlens_padded, cp, *, head_groups=1, scale=0.0, out=None, lse=None,
-             workspace=None, status=None, stream=None, check=True):
-    """Forward: returns (o, lse).  q [T,Hq,D] (or [G,T,Hq/G,D]), k/v likewise, bf16 on cuda."""
+             workspace=None, status=None, stream=None, check=True, fused=False):
+    """Forward: returns (o, lse).  q [T,Hq,D] (or [G,T,Hq/G,D]), k/v likewise, bf16 on cuda.
+    fused=True runs ccg_attn_fwd_fused (one online softmax over all ring steps)."""
     import torch
     desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale)
     o = torch.empty_like(q) if out is None else out
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     ws = workspace or Workspace(q.device)
-    wptr, wbytes = ws.get(workspace_size(desc, False))
+    wptr, wbytes = ws.get(workspace_size(desc, 2 if fused else 0))
     st = _new_status(q.device) if status is None else status
-    _check(load().ccg_attn_fwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens),
-                               _ptr(cu_seqlens_padded), _ptr(o), _ptr(lse), wptr, wbytes, _ptr(st),
-                               _stream(stream)), "ccg_attn_fwd")
+    fn = load().ccg_attn_fwd_fused if fused else load().ccg_attn_fwd
+    _check(fn(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(cu_seqlens_padded), _ptr(o),
+              _ptr(lse), wptr, wbytes, _ptr(st), _stream(stream)), "ccg_attn_fwd_fused" if fused else "ccg_attn_fwd")
     if check:
         _check(get_status(st, stream), "ccg_attn_fwd (device)")
     return o, lse

@@ -19,6 +19,8 @@ SIGNATURES = {
     "ccg_workspace_size": (c_sz, [ctypes.POINTER(AttnDesc), ctypes.c_int]),
     "ccg_attn_fwd": (ctypes.c_int, [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                     c_vp, c_sz, c_vp, c_vp]),
+    "ccg_attn_fwd_fused": (ctypes.c_int, [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                          c_vp, c_sz, c_vp, c_vp]),
     "ccg_attn_fwd_step": (ctypes.c_int, [ctypes.POINTER(AttnDesc), c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
                                          c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "ccg_attn_bwd": (ctypes.c_int, [ctypes.POINTER(AttnDesc), c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
@@ -32,6 +34,7 @@ SIGNATURES = {
     "ccg_thd_pack": (ctypes.c_int, [c_vp, c_vp, c_i32, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
     "ccg_thd_unpack": (ctypes.c_int, [c_vp, c_vp, c_i32, c_i64, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
     "ccg_get_status": (ctypes.c_int, [c_vp, c_vp]),
+    "ccg_selftest_bounded_wait": (ctypes.c_int, [c_vp, ctypes.c_uint32, c_vp]),
     "ccg_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "ccg_last_launch_count": (c_i32, []),
     "ccg_profile_begin": (ctypes.c_int, [c_i32]),

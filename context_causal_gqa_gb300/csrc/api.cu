@@ -29,7 +29,9 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
                             const int32_t* cu_pad, void* o, float* lse, int64_t o_slab, int64_t lse_slab,
                             int32_t* status, int cp, int hq, int hkv, int head_groups, int64_t T, int D,
-                            float scale, int num_sms, cudaStream_t stream);
+                            float scale, int fused, int num_sms, cudaStream_t stream);
+cudaError_t launch_pad_rows(void* o, float* lse, const int32_t* cu, const int32_t* cu_pad, int B, int64_t T,
+                            int H, int hpg, int D, const int32_t* status, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items,
                             const WorkItem* kv_items, const PlanHeader* hdr, const int32_t* cu,
                             const int32_t* cu_pad, const float* lse, const float* delta, void* dq,
@@ -41,6 +43,7 @@ int bwd_q_tile_rows(int D);
 int bwd_map_rows(int which, int D);
 
 cudaError_t launch_lse_merge(const MergeArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_bounded_wait_selftest(int32_t* status, uint32_t limit_us, cudaStream_t stream);
 
 }  // namespace ccg
 
@@ -104,7 +107,7 @@ ccg_status check_desc(const ccg_attn_desc* d) {
   if (d->head_dim != 128 && d->head_dim != 256) return CCG_ERR_UNSUPPORTED;
   if (d->hq % d->hkv != 0) return CCG_ERR_UNSUPPORTED;
   if (d->cp < 1 || d->cp > kMaxCP) return CCG_ERR_UNSUPPORTED;
-  if (d->head_groups != 1 && d->head_groups != d->cp) return CCG_ERR_UNSUPPORTED;
+  if (d->head_groups < 1) return CCG_ERR_INVALID_ARG;
   if (d->hq % d->head_groups != 0 || d->hkv % d->head_groups != 0) return CCG_ERR_UNSUPPORTED;
   if (d->total_tokens % (2 * d->cp) != 0) return CCG_ERR_UNSUPPORTED;
   // 32-bit coordinates inside the kernels and TMA maps
@@ -124,7 +127,11 @@ struct Layout {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-Layout workspace_layout(const ccg_attn_desc* d, int is_bwd) {
+// kind: 0 forward (plan + CP partials), 1 backward (plan + Delta), 2 fused
+// forward (plan only).
+Layout workspace_layout(const ccg_attn_desc* d, int kind) {
+  const int is_bwd = kind == 1;
+  const bool partials = kind == 0;
   Layout L{};
   const int64_t C = 2 * d->cp;
   L.cap_q = static_cast<int>(d->total_tokens / kQTile + d->batch * C + 1);
@@ -140,9 +147,9 @@ Layout workspace_layout(const ccg_attn_desc* d, int is_bwd) {
   off = align_up(off + (is_bwd ? size_t(L.cap_kv) * sizeof(WorkItem) : 0), 256);
   const size_t rows = size_t(d->total_tokens) * d->hq;
   L.o_parts = off;
-  off = align_up(off + (is_bwd ? 0 : size_t(d->cp) * rows * d->head_dim * 2), 256);
+  off = align_up(off + (partials ? size_t(d->cp) * rows * d->head_dim * 2 : 0), 256);
   L.lse_parts = off;
-  off = align_up(off + (is_bwd ? 0 : size_t(d->cp) * rows * 4), 256);
+  off = align_up(off + (partials ? size_t(d->cp) * rows * 4 : 0), 256);
   L.delta = off;
   off = align_up(off + (is_bwd ? rows * 4 : 0), 256);
   L.total = off;
@@ -196,12 +203,12 @@ bool make_thd_map(CUtensorMap* m, const void* base, int D, int hpg, int64_t rows
 
 ccg_status fwd_prepare(const ccg_attn_desc* d, const void* q, const void* k, const void* v,
                        const int32_t* cu, const int32_t* cu_pad, void* workspace, size_t ws_bytes,
-                       int32_t* status, Layout* L) {
+                       int32_t* status, Layout* L, int kind = 0) {
   ccg_status st = check_desc(d);
   if (st != CCG_OK) return st;
   if (!q || !k || !v || !cu || !cu_pad || !status) return CCG_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return CCG_ERR_ALIGNMENT;
-  *L = workspace_layout(d, 0);
+  *L = workspace_layout(d, kind);
   if (workspace == nullptr || ws_bytes < L->total) return CCG_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CCG_ERR_ALIGNMENT;
   return CCG_OK;
@@ -211,9 +218,10 @@ ccg_status fwd_prepare(const ccg_attn_desc* d, const void* q, const void* k, con
 
 extern "C" {
 
-size_t ccg_workspace_size(const ccg_attn_desc* desc, int is_bwd) {
+size_t ccg_workspace_size(const ccg_attn_desc* desc, int kind) {
   if (check_desc(desc) != CCG_OK) return 0;
-  return workspace_layout(desc, is_bwd ? 1 : 0).total;
+  if (kind < 0 || kind > 2) return 0;
+  return workspace_layout(desc, kind).total;
 }
 
 const char* ccg_status_str(ccg_status s) {
@@ -262,6 +270,17 @@ ccg_status ccg_profile_get(int32_t i, const char** kernel_name, float* ms) {
   if (cudaEventSynchronize(p.ev[2 * i + 1]) != cudaSuccess) return CCG_ERR_CUDA;
   if (cudaEventElapsedTime(ms, p.ev[2 * i], p.ev[2 * i + 1]) != cudaSuccess) return CCG_ERR_CUDA;
   *kernel_name = p.names[i];
+  return CCG_OK;
+}
+
+ccg_status ccg_selftest_bounded_wait(int32_t* d_status, uint32_t limit_us, ccg_stream_t stream) {
+  int launches = 0;
+  g_last_launches = 0;
+  if (d_status == nullptr) return CCG_ERR_INVALID_ARG;
+  if (limit_us < 1 || limit_us > 1000000) return CCG_ERR_INVALID_ARG;
+  CCG_LAUNCH("selftest_bounded_wait", reinterpret_cast<cudaStream_t>(stream),
+             launch_bounded_wait_selftest(d_status, limit_us, reinterpret_cast<cudaStream_t>(stream)));
+  g_last_launches = launches;
   return CCG_OK;
 }
 
@@ -370,14 +389,15 @@ ccg_status ccg_thd_unpack(const void* in_head_split, const int32_t* cu_seqlens_p
 static ccg_status fwd_partials(const ccg_attn_desc* d, int step_only, const void* q, const void* k,
                                const void* v, const int32_t* cu, const int32_t* cu_pad, void* o_part,
                                int64_t o_slab, float* lse_part, int64_t lse_slab, void* workspace,
-                               const Layout& L, int32_t* status, cudaStream_t s, int* launches_out) {
+                               const Layout& L, int32_t* status, cudaStream_t s, int* launches_out,
+                               int fused = 0) {
   int launches = *launches_out;
   auto* base = static_cast<uint8_t*>(workspace);
   auto* hdr = reinterpret_cast<PlanHeader*>(base + L.hdr);
   auto* items = reinterpret_cast<WorkItem*>(base + L.fwd_items);
   CCG_LAUNCH("plan", s,
-             launch_plan(cu, cu_pad, d->batch, d->total_tokens, d->cp, kQTile, kMinKvTile, L.cap_q, L.cap_kv, 1,
-                         step_only, hdr, items, nullptr, nullptr, status, s));
+             launch_plan(cu, cu_pad, d->batch, d->total_tokens, d->cp, kQTile, kMinKvTile, L.cap_q, L.cap_kv,
+                         fused ? 4 : 1, step_only, hdr, items, nullptr, nullptr, status, s));
   const int hg = d->head_groups;
   const int64_t rows = d->total_tokens * hg;
   const int bn = d->head_dim == 128 ? 128 : 64;
@@ -388,8 +408,8 @@ static ccg_status fwd_partials(const ccg_attn_desc* d, int step_only, const void
     return CCG_ERR_CUDA;
   CCG_LAUNCH("attn_fwd", s,
              launch_attn_fwd(tq, tk, tv, items, hdr, cu, cu_pad, o_part, lse_part, o_slab, lse_slab, status, d->cp,
-                             d->hq, d->hkv, hg, d->total_tokens, d->head_dim, softmax_scale(d), num_sms_cached(),
-                             s));
+                             d->hq, d->hkv, hg, d->total_tokens, d->head_dim, softmax_scale(d), fused,
+                             num_sms_cached(), s));
   *launches_out = launches;
   return CCG_OK;
 }
@@ -452,6 +472,29 @@ ccg_status ccg_attn_fwd(const ccg_attn_desc* desc, const void* q, const void* k,
   a.D = desc->head_dim;
   a.status = d_status;
   CCG_LAUNCH("lse_merge", s, launch_lse_merge(a, num_sms_cached(), s));
+  g_last_launches = launches;
+  return CCG_OK;
+}
+
+ccg_status ccg_attn_fwd_fused(const ccg_attn_desc* desc, const void* q, const void* k, const void* v,
+                              const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded, void* o, float* lse,
+                              void* workspace, size_t workspace_bytes, int32_t* d_status, ccg_stream_t stream) {
+  g_last_launches = 0;
+  Layout L;
+  ccg_status st = fwd_prepare(desc, q, k, v, cu_seqlens, cu_seqlens_padded, workspace, workspace_bytes,
+                              d_status, &L, 2);
+  if (st != CCG_OK) return st;
+  if (!o || !lse) return CCG_ERR_INVALID_ARG;
+  if (!aligned16(o)) return CCG_ERR_ALIGNMENT;
+  if (desc->total_tokens == 0) return CCG_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int launches = 0;
+  st = fwd_partials(desc, -1, q, k, v, cu_seqlens, cu_seqlens_padded, o, 0, lse, 0, workspace, L, d_status, s,
+                    &launches, 1);
+  if (st != CCG_OK) return st;
+  CCG_LAUNCH("pad_rows", s,
+             launch_pad_rows(o, lse, cu_seqlens, cu_seqlens_padded, desc->batch, desc->total_tokens, desc->hq,
+                             desc->hq / desc->head_groups, desc->head_dim, d_status, num_sms_cached(), s));
   g_last_launches = launches;
   return CCG_OK;
 }

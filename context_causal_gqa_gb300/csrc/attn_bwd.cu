@@ -127,11 +127,17 @@ struct KvCfg {
 template <int BN>
 struct DqIter {
   int cp, r, cq, L, S, q_valid_hi;
-  int s, nv, vi, vis[2], t, ntile, kv_lo, kv_hi;
+  int s, nv, vi, vis0, vis1, t, ntile, kv_lo, kv_hi;   // vis0/vis1: no indexed array (stays in registers)
   bool diag, done;
 
+  __device__ void load_vis() {
+    int v[2];
+    nv = visible_kv_chunks(cq, ring_source(r, s, cp), cp, v);
+    vis0 = v[0];
+    vis1 = v[1];
+  }
   __device__ void load_segment() {
-    const int j = vis[vi];
+    const int j = vi == 0 ? vis0 : vis1;
     diag = (j == cq);
     kv_lo = j * L;
     kv_hi = min((j + 1) * L, S);
@@ -149,7 +155,7 @@ struct DqIter {
       }
       ++s;
       if (s >= cp) { done = true; return; }
-      nv = visible_kv_chunks(cq, ring_source(r, s, cp), cp, vis);
+      load_vis();
       vi = 0;
       if (nv > 0) load_segment();
     }
@@ -158,7 +164,8 @@ struct DqIter {
     cp = cp_; cq = cq_; r = chunk_owner(cq_, cp_); L = L_; S = S_; q_valid_hi = q_valid_hi_;
     done = q_valid_hi <= q_lo;       // no real query row in this tile
     s = 0;
-    nv = visible_kv_chunks(cq, ring_source(r, 0, cp), cp, vis);
+    vis0 = vis1 = 0;
+    load_vis();
     vi = 0;
     ntile = 0;
     t = 0;

@@ -76,65 +76,95 @@ struct FwdParams {
   int cp, hq, hkv, hpg_q, hpg_kv;
   int64_t T;
   float scale_log2;
+  int fused;                    // 1: every ring step of the rank in one online softmax (no partials)
 };
 
-// KV tiles of one work item: up to two segments (KV chunks of the source
-// rank), each [lo, hi) in sequence positions; `diag` marks the causal chunk.
-struct TilePlan {
-  int q_lo, q_hi;               // rows [q_lo, q_hi) are written
-  int nseg;
-  int seg_lo[2], seg_hi[2], seg_tiles[2];
-  bool seg_diag[2];
-  int ntiles;
+// The query rows of one work item.
+struct ItemRows {
+  int q_lo, q_hi;               // rows [q_lo, q_hi) are written (real tokens of the tile)
   int seq_start;
 };
 
-template <int BN>
-__device__ __forceinline__ TilePlan make_tile_plan(const FwdParams& p, const WorkItem& it) {
-  TilePlan tp;
-  const int C = 2 * p.cp;
+__device__ __forceinline__ ItemRows item_rows(const FwdParams& p, const WorkItem& it) {
+  ItemRows ir;
   const int start = __ldg(p.cu_pad + it.b);
   const int S = __ldg(p.cu + it.b + 1) - __ldg(p.cu + it.b);
-  const int L = (__ldg(p.cu_pad + it.b + 1) - start) / C;
-  tp.seq_start = start;
-  tp.q_lo = it.c * L + it.tile * kBM;
-  tp.q_hi = min(min(tp.q_lo + kBM, (it.c + 1) * L), S);
-  int vis[2];
-  const int src = ring_source(chunk_owner(it.c, p.cp), it.step, p.cp);
-  tp.nseg = visible_kv_chunks(it.c, src, p.cp, vis);
-  tp.ntiles = 0;
-  for (int i = 0; i < 2; ++i) {
-    if (i < tp.nseg) {
-      const int j = vis[i];
-      tp.seg_diag[i] = (j == it.c);
-      tp.seg_lo[i] = j * L;
-      int hi = min((j + 1) * L, S);
-      if (tp.seg_diag[i]) hi = min(hi, tp.q_hi);   // keys past the last row are invisible
-      tp.seg_hi[i] = hi;
-      tp.seg_tiles[i] = hi > tp.seg_lo[i] ? (hi - tp.seg_lo[i] + BN - 1) / BN : 0;
-    } else {
-      tp.seg_diag[i] = false;
-      tp.seg_lo[i] = tp.seg_hi[i] = 0;
-      tp.seg_tiles[i] = 0;
-    }
-    tp.ntiles += tp.seg_tiles[i];
-  }
-  return tp;
+  const int L = (__ldg(p.cu_pad + it.b + 1) - start) / (2 * p.cp);
+  ir.seq_start = start;
+  ir.q_lo = it.c * L + it.tile * kBM;
+  ir.q_hi = min(min(ir.q_lo + kBM, (it.c + 1) * L), S);
+  return ir;
 }
 
-// Sequence position of the first key of tile j, its segment end and kind.
+// KV tiles one work item attends, in ring order: for each ring step of the
+// item (its own step, or every step of its rank when fused), the source
+// rank's KV chunks the query chunk can see, ascending; tiles ascending.  On
+// the diagonal chunk, keys past the item's last real row are skipped.
 template <int BN>
-__device__ __forceinline__ void tile_of(const TilePlan& tp, int j, int* k0, int* khi, bool* diag) {
-  if (j < tp.seg_tiles[0]) {
-    *k0 = tp.seg_lo[0] + j * BN;
-    *khi = tp.seg_hi[0];
-    *diag = tp.seg_diag[0];
-  } else {
-    j -= tp.seg_tiles[0];
-    *k0 = tp.seg_lo[1] + j * BN;
-    *khi = tp.seg_hi[1];
-    *diag = tp.seg_diag[1];
+struct KvTileIter {
+  int cp, cq, r, L, S, q_hi, s, s_end, nv, vi, vis0, vis1, t, ntile, lo, hi;
+  bool diag, done;
+
+  __device__ void load_vis() {
+    int v[2];
+    nv = visible_kv_chunks(cq, ring_source(r, s, cp), cp, v);
+    vis0 = v[0];
+    vis1 = v[1];
   }
+  __device__ void load_segment() {
+    const int j = vi == 0 ? vis0 : vis1;
+    diag = (j == cq);
+    lo = j * L;
+    hi = min((j + 1) * L, S);
+    if (diag) hi = min(hi, q_hi);
+    ntile = hi > lo ? (hi - lo + BN - 1) / BN : 0;
+    t = 0;
+  }
+  __device__ void settle() {
+    while (!done) {
+      if (vi < nv && t < ntile) return;
+      if (vi < nv) {
+        ++vi;
+        if (vi < nv) { load_segment(); continue; }
+      }
+      if (++s > s_end) { done = true; return; }
+      load_vis();
+      vi = 0;
+      if (nv > 0) load_segment();
+    }
+  }
+  __device__ void init(const FwdParams& p, const WorkItem& it, const ItemRows& ir) {
+    cp = p.cp;
+    cq = it.c;
+    r = chunk_owner(cq, cp);
+    const int start = ir.seq_start;
+    S = __ldg(p.cu + it.b + 1) - __ldg(p.cu + it.b);
+    L = (__ldg(p.cu_pad + it.b + 1) - start) / (2 * cp);
+    q_hi = ir.q_hi;
+    s = p.fused ? 0 : it.step;
+    s_end = p.fused ? cp - 1 : it.step;
+    done = q_hi <= ir.q_lo;
+    vi = 0;
+    t = 0;
+    ntile = 0;
+    load_vis();
+    if (!done && nv > 0) load_segment();
+    settle();
+  }
+  __device__ int k0() const { return lo + t * BN; }
+  __device__ void next() {
+    ++t;
+    settle();
+  }
+};
+
+template <int BN>
+__device__ __forceinline__ int count_tiles(const FwdParams& p, const WorkItem& it, const ItemRows& ir) {
+  KvTileIter<BN> c;
+  c.init(p, it, ir);
+  int n = 0;
+  for (; !c.done; c.next()) ++n;
+  return n;
 }
 
 template <int D, int NH>
@@ -217,10 +247,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const WorkItem it = p.items[w / nhg];
         const int h0 = static_cast<int>(w % nhg) * NH;
         const int g = h0 / (p.hq / p.hkv);
-        const TilePlan tp = make_tile_plan<BN>(p, it);
+        const ItemRows ir = item_rows(p, it);
         if (item_k > 0) ok = mbar_wait(q_free, (item_k - 1) & 1, abort_flag);
         if (!ok) break;
-        const int qrow_base = tp.seq_start + tp.q_lo;
+        const int qrow_base = ir.seq_start + ir.q_lo;
         mbar_arrive_expect_tx(q_full, NH * Cfg::Q_BYTES);
         for (int h = 0; h < NH; ++h) {
           const int hq = h0 + h;
@@ -230,11 +260,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         hq % p.hpg_q, row, q_full);
         }
         ++q_loads;
-        const int kv_group_row = static_cast<int>((g / p.hpg_kv) * p.T) + tp.seq_start;
-        auto load = [&](int which, int j) -> bool {          // which: 0 = K_j, 1 = V_j
-          int k0, khi;
-          bool diag;
-          tile_of<BN>(tp, j, &k0, &khi, &diag);
+        const int kv_group_row = static_cast<int>((g / p.hpg_kv) * p.T) + ir.seq_start;
+        auto load = [&](int which, int k0) -> bool {         // which: 0 = K tile, 1 = V tile
           const int sl = static_cast<int>(u % NSLOT);
           if (u >= NSLOT && !mbar_wait(kv_empty + sl, static_cast<uint32_t>((u / NSLOT) - 1) & 1, abort_flag))
             return false;
@@ -247,11 +274,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           ++u;
           return true;
         };
-        const int n = tp.ntiles;
-        for (int j = 0; j < min(Cfg::LA, n) && ok; ++j) ok = load(0, j);
-        for (int j = 0; j < n && ok; ++j) {
-          if (j + Cfg::LA < n) ok = load(0, j + Cfg::LA);
-          if (ok) ok = load(1, j);
+        const int n = count_tiles<BN>(p, it, ir);
+        KvTileIter<BN> ahead, cur;                      // K runs LA tiles ahead of V
+        ahead.init(p, it, ir);
+        cur.init(p, it, ir);
+        for (int j = 0; j < min(Cfg::LA, n) && ok; ++j, ahead.next()) ok = load(0, ahead.k0());
+        for (int j = 0; j < n && ok; ++j, cur.next()) {
+          if (j + Cfg::LA < n) {
+            ok = load(0, ahead.k0());
+            ahead.next();
+          }
+          if (ok) ok = load(1, cur.k0());
         }
       }
       if (!ok) {
@@ -315,8 +348,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       };
       int item_k = 0;
       for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item_k) {
-        const TilePlan tp = make_tile_plan<BN>(p, p.items[w / nhg]);
-        const int n = tp.ntiles;
+        const WorkItem it = p.items[w / nhg];
+        const int n = count_tiles<BN>(p, it, item_rows(p, it));
         ok = mbar_wait(q_full, item_k & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
@@ -386,22 +419,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
       const WorkItem it = p.items[w / nhg];
       const int h0 = static_cast<int>(w % nhg) * NH;
-      const TilePlan tp = make_tile_plan<BN>(p, it);
-      const int n = tp.ntiles;
-      const int q_pos = tp.q_lo + row;
+      const ItemRows ir = item_rows(p, it);
+      KvTileIter<BN> kt_it;
+      kt_it.init(p, it, ir);
+      const int q_pos = ir.q_lo + row;
       float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < n; ++j) {
+      int n = 0;                                        // tiles of this item (counted as they go)
+      for (int j = 0; !kt_it.done; ++j, ++n, kt_it.next()) {
         const int64_t t = gs + j;
         const int buf = static_cast<int>(t % SBUF);
         ok = __all_sync(0xffffffffu,
                         mbar_wait(s_full + h * SBUF + buf, static_cast<uint32_t>(t / SBUF) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        int k0, khi;
-        bool diag;
-        tile_of<BN>(tp, j, &k0, &khi, &diag);
+        const int k0 = kt_it.k0();
         // keys visible to this row: k < kend (segment end, and k <= q_pos on the diagonal chunk)
-        const int kend = diag ? min(khi, q_pos + 1) : khi;
+        const int kend = kt_it.diag ? min(kt_it.hi, q_pos + 1) : kt_it.hi;
         const int nvalid = kend - k0;                     // may be <= 0 or >= BN
         const uint32_t t_s = t_head + buf * BN;
         // S row columns held in registers at once: the whole row when the
@@ -486,11 +519,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       // read O out of TMEM, then release it for the next item's first P V
-      const bool valid = q_pos < tp.q_hi;
+      const bool valid = q_pos < ir.q_hi;
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const int hq = h0 + h;
-      const int64_t orow = thd_row(tp.seq_start + q_pos, hq, p.hpg_q, p.T);
-      uint4* dst = reinterpret_cast<uint4*>(p.o + it.step * p.o_slab + orow * D);
+      const int64_t orow = thd_row(ir.seq_start + q_pos, hq, p.hpg_q, p.T);
+      const int64_t slab = p.fused ? 0 : it.step;
+      uint4* dst = reinterpret_cast<uint4*>(p.o + slab * p.o_slab + orow * D);
       uint32_t r[32];
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -512,7 +546,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
       }
-      if (valid) p.lse[it.step * p.lse_slab + orow] = (m + __log2f(l)) * kLn2;
+      if (valid) p.lse[slab * p.lse_slab + orow] = (m + __log2f(l)) * kLn2;
       gs += n;
     }
     if (!ok) {
@@ -553,8 +587,9 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
                             const int32_t* cu_pad, void* o, float* lse, int64_t o_slab, int64_t lse_slab,
                             int32_t* status, int cp, int hq, int hkv, int head_groups, int64_t T, int D,
-                            float scale, int num_sms, cudaStream_t stream) {
+                            float scale, int fused, int num_sms, cudaStream_t stream) {
   FwdParams p;
+  p.fused = fused;
   p.items = items;
   p.hdr = hdr;
   p.cu = cu;

@@ -189,6 +189,30 @@ thd_permute_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
   }
 }
 
+// O = 0 and LSE = -inf on padding rows (positions >= S_b of their sequence):
+// one warp per token, walking a contiguous range of tokens.
+__global__ void __launch_bounds__(256)
+pad_rows_kernel(uint4* __restrict__ o, float* __restrict__ lse, const int32_t* __restrict__ cu,
+                const int32_t* __restrict__ cu_pad, int B, int64_t T, int H, int hpg, int D,
+                int64_t tokens_per_warp, const int32_t* status) {
+  if (status_bad(status)) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t t_begin = warp_id * tokens_per_warp, t_end = min(T, t_begin + tokens_per_warp);
+  const int w16 = D / 8;
+  SeqCache sc;
+  for (int64_t t = t_begin; t < t_end; ++t) {
+    const int b = sc.get(cu_pad, B, t);
+    const int S = __ldg(cu + b + 1) - __ldg(cu + b);
+    if (t - sc.lo < S) continue;                     // a real token: written by the attention kernel
+    for (int h = 0; h < H; ++h) {
+      const int64_t row = thd_row(t, h, hpg, T);
+      for (int u = lane; u < w16; u += 32) o[row * w16 + u] = make_uint4(0, 0, 0, 0);
+      if (lane == 0) lse[row] = -INFINITY;
+    }
+  }
+}
+
 int grid_for(int64_t units, int per_block, int max_blocks) {
   int64_t g = (units + per_block - 1) / per_block;
   if (g > max_blocks) g = max_blocks;
@@ -205,6 +229,15 @@ cudaError_t launch_lse_merge(const MergeArgs& a, int num_sms, cudaStream_t strea
   if (tpr == 16) lse_merge_kernel<16><<<grid, 256, 0, stream>>>(a, rpb);
   else if (tpr == 32) lse_merge_kernel<32><<<grid, 256, 0, stream>>>(a, rpb);
   else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_rows(void* o, float* lse, const int32_t* cu, const int32_t* cu_pad, int B, int64_t T,
+                            int H, int hpg, int D, const int32_t* status, int num_sms, cudaStream_t stream) {
+  const int grid = grid_for(T, 8, num_sms * 16);
+  const int64_t warps = static_cast<int64_t>(grid) * 8;
+  const int64_t tpw = (T + warps - 1) / warps;
+  pad_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4*>(o), lse, cu, cu_pad, B, T, H, hpg, D, tpw, status);
   return cudaGetLastError();
 }
 

@@ -8,6 +8,7 @@
 // promise writes CCG_ERR_SEQLENS into the status word (no trap) and an
 // empty plan, so that every later kernel returns without writing.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace ccg {
 
@@ -130,6 +131,24 @@ plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, 
       for (int s = 0; s < kMaxCP; ++s) hdr->n_fwd[s] = 0;
     }
   }
+  if (want & 4) {
+    // fused forward: one item per query tile with real rows, all ring steps of
+    // its rank; later query chunks see more keys, so they go first
+    int slot = 0;
+    const int cap_all = cp * cap_q;
+    for (int c = C - 1; c >= 0; --c) {
+      auto count = [&](int b) { return valid_tiles(b, c, bm); };
+      auto write = [&](int b, int first, int n) {
+        for (int t = 0; t < n && first + t < cap_all; ++t) fwd_items[first + t] = WorkItem{b, c, t, -1};
+      };
+      slot = block_emit(B, slot, count, write);
+    }
+    if (slot > cap_all) overflow = 1;
+    if (threadIdx.x == 0) {
+      hdr->n_fwd_all = min(slot, cap_all);
+      for (int s = 0; s < kMaxCP; ++s) hdr->n_fwd[s] = 0;
+    }
+  }
   if (want & 2) {
     // dQ pass: later query chunks see more keys, so they go first
     int slot = 0;
@@ -176,7 +195,27 @@ __global__ void chunk_table_kernel(const int32_t* __restrict__ cu, const int32_t
   table[2 * i + 1] = L;
 }
 
+// A bounded wait on a barrier nothing arrives at: gives up after limit_ns and
+// records the timeout, like every wait in the attention kernels.
+__global__ void bounded_wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile int never = 0;
+    if (!mbar_wait(&bar, 0, &never, limit_ns)) raise_status(status, CCG_ERR_TIMEOUT);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bounded_wait_selftest(int32_t* status, uint32_t limit_us, cudaStream_t stream) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(status, static_cast<uint64_t>(limit_us) * 1000ull);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp, int bm,
                         int bn, int cap_q, int cap_kv, int want, int step_only, PlanHeader* hdr,

@@ -23,15 +23,26 @@ class AttentionStep:
     `device`), cu_seqlens and cu_seqlens_padded (int32).  With the A2A round
     trip (w.pack_roundtrip) the inputs are in the rank-major local layout and
     the outputs come back in it; otherwise everything is plain packed THD.
+
+    schedule: "ring" (default) -- the CP-emulated ring over w.cp ranks on the
+    (possibly head-split) layout; "a2a" -- the A2A (Ulysses-style) schedule:
+    pack to w.cp head groups, full-sequence attention per head group (CP = 1,
+    no partials, no merge), unpack.  fused: forward with one online softmax
+    over all ring steps (ccg_attn_fwd_fused) instead of partials + merge.
     """
 
-    def __init__(self, w, inputs, device="cuda"):
+    def __init__(self, w, inputs, device="cuda", schedule="ring", fused=False):
         load()
+        if schedule not in ("ring", "a2a"):
+            raise ValueError(schedule)
         self.w = w
         self.x = inputs
         self.device = device
+        self.schedule = schedule
+        self.fused = fused or schedule == "a2a"
+        self.attn_cp = 1 if schedule == "a2a" else w.cp
         T, hq, hkv, D, cp = w.total_tokens, w.hq, w.hkv, w.head_dim, w.cp
-        self.split = bool(w.pack_roundtrip)
+        self.split = bool(w.pack_roundtrip) or schedule == "a2a"
         e = dict(dtype=torch.bfloat16, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.ws_f = Workspace(device)
@@ -72,9 +83,10 @@ class AttentionStep:
             q, k, v, do, hg = self.qs, self.ks, self.vs, self.dos, w.cp
         else:
             q, k, v, do, hg = x["q"], x["k"], x["v"], x["do"], 1
-        attn_fwd(q, k, v, cu, cpad, w.cp, head_groups=hg, out=self.os, lse=self.lse, workspace=self.ws_f, **kw)
+        attn_fwd(q, k, v, cu, cpad, self.attn_cp, head_groups=hg, out=self.os, lse=self.lse, workspace=self.ws_f,
+                 fused=self.fused, **kw)
         n += last_launch_count()
-        attn_bwd(q, k, v, self.os, do, self.lse, cu, cpad, w.cp, head_groups=hg, dq=self.dqs, dk=self.dks,
+        attn_bwd(q, k, v, self.os, do, self.lse, cu, cpad, self.attn_cp, head_groups=hg, dq=self.dqs, dk=self.dks,
                  dv=self.dvs, workspace=self.ws_b, **kw)
         n += last_launch_count()
         if self.split:

@@ -33,8 +33,8 @@
  *  - Tensor layout "THD with head groups": a tensor with H heads of width D
  *    and `head_groups` = G_h (1 or CP) is stored as [G_h][T][H/G_h][D]; head
  *    h of token t lives at row (h / (H/G_h)) * T + t, slot h % (H/G_h).
- *    G_h = 1 is the plain packed THD layout [T][H][D].  G_h = CP is the A2A
- *    head-split layout produced by ccg_thd_pack.  LSE tensors use the same
+ *    G_h = 1 is the plain packed THD layout [T][H][D].  G_h = the A2A size is
+ *    the head-split layout produced by ccg_thd_pack.  LSE tensors use the same
  *    grouping with D = 1: [G_h][T][Hq/G_h] float.
  *  - Sequences: cu_seqlens[B+1] (logical lengths S_b) and
  *    cu_seqlens_padded[B+1] (physical offsets, padded lengths P_b), int32,
@@ -79,18 +79,20 @@ typedef struct {
   int32_t head_dim;       /* D: 128 or 256                                             */
   int32_t causal;         /* must be 1 (the path is causal attention)                  */
   int32_t cp;             /* emulated context-parallel ranks, 1..16                    */
-  int32_t head_groups;    /* 1 (plain THD) or cp (head-split); hq, hkv divisible by it */
+  int32_t head_groups;    /* G_h >= 1: 1 = plain THD, >1 = head-split layout (e.g. the
+                             A2A layout of ccg_thd_pack); hq, hkv divisible by it    */
   int32_t reserved;       /* must be 0                                                 */
   int64_t total_tokens;   /* T = cu_seqlens_padded[B]                                  */
   float softmax_scale;    /* <= 0 selects 1/sqrt(D)                                    */
 } ccg_attn_desc;
 
-/* Bytes of device workspace ccg_attn_fwd (is_bwd = 0) or ccg_attn_bwd
- * (is_bwd = 1) needs for `desc`; 0 if `desc` is invalid.  The forward
- * workspace holds the work plan plus CP per-step partial outputs
- * (CP x T x Hq x D BF16) and their LSE (CP x T x Hq float); the backward
- * workspace holds the work plan and Delta (T x Hq float). */
-size_t ccg_workspace_size(const ccg_attn_desc* desc, int is_bwd);
+/* Bytes of device workspace needed for `desc` by ccg_attn_fwd (kind = 0),
+ * ccg_attn_bwd (kind = 1) or ccg_attn_fwd_fused (kind = 2); 0 if `desc` or
+ * `kind` is invalid.  The forward workspace holds the work plan plus CP
+ * per-step partial outputs (CP x T x Hq x D BF16) and their LSE (CP x T x Hq
+ * float); the backward workspace holds the work plan and Delta (T x Hq
+ * float); the fused forward workspace holds only the work plan. */
+size_t ccg_workspace_size(const ccg_attn_desc* desc, int kind);
 
 /* Forward: O = softmax(scale Q K^T + causal mask) V and its row LSE, computed
  * as CP emulated ranks do it (TransformerEngine PR, Independent-node
@@ -107,6 +109,20 @@ ccg_status ccg_attn_fwd(const ccg_attn_desc* desc, const void* q, const void* k,
                         const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded,
                         void* o, float* lse, void* workspace, size_t workspace_bytes,
                         int32_t* d_status, ccg_stream_t stream);
+
+/* Forward with the merge folded into the attention (the next step after the
+ * ring-partials path; TransformerEngine PR, Description: the partials exist
+ * only to be combined by LSE rescaling): each query tile runs ONE online
+ * softmax over the KV chunks of every ring step of its rank, in ring order,
+ * instead of one softmax per step followed by the K-way merge.  Same result
+ * up to rounding order, same arguments and layouts as ccg_attn_fwd; the
+ * workspace is ccg_workspace_size(desc, 2) bytes (the plan only: no partials
+ * are materialised). */
+ccg_status ccg_attn_fwd_fused(const ccg_attn_desc* desc, const void* q, const void* k,
+                              const void* v, const int32_t* cu_seqlens,
+                              const int32_t* cu_seqlens_padded, void* o, float* lse,
+                              void* workspace, size_t workspace_bytes, int32_t* d_status,
+                              ccg_stream_t stream);
 
 /* One ring step of the forward, exposed for inspection: the partial
  * (O_s, LSE_s) of step `step` for all emulated ranks.  Rows that have no
@@ -208,6 +224,15 @@ ccg_status ccg_thd_pack(const void* x_rank_major, const int32_t* cu_seqlens_padd
 ccg_status ccg_thd_unpack(const void* in_head_split, const int32_t* cu_seqlens_padded,
                           int32_t batch, int64_t total_tokens, int32_t heads, int32_t head_dim,
                           int32_t cp, void* x_rank_major, int32_t* d_status, ccg_stream_t stream);
+
+/* Self-test of the device failure path; no fault is involved.  Launches one
+ * CTA whose thread waits, bounded by `limit_us` microseconds (1..1000000), on
+ * a shared-memory barrier that nothing arrives at: the wait gives up, the
+ * kernel writes CCG_ERR_TIMEOUT into d_status and returns normally, exactly
+ * as the attention kernels do when one of their bounded waits runs out.  Lets
+ * a caller check that device-detected errors reach the host and that the
+ * CUDA context stays usable afterwards. */
+ccg_status ccg_selftest_bounded_wait(int32_t* d_status, uint32_t limit_us, ccg_stream_t stream);
 
 /* Synchronises `stream`, reads the device status word and returns it
  * (CCG_OK, CCG_ERR_SEQLENS or CCG_ERR_TIMEOUT), or CCG_ERR_CUDA if the

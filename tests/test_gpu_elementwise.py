@@ -84,3 +84,22 @@ def test_broken_promise_sets_status_and_writes_nothing(lib):
         lib.attn_fwd(x["q"], x["k"], x["v"], cu2, cp2, w.cp, out=o, lse=lse)
     assert "SEQLENS" in str(e.value)
     assert torch.all(o == 7.0) and torch.all(lse == 7.0)
+
+
+def test_bounded_wait_times_out_into_status_and_context_stays_usable(lib):
+    """Failure detection without a fault: a bounded wait that nothing
+    satisfies gives up, the status word reports CCG_ERR_TIMEOUT, and the
+    next computation on the same context is correct."""
+    import ctypes
+    L = lib.load()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    code = L.ccg_selftest_bounded_wait(ctypes.c_void_p(st.data_ptr()), 2000,
+                                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert code == 0
+    assert lib.get_status(st) == 6                       # CCG_ERR_TIMEOUT
+    assert L.ccg_selftest_bounded_wait(ctypes.c_void_p(st.data_ptr()), 0, None) == 1
+    w = W.WORKLOADS["tiny"]
+    x = W.make_inputs(w, device="cuda")
+    o, lse = lib.attn_fwd(x["q"], x["k"], x["v"], x["cu_seqlens"], x["cu_seqlens_padded"], w.cp)
+    o_ref, _ = oracle.attention_forward(f64(x["q"]), f64(x["k"]), f64(x["v"]), w.cu_seqlens, w.cu_seqlens_padded)
+    assert_o_close(f64(o), o_ref)
