@@ -29,7 +29,7 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
                             const int32_t* cu_pad, void* o, float* lse, int64_t o_slab, int64_t lse_slab,
                             int32_t* status, int cp, int hq, int hkv, int head_groups, int64_t T, int D,
-                            float scale, int fused, int num_sms, cudaStream_t stream);
+                            float scale, int mode, int num_sms, cudaStream_t stream);
 cudaError_t launch_pad_rows(void* o, float* lse, const int32_t* cu, const int32_t* cu_pad, int B, int64_t T,
                             int H, int hpg, int D, const int32_t* status, int num_sms, cudaStream_t stream);
 cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items,
@@ -384,23 +384,25 @@ ccg_status ccg_thd_unpack(const void* in_head_split, const int32_t* cu_seqlens_p
                      x_rank_major, d_status, stream);
 }
 
-// Plans and launches the ring-step partials: all steps (step_only < 0) into
-// consecutive slabs of o_part / lse_part, or one step into o_part / lse_part.
+// Plans and launches the forward attention kernel.  mode 0: the partial of
+// ring step `step_only` into o_part / lse_part; mode 1: the partials of every
+// ring step into consecutive slabs of o_part / lse_part (one item per query
+// tile walks all steps of its rank); mode 2: every ring step in one online
+// softmax, the final O and LSE into o_part / lse_part.
 static ccg_status fwd_partials(const ccg_attn_desc* d, int step_only, const void* q, const void* k,
                                const void* v, const int32_t* cu, const int32_t* cu_pad, void* o_part,
                                int64_t o_slab, float* lse_part, int64_t lse_slab, void* workspace,
-                               const Layout& L, int32_t* status, cudaStream_t s, int* launches_out,
-                               int fused = 0) {
+                               const Layout& L, int32_t* status, cudaStream_t s, int* launches_out, int mode) {
   int launches = *launches_out;
   auto* base = static_cast<uint8_t*>(workspace);
   auto* hdr = reinterpret_cast<PlanHeader*>(base + L.hdr);
   auto* items = reinterpret_cast<WorkItem*>(base + L.fwd_items);
   CCG_LAUNCH("plan", s,
              launch_plan(cu, cu_pad, d->batch, d->total_tokens, d->cp, kQTile, kMinKvTile, L.cap_q, L.cap_kv,
-                         fused ? 4 : 1, step_only, hdr, items, nullptr, nullptr, status, s));
+                         mode == 0 ? 1 : 4, step_only, hdr, items, nullptr, nullptr, status, s));
   const int hg = d->head_groups;
   const int64_t rows = d->total_tokens * hg;
-  const int bn = d->head_dim == 128 ? 128 : 64;
+  const int bn = 128;                                   // forward K/V tile rows
   CUtensorMap tq, tk, tv;
   if (!make_thd_map(&tq, q, d->head_dim, d->hq / hg, rows, kQTile) ||
       !make_thd_map(&tk, k, d->head_dim, d->hkv / hg, rows, bn) ||
@@ -408,7 +410,7 @@ static ccg_status fwd_partials(const ccg_attn_desc* d, int step_only, const void
     return CCG_ERR_CUDA;
   CCG_LAUNCH("attn_fwd", s,
              launch_attn_fwd(tq, tk, tv, items, hdr, cu, cu_pad, o_part, lse_part, o_slab, lse_slab, status, d->cp,
-                             d->hq, d->hkv, hg, d->total_tokens, d->head_dim, softmax_scale(d), fused,
+                             d->hq, d->hkv, hg, d->total_tokens, d->head_dim, softmax_scale(d), mode,
                              num_sms_cached(), s));
   *launches_out = launches;
   return CCG_OK;
@@ -429,7 +431,7 @@ ccg_status ccg_attn_fwd_step(const ccg_attn_desc* desc, int32_t step, const void
   if (desc->total_tokens == 0) return CCG_OK;
   int launches = 0;
   st = fwd_partials(desc, step, q, k, v, cu_seqlens, cu_seqlens_padded, o_part, 0, lse_part, 0, workspace, L,
-                    d_status, reinterpret_cast<cudaStream_t>(stream), &launches);
+                    d_status, reinterpret_cast<cudaStream_t>(stream), &launches, 0);
   g_last_launches = launches;
   return st;
 }
@@ -452,7 +454,7 @@ ccg_status ccg_attn_fwd(const ccg_attn_desc* desc, const void* q, const void* k,
   int launches = 0;
   st = fwd_partials(desc, -1, q, k, v, cu_seqlens, cu_seqlens_padded, base + L.o_parts,
                     static_cast<int64_t>(rows * desc->head_dim), reinterpret_cast<float*>(base + L.lse_parts),
-                    static_cast<int64_t>(rows), workspace, L, d_status, s, &launches);
+                    static_cast<int64_t>(rows), workspace, L, d_status, s, &launches, 1);
   if (st != CCG_OK) return st;
   MergeArgs a{};
   for (int p = 0; p < desc->cp; ++p) {
@@ -490,7 +492,7 @@ ccg_status ccg_attn_fwd_fused(const ccg_attn_desc* desc, const void* q, const vo
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int launches = 0;
   st = fwd_partials(desc, -1, q, k, v, cu_seqlens, cu_seqlens_padded, o, 0, lse, 0, workspace, L, d_status, s,
-                    &launches, 1);
+                    &launches, 2);
   if (st != CCG_OK) return st;
   CCG_LAUNCH("pad_rows", s,
              launch_pad_rows(o, lse, cu_seqlens, cu_seqlens_padded, desc->batch, desc->total_tokens, desc->hq,

@@ -7,14 +7,19 @@
 // and keeps the partial output with its LSE ("Stats") for the merge.
 //
 // One persistent launch covers every ring step: the work list holds one item
-// per (ring step, query chunk, 128-row query tile), heaviest first, and each
-// item is computed for NH q heads that share one kv head (GQA K/V reuse:
-// every K/V tile is loaded once for the NH heads).  An item attends its query
-// tile over the KV chunks of the step's source rank that it can see (causal
-// block skipping: KV tiles past the tile's last row are never loaded) with a
-// fresh online softmax, and writes the step's partial (O_s, LSE_s).  CTAs
-// stride through the list, so the next item's Q load and first S = Q K^T
-// products overlap the current item's last P V product and its epilogue.
+// per (query chunk, 128-row query tile), heaviest first, and each item is
+// computed for NH q heads that share one kv head (GQA K/V reuse: every K/V
+// tile is loaded once for the NH heads).  An item walks the ring steps of its
+// chunk's rank in order; at each step it attends the source rank's KV chunks
+// that it can see (causal block skipping: KV tiles past the tile's last row
+// are never loaded) with a fresh online softmax and writes that step's
+// partial (O_s, LSE_s).  Q is loaded once per item and the K/V stream, the S
+// lookahead and the tensor core run on across the step boundaries; only the
+// O read-out of a finished step waits on its last P V product.  CTAs stride
+// through the list, so the next item's Q load and first S = Q K^T products
+// overlap the current item's last P V product and its epilogue.  The same
+// kernel computes one ring step alone (one item per tile of that step), or
+// every step in one online softmax (the fused forward, no partials).
 // Roles:
 //   warp 0     TMA producer: Q per item, K and V tiles through single-tile slots
 //   warp 1     MMA issuer (one thread): S = Q K^T (SMEM x SMEM -> TMEM),
@@ -38,28 +43,36 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale only past 2^8
 
 template <int D, int NH>
 struct FwdCfg {
-  static constexpr int BN = D == 128 ? 128 : 64;
-  // One head per CTA: three S buffers, so S of tile t+2 is issued before the
-  // MMA warp waits for P of tile t (lookahead LA = 2).  Two heads per CTA:
-  // one S buffer per head, the heads' MMAs and softmaxes interleave (LA = 1).
-  static constexpr int SBUF = NH == 1 ? 3 : 1;
-  static constexpr int LA = NH == 1 ? 2 : 1;
+  // 128-key tiles: the S = Q K^T products run at N = 128 (full tensor rate;
+  // N = 64 issues at two thirds of it) and the MMA warp's per-tile
+  // synchronisation is spread over twice the keys.
+  static constexpr int BN = 128;
+  // TMEM per head: SBUF S buffers (BN columns each) + O (D columns).
+  //   D=128, one head:  3 S buffers, S of tile t+2 issued before P of tile t (LA = 2)
+  //   D=256, one head:  2 S buffers, LA = 1
+  //   D=128, two heads: 1 S buffer per head, the heads interleave (LA = 1)
+  static constexpr int SBUF = NH == 2 ? 1 : (D == 128 ? 3 : 2);
+  static constexpr int LA = SBUF == 3 ? 2 : 1;
   static constexpr int KCH = D / 64;                       // 64-wide (128-byte) column chunks
   static constexpr int Q_BYTES = kBM * D * 2;              // one head
   static constexpr int KV_BYTES = BN * D * 2;              // one K (or V) tile
   // K and V tiles stream through NSLOT single-tile slots in the order the MMA
   // warp consumes them (per item: K_0..K_{LA-1}, then K_{j+LA} and V_j for
   // j = 0, 1, ...); a slot is released when its S or P V product is done.
+  // At D=256 only two slots fit: K_{t+1} reloads while softmax(t) runs and
+  // V_{t+1} while S(t+2) and softmax(t+1) run.
   static constexpr int NSLOT = (227 * 1024 - 2048 - NH * Q_BYTES) / KV_BYTES;
   static constexpr int SMEM_Q = 0;
   static constexpr int SMEM_KV = SMEM_Q + NH * Q_BYTES;
   static constexpr int SMEM_BAR = SMEM_KV + NSLOT * KV_BYTES;
-  static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
+  static constexpr int BAR_WORDS = 3 + 2 * NSLOT + 2 * NH * SBUF + 5 * NH;  // mbarriers (8 bytes each)
+  static constexpr int SMEM_TOTAL = SMEM_BAR + 512;
   static constexpr int TMEM_HEAD = SBUF * BN + D;  // S buffers, then O
   static constexpr int TMEM_USED = NH * TMEM_HEAD;
   static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : (TMEM_USED <= 256 ? 256 : 512);
   static constexpr int THREADS = 128 + 128 * NH;
-  static_assert(NSLOT >= 4, "at least two tiles in flight");
+  static_assert(NSLOT >= 2, "K and V slots");
+  static_assert(BAR_WORDS * 8 + 8 + 4 * NH * SBUF <= 512, "barrier region");
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM budget");
 };
@@ -76,7 +89,11 @@ struct FwdParams {
   int cp, hq, hkv, hpg_q, hpg_kv;
   int64_t T;
   float scale_log2;
-  int fused;                    // 1: every ring step of the rank in one online softmax (no partials)
+  // 0: an item is one ring step of a query tile, written as that step's partial;
+  // 1: an item is every ring step of a query tile's rank, a fresh online
+  //    softmax per step and one partial (O_s, LSE_s) written per step;
+  // 2: an item is every ring step in ONE online softmax (final O and LSE).
+  int mode;
 };
 
 // The query rows of one work item.
@@ -97,7 +114,7 @@ __device__ __forceinline__ ItemRows item_rows(const FwdParams& p, const WorkItem
 }
 
 // KV tiles one work item attends, in ring order: for each ring step of the
-// item (its own step, or every step of its rank when fused), the source
+// item (its own step, or every step of its rank in modes 1 and 2), the source
 // rank's KV chunks the query chunk can see, ascending; tiles ascending.  On
 // the diagonal chunk, keys past the item's last real row are skipped.
 template <int BN>
@@ -141,8 +158,8 @@ struct KvTileIter {
     S = __ldg(p.cu + it.b + 1) - __ldg(p.cu + it.b);
     L = (__ldg(p.cu_pad + it.b + 1) - start) / (2 * cp);
     q_hi = ir.q_hi;
-    s = p.fused ? 0 : it.step;
-    s_end = p.fused ? cp - 1 : it.step;
+    s = p.mode != 0 ? 0 : it.step;
+    s_end = p.mode != 0 ? cp - 1 : it.step;
     done = q_hi <= ir.q_lo;
     vi = 0;
     t = 0;
@@ -157,6 +174,13 @@ struct KvTileIter {
     settle();
   }
 };
+
+// Tile j of an item opens a new online-softmax segment (fresh max, sum and
+// O accumulator): the item's first tile, and with one partial per ring step
+// the first tile of each later step.
+__device__ __forceinline__ bool new_segment(int mode, int j, int step, int prev_step) {
+  return j == 0 || (mode == 1 && step != prev_step);
+}
 
 template <int BN>
 __device__ __forceinline__ int count_tiles(const FwdParams& p, const WorkItem& it, const ItemRows& ir) {
@@ -194,12 +218,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // complete, PV(t-3) is too (S is issued at most two tiles ahead of P V), so
   // the barrier's previous phase (PV(t-4)) has completed and PV(t+4) cannot
   // have been issued.  The softmax waits only when it must rescale O, and
-  // once per item before reading O out.
+  // once per segment before reading O out.
   uint64_t* o_done = p_full + NH * SBUF;
-  uint64_t* o_free = o_done + NH * 4;                  // [NH]: the item's O has been read out
+  uint64_t* o_free = o_done + NH * 4;                  // [NH]: a segment's O has been read out
   uint64_t* mma_done = o_free + NH;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // [NH][SBUF]: 1 when the P in that S buffer opens a softmax segment (its
+  // P V starts a fresh O); written by the softmax before it arrives on
+  // p_full, read by the MMA issuer after its wait on p_full.
+  volatile int* seg_flag = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -347,6 +375,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         return true;
       };
       int item_k = 0;
+      int64_t segs = 0;  // softmax segments opened by this CTA (one O read-out each)
       for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item_k) {
         const WorkItem it = p.items[w / nhg];
         const int n = count_tiles<BN>(p, it, item_rows(p, it));
@@ -379,13 +408,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int buf = static_cast<int>(t % SBUF);
             ok = mbar_wait(p_full + h * SBUF + buf, static_cast<uint32_t>(t / SBUF) & 1, abort_flag);
             if (!ok) break;
-            if (j == 0 && item_k > 0) {
-              // the previous item's O must have been read out before it is overwritten
-              ok = mbar_wait(o_free + h, (item_k - 1) & 1, abort_flag);
+            const bool seg_start = p.mode == 1 ? seg_flag[h * SBUF + buf] != 0 : j == 0;
+            if (h == 0 && seg_start) ++segs;
+            if (seg_start && segs > 1) {
+              // the previous segment's O must have been read out before it is overwritten
+              ok = mbar_wait(o_free + h, static_cast<uint32_t>(segs - 2) & 1, abort_flag);
               if (!ok) break;
             }
             tc_fence_after();
-            issue_pv(h, t, vsl, j == 0);
+            issue_pv(h, t, vsl, seg_start);
             // one buffer per head: this head's next S goes right behind its P V,
             // while the other head's softmax keeps the tensor core busy
             if (SBUF == 1 && ahead) issue_s(h, t + 1, static_cast<int>(k_next % NSLOT));
@@ -423,10 +454,65 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       KvTileIter<BN> kt_it;
       kt_it.init(p, it, ir);
       const int q_pos = ir.q_lo + row;
+      const bool valid = q_pos < ir.q_hi;
+      const int64_t orow = thd_row(ir.seq_start + q_pos, h0 + h, p.hpg_q, p.T);
       float m = -INFINITY, l = 0.f;
+      int seg_step = -1;                                // ring step of the open segment
+      // Closes the open segment once its last P V product (tile t_last) has
+      // landed: reads O out of TMEM, releases it for the next segment's first
+      // P V, and writes O / l and the LSE -- the partial of ring step `step`
+      // (modes 0, 1) or the final output (mode 2).
+      auto flush = [&](int64_t t_last, int step) -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done + h * 4 + static_cast<int>(t_last % 4),
+                                               static_cast<uint32_t>(t_last / 4) & 1, abort_flag)))
+          return false;
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const int64_t slab = p.mode == 2 ? 0 : step;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + slab * p.o_slab + orow * D);
+        uint32_t r[32];
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          tmem_ld32(t_o + c * 32, r);
+          tmem_wait_ld();
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(o_free + h);
+          }
+          if (valid) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * inv_l, __uint_as_float(r[8 * v4 + 1]) * inv_l);
+              u.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * inv_l, __uint_as_float(r[8 * v4 + 3]) * inv_l);
+              u.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * inv_l, __uint_as_float(r[8 * v4 + 5]) * inv_l);
+              u.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * inv_l, __uint_as_float(r[8 * v4 + 7]) * inv_l);
+              dst[c * 4 + v4] = u;
+            }
+          }
+        }
+        if (valid) p.lse[slab * p.lse_slab + orow] = (m + __log2f(l)) * kLn2;
+        return true;
+      };
       int n = 0;                                        // tiles of this item (counted as they go)
-      for (int j = 0; !kt_it.done; ++j, ++n, kt_it.next()) {
+      for (int j = 0;; ++j, kt_it.next()) {
         const int64_t t = gs + j;
+        const bool end = kt_it.done;
+        const bool seg_open = !end && new_segment(p.mode, j, kt_it.s, seg_step);
+        if ((end || seg_open) && j > 0) {
+          // the open segment is complete: its ring step or the item ended
+          ok = flush(t - 1, seg_step);
+          if (!ok) break;
+        }
+        if (end) {
+          n = j;
+          break;
+        }
+        if (seg_open) {
+          m = -INFINITY;
+          l = 0.f;
+          seg_step = kt_it.s;
+        }
         const int buf = static_cast<int>(t % SBUF);
         ok = __all_sync(0xffffffffu,
                         mbar_wait(s_full + h * SBUF + buf, static_cast<uint32_t>(t / SBUF) & 1, abort_flag));
@@ -441,19 +527,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // register budget allows (one TMEM round trip), else halves
         constexpr int HOLD = (NH == 1) ? BN : 64;
         uint32_t sr[HOLD];
-        float mx = -INFINITY;
-#pragma unroll
-        for (int g0 = 0; g0 < BN; g0 += HOLD) {
+        // Only tiles that cross a row's last visible key need a mask; there
+        // the hidden scores are set to -inf in registers, so that the max
+        // ignores them and their probabilities come out exactly 0.
+        const bool masked = __any_sync(0xffffffffu, nvalid < BN);
+        auto load_s = [&](int g0) {
 #pragma unroll
           for (int c = 0; c < HOLD / 32; ++c)
             tmem_ld32(t_s + g0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
           tmem_wait_ld();
+          if (masked) {
 #pragma unroll
-          for (int x = 0; x < HOLD; ++x) {
-            const float sv = __uint_as_float(sr[x]) * p.scale_log2;
-            mx = (g0 + x < nvalid) ? fmaxf(mx, sv) : mx;
+            for (int x = 0; x < HOLD; ++x) sr[x] = (g0 + x < nvalid) ? sr[x] : 0xff800000u;
           }
+        };
+        // max of the raw scores, scaled once (the scale is positive, and a
+        // correctly rounded product preserves order)
+        float mxr = -INFINITY;
+#pragma unroll
+        for (int g0 = 0; g0 < BN; g0 += HOLD) {
+          load_s(g0);
+#pragma unroll
+          for (int x = 0; x < HOLD; x += 2) mxr = fmax3(mxr, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
         }
+        const float mx = mxr * p.scale_log2;
         float alpha = 1.f;
         if (mx > m) {
           if (m == -INFINITY) {
@@ -464,36 +561,37 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
         const float m_use = (m == -INFINITY) ? 0.f : m;
-        float psum = 0.f;
+        // p = 2^(s * scale_log2 - m), two columns per packed FMA
+        const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2);
+        const uint64_t negm2 = f32x2(-m_use, -m_use);
+        uint64_t psum2 = f32x2(0.f, 0.f);
 #pragma unroll
         for (int g0 = 0; g0 < BN; g0 += HOLD) {
-          if (HOLD < BN) {
-#pragma unroll
-            for (int c = 0; c < HOLD / 32; ++c)
-              tmem_ld32(t_s + g0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
-            tmem_wait_ld();
-          }
+          if (HOLD < BN) load_s(g0);
 #pragma unroll
           for (int c = 0; c < HOLD / 32; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
-              const int cl = c * 32 + 2 * x, c0 = g0 + cl;
-              const float p0 = (c0 < nvalid) ? ex2_approx(fmaf(__uint_as_float(sr[cl]), p.scale_log2, -m_use)) : 0.f;
-              const float p1 =
-                  (c0 + 1 < nvalid) ? ex2_approx(fmaf(__uint_as_float(sr[cl + 1]), p.scale_log2, -m_use)) : 0.f;
-              psum += p0 + p1;
+              const int cl = c * 32 + 2 * x;
+              float a0, a1;
+              f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[cl]), __uint_as_float(sr[cl + 1])), scale2, negm2), a0,
+                          a1);
+              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+              psum2 = add_f32x2(psum2, f32x2(p0, p1));
               pk[x] = pack_bf16x2(p0, p1);
             }
             tmem_st16(t_s + (g0 + c * 32) / 2, pk);
           }
         }
         tmem_wait_st();
-        l = l * alpha + psum;
+        float ps0, ps1;
+        f32x2_split(psum2, ps0, ps1);
+        l = l * alpha + (ps0 + ps1);
         // rescale the running O (rare: the reference max grew past the
         // threshold) once the previous P V product has landed
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const int64_t tp1 = t - 1;                     // alpha != 1 implies j > 0
+          const int64_t tp1 = t - 1;                     // alpha != 1: not a segment's first tile
           ok = __all_sync(0xffffffffu, mbar_wait(o_done + h * 4 + static_cast<int>(tp1 % 4),
                                                  static_cast<uint32_t>(tp1 / 4) & 1, abort_flag));
           if (!ok) break;
@@ -509,44 +607,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
           tmem_wait_st();
         }
+        if (row == 0) seg_flag[h * SBUF + buf] = seg_open ? 1 : 0;
         tc_fence_before();
         mbar_arrive(p_full + h * SBUF + buf);
       }
       if (!ok) break;
-      const int64_t t_last = gs + n - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(o_done + h * 4 + static_cast<int>(t_last % 4),
-                                             static_cast<uint32_t>(t_last / 4) & 1, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      // read O out of TMEM, then release it for the next item's first P V
-      const bool valid = q_pos < ir.q_hi;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const int hq = h0 + h;
-      const int64_t orow = thd_row(ir.seq_start + q_pos, hq, p.hpg_q, p.T);
-      const int64_t slab = p.fused ? 0 : it.step;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + slab * p.o_slab + orow * D);
-      uint32_t r[32];
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(t_o + c * 32, r);
-        tmem_wait_ld();
-        if (c == D / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive(o_free + h);
-        }
-        if (valid) {
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * inv_l, __uint_as_float(r[8 * v4 + 1]) * inv_l);
-            u.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * inv_l, __uint_as_float(r[8 * v4 + 3]) * inv_l);
-            u.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * inv_l, __uint_as_float(r[8 * v4 + 5]) * inv_l);
-            u.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * inv_l, __uint_as_float(r[8 * v4 + 7]) * inv_l);
-            dst[c * 4 + v4] = u;
-          }
-        }
-      }
-      if (valid) p.lse[slab * p.lse_slab + orow] = (m + __log2f(l)) * kLn2;
       gs += n;
     }
     if (!ok) {
@@ -587,9 +652,9 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
                             const int32_t* cu_pad, void* o, float* lse, int64_t o_slab, int64_t lse_slab,
                             int32_t* status, int cp, int hq, int hkv, int head_groups, int64_t T, int D,
-                            float scale, int fused, int num_sms, cudaStream_t stream) {
+                            float scale, int mode, int num_sms, cudaStream_t stream) {
   FwdParams p;
-  p.fused = fused;
+  p.mode = mode;
   p.items = items;
   p.hdr = hdr;
   p.cu = cu;
