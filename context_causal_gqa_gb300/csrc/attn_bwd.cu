@@ -101,7 +101,7 @@ struct KvCfg {
   static constexpr int SLOT_BYTES = BN * D * 2;
   static constexpr int SMEM_RES = 0;
   static constexpr int SMEM_SLOT = NRES * RES_BYTES;
-  static constexpr int SMEM_VEC = SMEM_SLOT + NSLOT * SLOT_BYTES;   // [WG][lse2 BN | delta BN]
+  static constexpr int SMEM_VEC = SMEM_SLOT + NSLOT * SLOT_BYTES;   // [WG][-lse2 BN | -delta*scale BN]
   static constexpr int SMEM_BAR = SMEM_VEC + 2 * 2 * BN * 4;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
   // TMEM: buffer b holds S^T at b*T_BUF and (if HAS_DP) dP^T at b*T_BUF + BN
@@ -452,6 +452,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int64_t grow = thd_row(si.start + q_pos, h, p.hpg_q, p.T);
     const float lse2 = row_valid ? __ldg(p.lse + grow) * kLog2e : 0.f;
     const float dlt = row_valid ? __ldg(p.delta + grow) : 0.f;
+    const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2), neg_lse2 = f32x2(-lse2, -lse2);
+    const uint64_t sc2 = f32x2(p.scale, p.scale), neg_dlt_s = f32x2(-dlt * p.scale, -dlt * p.scale);
     DqIter<BN> itr;
     itr.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
     const bool any = !itr.done;
@@ -466,23 +468,32 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const int k0 = itr.k0();
       const int kend = itr.diag ? min(itr.kv_hi, q_pos + 1) : itr.kv_hi;
       const int nvalid = row_valid ? kend - k0 : 0;
+      // hidden keys only on tiles that cross a row's last visible key: their
+      // scores become -inf in registers, so P (and dS) come out exactly 0
+      const bool masked = __any_sync(0xffffffffu, nvalid < BN);
       uint32_t rs[32], rp[32];
 #pragma unroll
       for (int c = c_first; c < c_first + NC; ++c) {
         tmem_ld32(tb + c * 32, rs);
         tmem_ld32(tb + BN + c * 32, rp);
         tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) rs[x] = (c * 32 + x < nvalid) ? rs[x] : 0xff800000u;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-          float ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = c * 32 + 2 * x + e;
-            const float pv = col < nvalid ? ex2_approx(fmaf(__uint_as_float(rs[2 * x + e]), p.scale_log2, -lse2)) : 0.f;
-            ds[e] = pv * (__uint_as_float(rp[2 * x + e]) - dlt) * p.scale;
-          }
-          pk[x] = pack_bf16x2(ds[0], ds[1]);
+          // P = 2^(s * scale_log2 - lse2); dS = P * (dP * scale - Delta * scale)
+          float a0, a1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2, neg_lse2),
+                      a0, a1);
+          const uint64_t pv = f32x2(ex2_approx(a0), ex2_approx(a1));
+          const uint64_t t =
+              fma_f32x2(f32x2(__uint_as_float(rp[2 * x]), __uint_as_float(rp[2 * x + 1])), sc2, neg_dlt_s);
+          float d0, d1;
+          f32x2_split(mul_f32x2(pv, t), d0, d1);
+          pk[x] = pack_bf16x2(d0, d1);
         }
         tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_A : tb) + c * 16, pk);
       }
@@ -733,8 +744,8 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int qp = itr.q0() + col;
         const bool qv = qp < itr.q_valid_hi;
         const int64_t gr = thd_row(si.start + qp, itr.head(), p.hpg_q, p.T);
-        vb[col] = qv ? __ldg(p.lse + gr) * kLog2e : 0.f;
-        vb[BN + col] = (qv && DO_DK) ? __ldg(p.delta + gr) : 0.f;
+        vb[col] = qv ? -__ldg(p.lse + gr) * kLog2e : 0.f;                 // -LSE in log2 units
+        vb[BN + col] = (qv && DO_DK) ? -__ldg(p.delta + gr) * p.scale : 0.f;  // -Delta * scale
       }
       mbar_arrive(vec_ready + wg);
       ok = __all_sync(0xffffffffu, mbar_wait(vec_ready + wg, k & 1, abort_flag));
@@ -747,25 +758,40 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       // query column c is visible to this key row iff q0+c >= k_pos and q0+c < q_valid_hi
       const int c_lo = k_valid ? max(0, k_pos - q0) : BN;
       const int c_hi = k_valid ? itr.q_valid_hi - q0 : 0;
+      // only contributions that cross the causal diagonal or a ragged end
+      // need a mask: hidden scores become -inf, so P and dS come out 0
+      const bool masked = __any_sync(0xffffffffu, c_lo > 0 || c_hi < BN);
+      const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2), sc2 = f32x2(p.scale, p.scale);
       uint32_t rs[32], rp[32];
 #pragma unroll
       for (int c = c_first; c < c_first + NC; ++c) {
         tmem_ld32(tb + c * 32, rs);
         if (DO_DK) tmem_ld32(tb + BN + c * 32, rp);
         tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int col = c * 32 + x;
+            rs[x] = (col >= c_lo && col < c_hi) ? rs[x] : 0xff800000u;
+          }
+        }
+        const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(vb + c * 32);        // -LSE2 pairs
+        const uint64_t* nds = reinterpret_cast<const uint64_t*>(vb + BN + c * 32);   // -Delta*scale pairs
         uint32_t pk[16], dk[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-          float pv[2], ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = c * 32 + 2 * x + e;
-            const bool vis = col >= c_lo && col < c_hi;
-            pv[e] = vis ? ex2_approx(fmaf(__uint_as_float(rs[2 * x + e]), p.scale_log2, -vb[col])) : 0.f;
-            if (DO_DK) ds[e] = pv[e] * (__uint_as_float(rp[2 * x + e]) - vb[BN + col]) * p.scale;
+          // P = 2^(s * scale_log2 - lse2); dS = P * (dP * scale - Delta * scale)
+          float a0, a1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2, nl2[x]),
+                      a0, a1);
+          const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+          pk[x] = pack_bf16x2(p0, p1);
+          if (DO_DK) {
+            const uint64_t t = fma_f32x2(f32x2(__uint_as_float(rp[2 * x]), __uint_as_float(rp[2 * x + 1])), sc2, nds[x]);
+            float d0, d1;
+            f32x2_split(mul_f32x2(f32x2(p0, p1), t), d0, d1);
+            dk[x] = pack_bf16x2(d0, d1);
           }
-          pk[x] = pack_bf16x2(pv[0], pv[1]);
-          if (DO_DK) dk[x] = pack_bf16x2(ds[0], ds[1]);
         }
         if (DO_DV) tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_AP : tb) + c * 16, pk);
         if (DO_DK) tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_AD : tb + BN) + c * 16, dk);
