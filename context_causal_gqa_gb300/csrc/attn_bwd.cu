@@ -396,20 +396,22 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         auto slot_mn = [&](int s2) { return slot_mn0 + s2 * kSlotStep; };
         ok = mbar_wait(res_full, 0, abort_flag);
         tc_fence_after();
-        // S and dP of tile j into buffer j % 2
+        // S and dP of tile j into buffer j % 2.  dP goes first: V_j is released
+        // right after it, so K_{j+1} (which reuses V_j's slot when slots are
+        // few) is loading for a whole tile before S of tile j+1 needs it.
         auto issue_sp = [&](int j) -> bool {
           const int tv = 2 * j, tk = 2 * j + 1;
           const int sv = tv % NSLOT, sk = tk % NSLOT;
           const int b = j % Cfg::NBUF;
           const uint32_t buf = tmem + b * Cfg::T_BUF;
-          if (!mbar_wait(full + sk, (tk / NSLOT) & 1, abort_flag)) return false;
-          tc_fence_after();
-          mma_kk<BM, BN, D>(buf, q_desc, slot_k(sk));
           if (!mbar_wait(full + sv, (tv / NSLOT) & 1, abort_flag)) return false;
           tc_fence_after();
           mma_kk<BM, BN, D>(buf + BN, do_desc, slot_k(sv));
-          umma_commit(s_full + b);
           umma_commit(empty + sv);
+          if (!mbar_wait(full + sk, (tk / NSLOT) & 1, abort_flag)) return false;
+          tc_fence_after();
+          mma_kk<BM, BN, D>(buf, q_desc, slot_k(sk));
+          umma_commit(s_full + b);
           return true;
         };
         int j_sp = 0;
@@ -664,17 +666,20 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           const int sq = tq % NSLOT, sdo = tdo % NSLOT;
           const int b = j % Cfg::NBUF;
           const uint32_t buf = tmem + b * Cfg::T_BUF;
-          if (!mbar_wait(full + sq, (tq / NSLOT) & 1, abort_flag)) return false;
-          tc_fence_after();
-          mma_kk<BM, BN, D>(buf, k_desc, slot_k(sq));
+          // dP^T first: with dK only, dO_i is released right after it, so
+          // Q_{i+1} (which reuses dO_i's slot when slots are few) is loading
+          // for a whole contribution before S^T of i+1 needs it
           if (DO_DK) {
             if (!mbar_wait(full + sdo, (tdo / NSLOT) & 1, abort_flag)) return false;
             tc_fence_after();
             mma_kk<BM, BN, D>(buf + BN, v_desc, slot_k(sdo));
+            if (MODE == KvMode::kDkOnly) umma_commit(empty + sdo);  // dO_i done after dP^T
           }
+          if (!mbar_wait(full + sq, (tq / NSLOT) & 1, abort_flag)) return false;
+          tc_fence_after();
+          mma_kk<BM, BN, D>(buf, k_desc, slot_k(sq));
           umma_commit(s_full + b);
           if (MODE == KvMode::kDvOnly) umma_commit(empty + sq);     // Q_i done after S^T
-          if (MODE == KvMode::kDkOnly) umma_commit(empty + sdo);    // dO_i done after dP^T
           return true;
         };
         int j_sp = 0;
