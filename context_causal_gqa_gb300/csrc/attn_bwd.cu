@@ -897,7 +897,7 @@ using Dq128 = DqCfg<128, 64, 8, 2>;
 #endif
 using Dq256 = DqCfg<256, CCG_BWD256_BN, (CCG_BWD256_BN == 32 ? 6 : 3), CCG_BWD256_NBUF>;
 using Kv128 = KvCfg<128, KvMode::kBoth, 64, 8, 2>;
-using Kv256V = KvCfg<256, KvMode::kDvOnly, CCG_BWD256_KBN, (CCG_BWD256_KBN == 32 ? 8 : 4), 2>;
+using Kv256V = KvCfg<256, KvMode::kDvOnly, CCG_BWD256_KBN, (CCG_BWD256_KBN == 32 ? 8 : 5), 2>;
 using Kv256K = KvCfg<256, KvMode::kDkOnly, CCG_BWD256_KBN, (CCG_BWD256_KBN == 32 ? 6 : 3), CCG_BWD256_NBUF>;
 
 }  // namespace
