@@ -64,26 +64,29 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a, int64_t row
       const int c = L > 0 ? pos / L : 0;
       K = c >= a.cp ? a.cp : c + 1;
     }
+    // every partial's LSE and O slice is requested before any is used: the
+    // loads depend only on the row's partial count, not on each other
+    const int64_t off = r * a.D + sub * 8;
     float l[kMaxCP];
-    float m = -INFINITY;
+    uint4 u[kMaxCP];
 #pragma unroll
     for (int s = 0; s < kMaxCP; ++s) {
-      l[s] = (s < K) ? __ldg(a.lse_parts[s] + r) : -INFINITY;
-      m = fmaxf(m, l[s]);
+      if (s < K) {
+        l[s] = __ldg(a.lse_parts[s] + r);
+        u[s] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o_parts[s]) + off));
+      } else {
+        l[s] = -INFINITY;
+      }
     }
-    const int64_t off = r * a.D + sub * 8;
+    float m = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kMaxCP; ++s) m = fmaxf(m, l[s]);
     uint4 outv;
     float lse_out;
     if (!valid || m == -INFINITY) {
       outv = make_uint4(0, 0, 0, 0);
       lse_out = -INFINITY;
     } else {
-      // issue every partial's load before using any of them
-      uint4 u[kMaxCP];
-#pragma unroll
-      for (int s = 0; s < kMaxCP; ++s)
-        if (s < K && l[s] != -INFINITY)
-          u[s] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o_parts[s]) + off));
       float sigma = 0.f;
 #pragma unroll
       for (int s = 0; s < kMaxCP; ++s)
