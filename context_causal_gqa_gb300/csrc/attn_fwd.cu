@@ -458,16 +458,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int64_t orow = thd_row(ir.seq_start + q_pos, h0 + h, p.hpg_q, p.T);
       float m = -INFINITY, l = 0.f;
       int seg_step = -1;                                // ring step of the open segment
-      // Closes the open segment once its last P V product (tile t_last) has
-      // landed: reads O out of TMEM, releases it for the next segment's first
-      // P V, and writes O / l and the LSE -- the partial of ring step `step`
-      // (modes 0, 1) or the final output (mode 2).
-      auto flush = [&](int64_t t_last, int step) -> bool {
+      // Closes a segment (running max mseg, sum lseg) once its last P V
+      // product (tile t_last) has landed: reads O out of TMEM, releases it for
+      // the next segment's first P V, and writes O / l and the LSE -- the
+      // partial of ring step `step` (modes 0, 1) or the final output (mode 2).
+      auto flush = [&](int64_t t_last, int step, float mseg, float lseg) -> bool {
         if (!__all_sync(0xffffffffu, mbar_wait(o_done + h * 4 + static_cast<int>(t_last % 4),
                                                static_cast<uint32_t>(t_last / 4) & 1, abort_flag)))
           return false;
         tc_fence_after();
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float inv_l = lseg > 0.f ? 1.f / lseg : 0.f;
         const int64_t slab = p.mode == 2 ? 0 : step;
         uint4* dst = reinterpret_cast<uint4*>(p.o + slab * p.o_slab + orow * D);
         uint32_t r[32];
@@ -491,125 +491,145 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
           }
         }
-        if (valid) p.lse[slab * p.lse_slab + orow] = (m + __log2f(l)) * kLn2;
+        if (valid) p.lse[slab * p.lse_slab + orow] = (mseg + __log2f(lseg)) * kLn2;
         return true;
       };
       int n = 0;                                        // tiles of this item (counted as they go)
-      for (int j = 0;; ++j, kt_it.next()) {
+      // A segment that ends inside the item (its ring step is over) is read
+      // out after the next segment's first P has been handed to the MMA warp,
+      // so that the tensor core finishes the last P V meanwhile.
+      bool pend = false;
+      float pm = 0.f, pl = 0.f;
+      int pstep = -1;
+      for (int j = 0;; ++j) {
         const int64_t t = gs + j;
         const bool end = kt_it.done;
-        const bool seg_open = !end && new_segment(p.mode, j, kt_it.s, seg_step);
-        if ((end || seg_open) && j > 0) {
-          // the open segment is complete: its ring step or the item ended
-          ok = flush(t - 1, seg_step);
+        if (end) {
+          if (j > 0) {                                  // the item's last segment
+            pend = true;
+            pm = m;
+            pl = l;
+            pstep = seg_step;
+          }
+        } else {
+          const bool seg_open = new_segment(p.mode, j, kt_it.s, seg_step);
+          if (seg_open) {
+            pend = j > 0;
+            pm = m;
+            pl = l;
+            pstep = seg_step;
+            m = -INFINITY;
+            l = 0.f;
+            seg_step = kt_it.s;
+          }
+          const int buf = static_cast<int>(t % SBUF);
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(s_full + h * SBUF + buf, static_cast<uint32_t>(t / SBUF) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const int k0 = kt_it.k0();
+          // keys visible to this row: k < kend (segment end, and k <= q_pos on the diagonal chunk)
+          const int kend = kt_it.diag ? min(kt_it.hi, q_pos + 1) : kt_it.hi;
+          const int nvalid = kend - k0;                     // may be <= 0 or >= BN
+          const uint32_t t_s = t_head + buf * BN;
+          // S row columns held in registers at once: the whole row when the
+          // register budget allows (one TMEM round trip), else halves
+          constexpr int HOLD = (NH == 1) ? BN : 64;
+          uint32_t sr[HOLD];
+          // Only tiles that cross a row's last visible key need a mask; there
+          // the hidden scores are set to -inf in registers, so that the max
+          // ignores them and their probabilities come out exactly 0.
+          const bool masked = __any_sync(0xffffffffu, nvalid < BN);
+          auto load_s = [&](int g0) {
+#pragma unroll
+            for (int c = 0; c < HOLD / 32; ++c)
+              tmem_ld32(t_s + g0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
+            tmem_wait_ld();
+            if (masked) {
+#pragma unroll
+              for (int x = 0; x < HOLD; ++x) sr[x] = (g0 + x < nvalid) ? sr[x] : 0xff800000u;
+            }
+          };
+          // max of the raw scores, scaled once (the scale is positive, and a
+          // correctly rounded product preserves order)
+          float mxr = -INFINITY;
+#pragma unroll
+          for (int g0 = 0; g0 < BN; g0 += HOLD) {
+            load_s(g0);
+#pragma unroll
+            for (int x = 0; x < HOLD; x += 2) mxr = fmax3(mxr, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
+          }
+          const float mx = mxr * p.scale_log2;
+          float alpha = 1.f;
+          if (mx > m) {
+            if (m == -INFINITY) {
+              m = mx;
+            } else if (mx > m + kRescaleThreshold) {
+              alpha = ex2_approx(m - mx);
+              m = mx;
+            }
+          }
+          const float m_use = (m == -INFINITY) ? 0.f : m;
+          // p = 2^(s * scale_log2 - m), two columns per packed FMA
+          const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2);
+          const uint64_t negm2 = f32x2(-m_use, -m_use);
+          uint64_t psum2 = f32x2(0.f, 0.f);
+#pragma unroll
+          for (int g0 = 0; g0 < BN; g0 += HOLD) {
+            if (HOLD < BN) load_s(g0);
+#pragma unroll
+            for (int c = 0; c < HOLD / 32; ++c) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int x = 0; x < 16; ++x) {
+                const int cl = c * 32 + 2 * x;
+                float a0, a1;
+                f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[cl]), __uint_as_float(sr[cl + 1])), scale2, negm2), a0,
+                            a1);
+                const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+                psum2 = add_f32x2(psum2, f32x2(p0, p1));
+                pk[x] = pack_bf16x2(p0, p1);
+              }
+              tmem_st16(t_s + (g0 + c * 32) / 2, pk);
+            }
+          }
+          tmem_wait_st();
+          float ps0, ps1;
+          f32x2_split(psum2, ps0, ps1);
+          l = l * alpha + (ps0 + ps1);
+          // rescale the running O (rare: the reference max grew past the
+          // threshold) once the previous P V product has landed
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            const int64_t tp1 = t - 1;                     // alpha != 1: not a segment's first tile
+            ok = __all_sync(0xffffffffu, mbar_wait(o_done + h * 4 + static_cast<int>(tp1 % 4),
+                                                   static_cast<uint32_t>(tp1 / 4) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t r[32];
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              tmem_ld32(t_o + c * 32, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+              tmem_st32(t_o + c * 32, r);
+            }
+            tmem_wait_st();
+          }
+          if (row == 0) seg_flag[h * SBUF + buf] = seg_open ? 1 : 0;
+          tc_fence_before();
+          mbar_arrive(p_full + h * SBUF + buf);
+        }
+        if (pend) {
+          pend = false;
+          ok = flush(t - 1, pstep, pm, pl);              // the segment ended with tile t - 1
           if (!ok) break;
         }
         if (end) {
           n = j;
           break;
         }
-        if (seg_open) {
-          m = -INFINITY;
-          l = 0.f;
-          seg_step = kt_it.s;
-        }
-        const int buf = static_cast<int>(t % SBUF);
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(s_full + h * SBUF + buf, static_cast<uint32_t>(t / SBUF) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        const int k0 = kt_it.k0();
-        // keys visible to this row: k < kend (segment end, and k <= q_pos on the diagonal chunk)
-        const int kend = kt_it.diag ? min(kt_it.hi, q_pos + 1) : kt_it.hi;
-        const int nvalid = kend - k0;                     // may be <= 0 or >= BN
-        const uint32_t t_s = t_head + buf * BN;
-        // S row columns held in registers at once: the whole row when the
-        // register budget allows (one TMEM round trip), else halves
-        constexpr int HOLD = (NH == 1) ? BN : 64;
-        uint32_t sr[HOLD];
-        // Only tiles that cross a row's last visible key need a mask; there
-        // the hidden scores are set to -inf in registers, so that the max
-        // ignores them and their probabilities come out exactly 0.
-        const bool masked = __any_sync(0xffffffffu, nvalid < BN);
-        auto load_s = [&](int g0) {
-#pragma unroll
-          for (int c = 0; c < HOLD / 32; ++c)
-            tmem_ld32(t_s + g0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
-          tmem_wait_ld();
-          if (masked) {
-#pragma unroll
-            for (int x = 0; x < HOLD; ++x) sr[x] = (g0 + x < nvalid) ? sr[x] : 0xff800000u;
-          }
-        };
-        // max of the raw scores, scaled once (the scale is positive, and a
-        // correctly rounded product preserves order)
-        float mxr = -INFINITY;
-#pragma unroll
-        for (int g0 = 0; g0 < BN; g0 += HOLD) {
-          load_s(g0);
-#pragma unroll
-          for (int x = 0; x < HOLD; x += 2) mxr = fmax3(mxr, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
-        }
-        const float mx = mxr * p.scale_log2;
-        float alpha = 1.f;
-        if (mx > m) {
-          if (m == -INFINITY) {
-            m = mx;
-          } else if (mx > m + kRescaleThreshold) {
-            alpha = ex2_approx(m - mx);
-            m = mx;
-          }
-        }
-        const float m_use = (m == -INFINITY) ? 0.f : m;
-        // p = 2^(s * scale_log2 - m), two columns per packed FMA
-        const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2);
-        const uint64_t negm2 = f32x2(-m_use, -m_use);
-        uint64_t psum2 = f32x2(0.f, 0.f);
-#pragma unroll
-        for (int g0 = 0; g0 < BN; g0 += HOLD) {
-          if (HOLD < BN) load_s(g0);
-#pragma unroll
-          for (int c = 0; c < HOLD / 32; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int x = 0; x < 16; ++x) {
-              const int cl = c * 32 + 2 * x;
-              float a0, a1;
-              f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[cl]), __uint_as_float(sr[cl + 1])), scale2, negm2), a0,
-                          a1);
-              const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-              psum2 = add_f32x2(psum2, f32x2(p0, p1));
-              pk[x] = pack_bf16x2(p0, p1);
-            }
-            tmem_st16(t_s + (g0 + c * 32) / 2, pk);
-          }
-        }
-        tmem_wait_st();
-        float ps0, ps1;
-        f32x2_split(psum2, ps0, ps1);
-        l = l * alpha + (ps0 + ps1);
-        // rescale the running O (rare: the reference max grew past the
-        // threshold) once the previous P V product has landed
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const int64_t tp1 = t - 1;                     // alpha != 1: not a segment's first tile
-          ok = __all_sync(0xffffffffu, mbar_wait(o_done + h * 4 + static_cast<int>(tp1 % 4),
-                                                 static_cast<uint32_t>(tp1 / 4) & 1, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-          uint32_t r[32];
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            tmem_ld32(t_o + c * 32, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
-            tmem_st32(t_o + c * 32, r);
-          }
-          tmem_wait_st();
-        }
-        if (row == 0) seg_flag[h * SBUF + buf] = seg_open ? 1 : 0;
-        tc_fence_before();
-        mbar_arrive(p_full + h * SBUF + buf);
+        kt_it.next();
       }
       if (!ok) break;
       gs += n;
