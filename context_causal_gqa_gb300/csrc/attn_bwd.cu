@@ -885,20 +885,11 @@ cudaError_t launch_kv(const CUtensorMap* m, const BwdParams& p, int grid_items, 
 
 // Tile shapes.  D = 256 is limited by shared memory: the resident 128-row
 // tiles take 128 KB (Q, dO) or 128 KB (K, V), so streamed tiles are 32 rows.
-#ifndef CCG_BWD256_BN
-#define CCG_BWD256_BN 64
-#endif
 using Dq128 = DqCfg<128, 64, 8, 2>;
-#ifndef CCG_BWD256_KBN
-#define CCG_BWD256_KBN CCG_BWD256_BN
-#endif
-#ifndef CCG_BWD256_NBUF
-#define CCG_BWD256_NBUF 1
-#endif
-using Dq256 = DqCfg<256, CCG_BWD256_BN, (CCG_BWD256_BN == 32 ? 6 : 3), CCG_BWD256_NBUF>;
+using Dq256 = DqCfg<256, 64, 3, 1>;
 using Kv128 = KvCfg<128, KvMode::kBoth, 64, 8, 2>;
-using Kv256V = KvCfg<256, KvMode::kDvOnly, CCG_BWD256_KBN, (CCG_BWD256_KBN == 32 ? 8 : 5), 2>;
-using Kv256K = KvCfg<256, KvMode::kDkOnly, CCG_BWD256_KBN, (CCG_BWD256_KBN == 32 ? 6 : 3), CCG_BWD256_NBUF>;
+using Kv256V = KvCfg<256, KvMode::kDvOnly, 64, 5, 2>;
+using Kv256K = KvCfg<256, KvMode::kDkOnly, 64, 3, 1>;
 
 }  // namespace
 
