@@ -885,7 +885,7 @@ cudaError_t launch_kv(const CUtensorMap* m, const BwdParams& p, int grid_items, 
 
 // Tile shapes.  D = 256 is limited by shared memory: the resident 128-row
 // tiles take 128 KB (Q, dO) or 128 KB (K, V), so streamed tiles are 32 rows.
-using Dq128 = DqCfg<128, 64, 8, 2>;
+using Dq128 = DqCfg<128, 128, 5, 1>;
 using Dq256 = DqCfg<256, 64, 3, 1>;
 using Kv128 = KvCfg<128, KvMode::kBoth, 64, 8, 2>;
 using Kv256V = KvCfg<256, KvMode::kDvOnly, 64, 5, 2>;
