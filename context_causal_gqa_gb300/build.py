@@ -7,7 +7,9 @@ driver library at link time (cuTensorMapEncodeTiled is fetched at run time).
 """
 
 import concurrent.futures
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -42,11 +44,29 @@ def _deps():
                                                                os.path.abspath(__file__)]
 
 
+def _fingerprint():
+    """Hash of every source the library is built from, the flags and the
+    machine type: a library built from other sources, or on another
+    architecture, is never reused (modification times alone can mislead when
+    a tree is copied between machines)."""
+    h = hashlib.sha256()
+    for d in sorted(_deps()):
+        h.update(d.encode())
+        with open(d, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(flags() + ARCH).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
+STAMP = LIB + ".fingerprint"
+
+
 def up_to_date():
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(d) <= t for d in _deps())
+    with open(STAMP) as f:
+        return f.read().strip() == _fingerprint()
 
 
 def _compile(src, verbose, extra=()):
@@ -80,6 +100,8 @@ def build(force=False, verbose=False, extra=()):
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(_fingerprint() if not extra else "custom flags")
     return LIB
 
 
