@@ -109,12 +109,12 @@ struct KvCfg {
   static constexpr int T_DV = NBUF * T_BUF;
   static constexpr int T_DK = M == KvMode::kBoth ? NBUF * T_BUF + D : NBUF * T_BUF;
   static constexpr int ACC_END = NBUF * T_BUF + (M == KvMode::kBoth ? 2 * D : D);
-  // P^T / dS^T (BF16 A operands): in place over S^T / dP^T when one warpgroup
-  // owns the whole tile, in their own regions when the columns are split
-  static constexpr int T_AP = SPLIT ? ACC_END : -1;
-  static constexpr int T_AD = SPLIT ? ACC_END + (M == KvMode::kDkOnly ? 0 : BN / 2) : -1;
+  // P^T / dS^T (BF16 A operands) are packed in place over S^T / dP^T: over
+  // the tile's first BN/2 columns when one warpgroup owns the tile, over the
+  // first half of each warpgroup's own columns when the columns are split
+  // (a warpgroup never writes columns the other one still reads)
   static constexpr int TMEM_COLS = 512;
-  static_assert(ACC_END + (SPLIT ? (M == KvMode::kBoth ? BN : BN / 2) : 0) <= 512, "TMEM");
+  static_assert(ACC_END <= 512, "TMEM");
   static_assert((SPLIT ? BN / 2 : BN) % 32 == 0, "softmax chunking");
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
 };
@@ -268,6 +268,18 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint64_t a_desc, uint64_
 #pragma unroll
   for (int k = 0; k < KD / 16; ++k)
     umma_ss(d_tmem, a_desc + kmajor_step(MROWS, k), b_desc + kmajor_step(NROWS, k), idesc, k > 0 ? 1u : 0u);
+}
+
+// As mma_tn, with A packed per warpgroup when the columns are split: the
+// first KROWS/2 rows of A at a_tmem, the second half KROWS/2 columns later.
+template <int KROWS, int D, bool SPLIT_A>
+__device__ __forceinline__ void mma_tn_split(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, false, true);
+  constexpr int KPW = SPLIT_A ? KROWS / 32 : KROWS / 16;   // k-steps per packed run
+#pragma unroll
+  for (int k = 0; k < KROWS / 16; ++k)
+    umma_ts(d_tmem, a_tmem + (k / KPW) * (KROWS / 2) + (k % KPW) * 8, b_desc + mnmajor_step(k), idesc,
+            (accumulate || k > 0) ? 1u : 0u);
 }
 
 // D[tmem, M=128 x N=D] (+)= A[tmem bf16, 128 x KROWS] * B[smem tile KROWS rows x D, MN-major];
@@ -699,10 +711,8 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (!ok) break;
           }
           tc_fence_after();
-          const uint32_t a_p = Cfg::SPLIT ? tmem + Cfg::T_AP : buf;
-          const uint32_t a_d = Cfg::SPLIT ? tmem + Cfg::T_AD : buf + BN;
-          if (DO_DV) mma_tn<BN, D>(tmem + Cfg::T_DV, a_p, slot_mn(sdo), j > 0);
-          if (DO_DK) mma_tn<BN, D>(tmem + Cfg::T_DK, a_d, slot_mn(sq), j > 0);
+          if (DO_DV) mma_tn_split<BN, D, Cfg::SPLIT>(tmem + Cfg::T_DV, buf, slot_mn(sdo), j > 0);
+          if (DO_DK) mma_tn_split<BN, D, Cfg::SPLIT>(tmem + Cfg::T_DK, buf + BN, slot_mn(sq), j > 0);
           if (MODE != KvMode::kDkOnly) umma_commit(empty + sdo);
           if (MODE != KvMode::kDvOnly) umma_commit(empty + sq);
           if (!ahead.done) {
@@ -798,8 +808,9 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             dk[x] = pack_bf16x2(d0, d1);
           }
         }
-        if (DO_DV) tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_AP : tb) + c * 16, pk);
-        if (DO_DK) tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_AD : tb + BN) + c * 16, dk);
+        const int packed = c_first * 32 + (c - c_first) * 16;   // in place, own columns
+        if (DO_DV) tmem_st16(tb + packed, pk);
+        if (DO_DK) tmem_st16(tb + BN + packed, dk);
       }
       mbar_arrive(vec_free + wg);          // done reading this contribution's LSE/Delta
       tmem_wait_st();
@@ -887,7 +898,7 @@ cudaError_t launch_kv(const CUtensorMap* m, const BwdParams& p, int grid_items, 
 // tiles take 128 KB (Q, dO) or 128 KB (K, V), so streamed tiles are 32 rows.
 using Dq128 = DqCfg<128, 128, 5, 1>;
 using Dq256 = DqCfg<256, 64, 3, 1>;
-using Kv128 = KvCfg<128, KvMode::kBoth, 64, 8, 2>;
+using Kv128 = KvCfg<128, KvMode::kBoth, 128, 4, 1>;
 using Kv256V = KvCfg<256, KvMode::kDvOnly, 64, 5, 2>;
 using Kv256K = KvCfg<256, KvMode::kDkOnly, 64, 3, 1>;
 
