@@ -899,7 +899,7 @@ cudaError_t launch_kv(const CUtensorMap* m, const BwdParams& p, int grid_items, 
 using Dq128 = DqCfg<128, 128, 5, 1>;
 using Dq256 = DqCfg<256, 64, 3, 1>;
 using Kv128 = KvCfg<128, KvMode::kBoth, 128, 4, 1>;
-using Kv256V = KvCfg<256, KvMode::kDvOnly, 64, 5, 2>;
+using Kv256V = KvCfg<256, KvMode::kDvOnly, 128, 2, 1>;
 using Kv256K = KvCfg<256, KvMode::kDkOnly, 64, 3, 1>;
 
 }  // namespace
