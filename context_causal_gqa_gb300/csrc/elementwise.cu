@@ -5,6 +5,8 @@
 // All use 16-byte vector loads/stores and 64-bit row arithmetic.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -41,8 +43,9 @@ struct SeqCache {
 };
 
 // Each block merges a contiguous range of rows (better DRAM locality and a
-// cached sequence lookup); TPR threads per row, 16 bytes each.
-template <int TPR>
+// cached sequence lookup); TPR threads per row, 16 bytes each.  NP bounds the
+// number of partials (registers for NP 16-byte slices per thread).
+template <int TPR, int NP>
 __global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a, int64_t rows_per_block) {
   if (a.status != nullptr && status_bad(a.status)) return;
   const int sub = threadIdx.x % TPR;
@@ -67,10 +70,10 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a, int64_t row
     // every partial's LSE and O slice is requested before any is used: the
     // loads depend only on the row's partial count, not on each other
     const int64_t off = r * a.D + sub * 8;
-    float l[kMaxCP];
-    uint4 u[kMaxCP];
+    float l[NP];
+    uint4 u[NP];
 #pragma unroll
-    for (int s = 0; s < kMaxCP; ++s) {
+    for (int s = 0; s < NP; ++s) {
       if (s < K) {
         l[s] = __ldg(a.lse_parts[s] + r);
         u[s] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o_parts[s]) + off));
@@ -80,7 +83,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a, int64_t row
     }
     float m = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < kMaxCP; ++s) m = fmaxf(m, l[s]);
+    for (int s = 0; s < NP; ++s) m = fmaxf(m, l[s]);
     uint4 outv;
     float lse_out;
     if (!valid || m == -INFINITY) {
@@ -89,12 +92,12 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a, int64_t row
     } else {
       float sigma = 0.f;
 #pragma unroll
-      for (int s = 0; s < kMaxCP; ++s)
+      for (int s = 0; s < NP; ++s)
         if (s < K) sigma += ex2_approx((l[s] - m) * kLog2e);
       lse_out = m + __logf(sigma);
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-      for (int s = 0; s < kMaxCP; ++s) {
+      for (int s = 0; s < NP; ++s) {
         if (s < K && l[s] != -INFINITY) {
           const float w = ex2_approx((l[s] - lse_out) * kLog2e);
           float f[8];
@@ -229,9 +232,19 @@ cudaError_t launch_lse_merge(const MergeArgs& a, int num_sms, cudaStream_t strea
   const int tpr = a.D / 8;
   const int grid = grid_for(a.rows, 256 / tpr, num_sms * 16);
   const int64_t rpb = (a.rows + grid - 1) / grid;
-  if (tpr == 16) lse_merge_kernel<16><<<grid, 256, 0, stream>>>(a, rpb);
-  else if (tpr == 32) lse_merge_kernel<32><<<grid, 256, 0, stream>>>(a, rpb);
-  else return cudaErrorInvalidValue;
+  auto go = [&](auto np) -> cudaError_t {
+    constexpr int NP = decltype(np)::value;
+    if (tpr == 16) lse_merge_kernel<16, NP><<<grid, 256, 0, stream>>>(a, rpb);
+    else if (tpr == 32) lse_merge_kernel<32, NP><<<grid, 256, 0, stream>>>(a, rpb);
+    else return cudaErrorInvalidValue;
+    return cudaSuccess;
+  };
+  cudaError_t e;
+  if (a.nparts <= 2) e = go(std::integral_constant<int, 2>{});
+  else if (a.nparts <= 4) e = go(std::integral_constant<int, 4>{});
+  else if (a.nparts <= 8) e = go(std::integral_constant<int, 8>{});
+  else e = go(std::integral_constant<int, kMaxCP>{});
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
