@@ -663,7 +663,6 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
 
 }  // namespace
 
-int fwd_kv_tile_rows(int D) { return D == 128 ? FwdCfg<128, 2>::BN : FwdCfg<256, 1>::BN; }
 int fwd_heads_per_cta(int D, int group) { return (D == 128 && group % 2 == 0) ? 2 : 1; }
 
 // Persistent launch over the combined work list: one CTA per SM (the work

@@ -262,8 +262,4 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 }  // namespace ccg
