@@ -282,12 +282,14 @@ def run_ccg(args):
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event between consecutive steps: the whole region and each step
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    e0, e1 = marks[0], marks[-1]
     e0.record(stream)
     launches = 0
-    for _ in range(args.steps):
+    for i in range(args.steps):
         launches += step.run()
-    e1.record(stream)
+        marks[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     barrier()
@@ -295,6 +297,7 @@ def run_ccg(args):
     step.check()
     ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(ms)
+    step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
     flops = w.flops_fwd_bwd()
     value = job_throughput(flops, world, ms_max)
 
@@ -382,6 +385,8 @@ def run_ccg(args):
                 "config": cfg, "frac_of_peak": round(value / world / pk["bf16_sustained"], 4),
                 "peak_tflops": pk["bf16_sustained"], "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches, "clocks": clk, "kernels": kernels,
+                "step_ms": {"median": round(statistics.median(step_ms), 3), "min": round(min(step_ms), 3),
+                            "max": round(max(step_ms), 3)},
                 "peak_mem_gb": round(torch.cuda.max_memory_allocated(dev) / 1e9, 2)}
         print(json.dumps(line))
     if pg is not None:
