@@ -867,12 +867,9 @@ cudaError_t set_smem(K kern, int bytes) {
 template <class Cfg, int D>
 cudaError_t launch_dq(const CUtensorMap* m, const BwdParams& p, int grid_items, cudaStream_t s) {
   const int smem = Cfg::SMEM_TOTAL + 1024;
-  static bool once = false;
-  if (!once) {
-    cudaError_t e = set_smem(attn_bwd_dq_kernel<Cfg, D>, smem);
-    if (e != cudaSuccess) return e;
-    once = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_dq_kernel<Cfg, D>, smem); });
+  if (e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(grid_items) * p.hq;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
   attn_bwd_dq_kernel<Cfg, D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(m[0], m[1], m[2], m[3], p);
@@ -882,12 +879,9 @@ cudaError_t launch_dq(const CUtensorMap* m, const BwdParams& p, int grid_items, 
 template <class Cfg, int D, KvMode MODE>
 cudaError_t launch_kv(const CUtensorMap* m, const BwdParams& p, int grid_items, cudaStream_t s) {
   const int smem = Cfg::SMEM_TOTAL + 1024;
-  static bool once = false;
-  if (!once) {
-    cudaError_t e = set_smem(attn_bwd_kv_kernel<Cfg, D, MODE>, smem);
-    if (e != cudaSuccess) return e;
-    once = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_kv_kernel<Cfg, D, MODE>, smem); });
+  if (e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(grid_items) * p.hkv;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
   attn_bwd_kv_kernel<Cfg, D, MODE><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(m[0], m[1], m[2], m[3], p);

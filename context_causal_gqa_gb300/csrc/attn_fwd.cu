@@ -650,13 +650,11 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             const FwdParams& p, int grid, cudaStream_t stream) {
   using Cfg = FwdCfg<D, NH>;
   auto kern = attn_fwd_kernel<D, NH>;
-  static bool attr_set = false;
+  static std::atomic<uint64_t> attr_done{0};
   const int smem = Cfg::SMEM_TOTAL + 1024;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = once_per_device(
+      attr_done, [&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); });
+  if (e != cudaSuccess) return e;
   kern<<<grid, Cfg::THREADS, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

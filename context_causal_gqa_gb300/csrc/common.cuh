@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "../../include/ccg.h"
 
 namespace ccg {
@@ -88,6 +90,21 @@ __device__ __forceinline__ int find_sequence(const int32_t* __restrict__ cu_pad,
     if (static_cast<int64_t>(__ldg(cu_pad + mid)) <= t) lo = mid; else hi = mid - 1;
   }
   return lo;
+}
+
+// Runs `set` (a per-device function attribute call) once for every device
+// it is used on; concurrent first calls may both run it, which is harmless.
+template <class F>
+inline cudaError_t once_per_device(std::atomic<uint64_t>& done, F set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = set();
+  if (e != cudaSuccess) return e;
+  done.fetch_or(bit, std::memory_order_release);
+  return cudaSuccess;
 }
 
 // Launch timing hooks (defined in api.cu): no-ops unless a profile is open
