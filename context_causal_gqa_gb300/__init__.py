@@ -48,9 +48,11 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def make_desc(batch, hq, hkv, head_dim, cp, total_tokens, head_groups=1, scale=0.0):
+def make_desc(batch, hq, hkv, head_dim, cp, total_tokens, head_groups=1, scale=0.0, pitches=(0, 0, 0, 0)):
+    """pitches: row pitch in elements of q, k, v, dO (0 = dense)."""
     return AttnDesc(batch=batch, hq=hq, hkv=hkv, head_dim=head_dim, causal=1, cp=cp,
-                    head_groups=head_groups, reserved=0, total_tokens=total_tokens, softmax_scale=scale)
+                    head_groups=head_groups, reserved=0, total_tokens=total_tokens, softmax_scale=scale,
+                    q_pitch=pitches[0], k_pitch=pitches[1], v_pitch=pitches[2], do_pitch=pitches[3])
 
 
 def workspace_size(desc, kind):
@@ -79,27 +81,51 @@ def _new_status(device):
     return torch.zeros(1, dtype=torch.int32, device=device)
 
 
-def _desc_for(q, k, cu_seqlens, cp, head_groups, scale):
+def _dense(t, name):
+    """Outputs, o and lse are dense: a strided view there would be misread."""
+    if t is not None and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _pitch(t, name):
+    """Row pitch of a [T, H, D] input: 0 when dense, else its token stride
+    (heads must stay contiguous, stride D; D contiguous)."""
+    if t is None or t.dim() != 3:
+        return 0
+    T, H, D = t.shape
+    if t.stride(2) != 1 or t.stride(1) != D:
+        raise ValueError(f"{name}: heads and head_dim must be contiguous (strides (*, {D}, 1)), got {t.stride()}")
+    return 0 if t.stride(0) == H * D or T <= 1 else t.stride(0)
+
+
+def _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=None, do=None):
     hg = head_groups
     if q.dim() == 4:        # head-split [G][T][H/G][D]
+        for t, name in ((q, "q"), (k, "k"), (v, "v"), (do, "do")):
+            _dense(t, name)
         hg = q.shape[0]
         T, hq, D = q.shape[1], q.shape[0] * q.shape[2], q.shape[3]
         hkv = k.shape[0] * k.shape[2]
+        pitches = (0, 0, 0, 0)
     else:
         T, hq, D = q.shape
         hkv = k.shape[1]
-    return make_desc(cu_seqlens.numel() - 1, hq, hkv, D, cp, T, hg, scale)
+        pitches = (_pitch(q, "q"), _pitch(k, "k"), _pitch(v, "v"), _pitch(do, "do"))
+    return make_desc(cu_seqlens.numel() - 1, hq, hkv, D, cp, T, hg, scale, pitches)
 
 
 def attn_fwd(q, k, v, cu_seqlens, cu_seqlens_padded, cp, *, head_groups=1, scale=0.0, out=None, lse=None,
              workspace=None, status=None, stream=None, check=True, fused=False):
     """Forward: returns (o, lse).  q [T,Hq,D] (or [G,T,Hq/G,D]), k/v likewise, bf16 on cuda.
+    q, k, v may be row-strided views (e.g. slices of a fused QKV buffer); o is dense.
     fused=True runs ccg_attn_fwd_fused (one online softmax over all ring steps)."""
     import torch
-    desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale)
-    o = torch.empty_like(q) if out is None else out
+    desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=v)
+    o = torch.empty(q.shape, dtype=q.dtype, device=q.device) if out is None else _dense(out, "out")
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    _dense(lse, "lse")
     ws = workspace or Workspace(q.device)
     wptr, wbytes = ws.get(workspace_size(desc, 2 if fused else 0))
     st = _new_status(q.device) if status is None else status
@@ -114,7 +140,7 @@ def attn_fwd(q, k, v, cu_seqlens, cu_seqlens_padded, cp, *, head_groups=1, scale
 def attn_fwd_step(q, k, v, cu_seqlens, cu_seqlens_padded, cp, step, o_part, lse_part, *, head_groups=1,
                   scale=0.0, workspace=None, status=None, stream=None, check=True):
     """One ring step's partial (o_part, lse_part), written in place (absent rows untouched)."""
-    desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale)
+    desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=v)
     ws = workspace or Workspace(q.device)
     wptr, wbytes = ws.get(workspace_size(desc, False))
     st = _new_status(q.device) if status is None else status
@@ -128,12 +154,16 @@ def attn_fwd_step(q, k, v, cu_seqlens, cu_seqlens_padded, cp, step, o_part, lse_
 
 def attn_bwd(q, k, v, o, do, lse, cu_seqlens, cu_seqlens_padded, cp, *, head_groups=1, scale=0.0,
              dq=None, dk=None, dv=None, workspace=None, status=None, stream=None, check=True):
-    """Backward: returns (dq, dk, dv)."""
+    """Backward: returns (dq, dk, dv).  q, k, v, do may be row-strided views; o and the
+    gradients are dense."""
     import torch
-    desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=v, do=do)
+    dense = lambda t: torch.empty(t.shape, dtype=t.dtype, device=t.device)  # noqa: E731
+    dq = dense(q) if dq is None else _dense(dq, "dq")
+    dk = dense(k) if dk is None else _dense(dk, "dk")
+    dv = dense(v) if dv is None else _dense(dv, "dv")
+    _dense(o, "o")
+    _dense(lse, "lse")
     ws = workspace or Workspace(q.device)
     wptr, wbytes = ws.get(workspace_size(desc, True))
     st = _new_status(q.device) if status is None else status

@@ -20,7 +20,8 @@ cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t
                         int32_t* status, cudaStream_t stream);
 cudaError_t launch_chunk_table(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp,
                                int32_t* table, int32_t* status, cudaStream_t stream);
-cudaError_t launch_bwd_dot(const void* o, const void* dout, int64_t rows, int D, float* delta,
+cudaError_t launch_bwd_dot(const void* o, const void* dout, int64_t rows, int D, int dout_heads,
+                           int64_t dout_pitch, float* delta,
                            const int32_t* status, int num_sms, cudaStream_t stream);
 cudaError_t launch_thd_permute(bool pack, const void* src, void* dst, const int32_t* cu_pad, int B,
                                int64_t T, int H, int D, int cp, int32_t* status, int num_sms,
@@ -113,7 +114,25 @@ ccg_status check_desc(const ccg_attn_desc* d) {
   // 32-bit coordinates inside the kernels and TMA maps
   if (d->total_tokens * d->head_groups >= (int64_t(1) << 31)) return CCG_ERR_UNSUPPORTED;
   if (d->batch > (1 << 20)) return CCG_ERR_UNSUPPORTED;
+  const int64_t pitches[4] = {d->q_pitch, d->k_pitch, d->v_pitch, d->do_pitch};
+  const int64_t dense[4] = {int64_t(d->hq) * d->head_dim, int64_t(d->hkv) * d->head_dim,
+                            int64_t(d->hkv) * d->head_dim, int64_t(d->hq) * d->head_dim};
+  for (int i = 0; i < 4; ++i) {
+    if (pitches[i] == 0) continue;
+    if (pitches[i] < dense[i]) return CCG_ERR_INVALID_ARG;
+    if (pitches[i] % 8 != 0) return CCG_ERR_ALIGNMENT;     // TMA row strides are multiples of 16 bytes
+    if (d->head_groups != 1) return CCG_ERR_UNSUPPORTED;
+    if (pitches[i] >= (int64_t(1) << 36)) return CCG_ERR_UNSUPPORTED;
+  }
   return CCG_OK;
+}
+
+// Row pitch (elements) of input `which` (0 q, 1 k, 2 v, 3 dO) in its
+// head-grouped layout: the caller's pitch, or dense H/G_h * D.
+int64_t input_pitch(const ccg_attn_desc* d, int which) {
+  const int64_t p[4] = {d->q_pitch, d->k_pitch, d->v_pitch, d->do_pitch};
+  const int h = (which == 1 || which == 2) ? d->hkv : d->hq;
+  return p[which] != 0 ? p[which] : int64_t(h / d->head_groups) * d->head_dim;
 }
 
 float softmax_scale(const ccg_attn_desc* d) {
@@ -177,14 +196,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a head-grouped THD tensor: dims (D, H/G_h, G_h*T), 128-byte
+// 3-D map over a head-grouped THD tensor: dims (D, H/G_h, G_h*T), heads D
+// elements apart, rows `pitch` elements apart (dense: H/G_h * D), 128-byte
 // swizzled boxes of 64 columns x 1 head x `box_rows` rows.
-bool make_thd_map(CUtensorMap* m, const void* base, int D, int hpg, int64_t rows, int box_rows) {
+bool make_thd_map(CUtensorMap* m, const void* base, int D, int hpg, int64_t rows, int box_rows, int64_t pitch) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hpg),
                         static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(hpg) * D * 2};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(pitch) * 2};
   cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -346,7 +366,7 @@ ccg_status ccg_bwd_dot(const void* o, const void* dout, int64_t rows, int32_t he
   if (!aligned16(o) || !aligned16(dout)) return CCG_ERR_ALIGNMENT;
   if (rows == 0) return CCG_OK;
   CCG_LAUNCH("bwd_dot", reinterpret_cast<cudaStream_t>(stream),
-             launch_bwd_dot(o, dout, rows, head_dim, delta, nullptr, num_sms_cached(),
+             launch_bwd_dot(o, dout, rows, head_dim, 1, head_dim, delta, nullptr, num_sms_cached(),
                             reinterpret_cast<cudaStream_t>(stream)));
   g_last_launches = launches;
   return CCG_OK;
@@ -404,9 +424,9 @@ static ccg_status fwd_partials(const ccg_attn_desc* d, int step_only, const void
   const int64_t rows = d->total_tokens * hg;
   const int bn = 128;                                   // forward K/V tile rows
   CUtensorMap tq, tk, tv;
-  if (!make_thd_map(&tq, q, d->head_dim, d->hq / hg, rows, kQTile) ||
-      !make_thd_map(&tk, k, d->head_dim, d->hkv / hg, rows, bn) ||
-      !make_thd_map(&tv, v, d->head_dim, d->hkv / hg, rows, bn))
+  if (!make_thd_map(&tq, q, d->head_dim, d->hq / hg, rows, kQTile, input_pitch(d, 0)) ||
+      !make_thd_map(&tk, k, d->head_dim, d->hkv / hg, rows, bn, input_pitch(d, 1)) ||
+      !make_thd_map(&tv, v, d->head_dim, d->hkv / hg, rows, bn, input_pitch(d, 2)))
     return CCG_ERR_CUDA;
   CCG_LAUNCH("attn_fwd", s,
              launch_attn_fwd(tq, tk, tv, items, hdr, cu, cu_pad, o_part, lse_part, o_slab, lse_slab, status, d->cp,
@@ -533,14 +553,17 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
                          bwd_q_tile_rows(D), bwd_kv_tile_rows(D), L.cap_q, L.cap_kv, 2, -1, hdr, nullptr, dq_items,
                          kv_items, d_status, s));
   CCG_LAUNCH("bwd_dot", s,
-             launch_bwd_dot(o, dout, desc->total_tokens * desc->hq, D, delta, d_status, num_sms_cached(), s));
+             launch_bwd_dot(o, dout, desc->total_tokens * desc->hq, D, desc->hq / desc->head_groups,
+                            input_pitch(desc, 3), delta,
+                            d_status, num_sms_cached(), s));
   // maps: q, k, v, dO for each of the three backward kernels (row boxes differ)
   CUtensorMap maps[12];
   const int hq_g = desc->hq / hg, hkv_g = desc->hkv / hg;
   const void* bases[4] = {q, k, v, dout};
   const int hpgs[4] = {hq_g, hkv_g, hkv_g, hq_g};
   for (int i = 0; i < 12; ++i)
-    if (!make_thd_map(&maps[i], bases[i % 4], D, hpgs[i % 4], rows, bwd_map_rows(i, D))) return CCG_ERR_CUDA;
+    if (!make_thd_map(&maps[i], bases[i % 4], D, hpgs[i % 4], rows, bwd_map_rows(i, D), input_pitch(desc, i % 4)))
+      return CCG_ERR_CUDA;
   int kl = 0;
   if (launch_attn_bwd(maps, dq_items, kv_items, hdr, cu_seqlens, cu_seqlens_padded, lse, delta, dq, dk, dv,
                       d_status, desc->cp, desc->hq, desc->hkv, hg, desc->total_tokens, D,

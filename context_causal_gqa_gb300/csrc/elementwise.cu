@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a, int64_t row
 template <int TPR>
 __global__ void __launch_bounds__(256)
 bwd_dot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-               int64_t rows, int D, float* __restrict__ delta, const int32_t* status) {
+               int64_t rows, int D, int dout_heads, int64_t dout_pitch, float* __restrict__ delta,
+               const int32_t* status) {
   if (status != nullptr && status_bad(status)) return;
   const int sub = threadIdx.x % TPR;
   const int64_t rows_per_block = 256 / TPR;
@@ -127,9 +128,11 @@ bwd_dot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restr
   const int64_t stride = static_cast<int64_t>(gridDim.x) * rows_per_block;
   for (int64_t r = row0; r < rows; r += stride) {
     const int64_t off = r * D + sub * 8;
+    // dO row r = (token r / H, head r % H), rows dout_pitch elements apart
+    const int64_t off_do = (r / dout_heads) * dout_pitch + (r % dout_heads) * D + sub * 8;
     float a[8], b[8];
     bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(o + off)), a);
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(dout + off)), b);
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(dout + off_do)), b);
     float acc = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc = fmaf(a[i], b[i], acc);
@@ -257,14 +260,15 @@ cudaError_t launch_pad_rows(void* o, float* lse, const int32_t* cu, const int32_
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dot(const void* o, const void* dout, int64_t rows, int D, float* delta,
-                           const int32_t* status, int num_sms, cudaStream_t stream) {
+cudaError_t launch_bwd_dot(const void* o, const void* dout, int64_t rows, int D, int dout_heads,
+                           int64_t dout_pitch, float* delta, const int32_t* status, int num_sms,
+                           cudaStream_t stream) {
   const int tpr = D / 8;
   const int grid = grid_for(rows, 256 / tpr, num_sms * 16);
   auto* po = static_cast<const __nv_bfloat16*>(o);
   auto* pd = static_cast<const __nv_bfloat16*>(dout);
-  if (tpr == 16) bwd_dot_kernel<16><<<grid, 256, 0, stream>>>(po, pd, rows, D, delta, status);
-  else if (tpr == 32) bwd_dot_kernel<32><<<grid, 256, 0, stream>>>(po, pd, rows, D, delta, status);
+  if (tpr == 16) bwd_dot_kernel<16><<<grid, 256, 0, stream>>>(po, pd, rows, D, dout_heads, dout_pitch, delta, status);
+  else if (tpr == 32) bwd_dot_kernel<32><<<grid, 256, 0, stream>>>(po, pd, rows, D, dout_heads, dout_pitch, delta, status);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }

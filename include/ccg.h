@@ -84,6 +84,14 @@ typedef struct {
   int32_t reserved;       /* must be 0                                                 */
   int64_t total_tokens;   /* T = cu_seqlens_padded[B]                                  */
   float softmax_scale;    /* <= 0 selects 1/sqrt(D)                                    */
+  /* Physical row pitch of the THD inputs: elements from one token's row to the
+   * next in q, k, v and dO (e.g. q, k, v sliced out of one fused [T][Hq+2Hkv][D]
+   * projection output).  0 = dense (H*D).  A nonzero pitch is at least H*D,
+   * a multiple of 8 (16 bytes), and needs head_groups == 1; the heads of a row
+   * stay contiguous (stride D).  Outputs (o, lse, dq, dk, dv) are always dense.
+   * This is the page's physical-pitch (strided) THD input (PR, CP8 AllGather:
+   * composition with first-gradient reuse). */
+  int64_t q_pitch, k_pitch, v_pitch, do_pitch;
 } ccg_attn_desc;
 
 /* Bytes of device workspace needed for `desc` by ccg_attn_fwd (kind = 0),

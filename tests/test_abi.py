@@ -58,6 +58,17 @@ def test_workspace_size_rejects_bad_descriptors(L, kw, code):
     assert ccg.workspace_size(_desc(**kw), True) == 0
 
 
+def test_row_pitch_validation_needs_no_gpu(L):
+    dense = 4 * 128                                   # q row: Hq * D elements
+    ok = _desc(pitches=(dense + 3 * 128, 1 * 128 + 8, 2 * 128, 0))       # e.g. a fused QKV buffer
+    assert ccg.workspace_size(ok, False) > 0
+    assert ccg.workspace_size(_desc(pitches=(dense, 128, 128, dense)), True) > 0   # explicit dense
+    assert _call_fwd(L, _desc(pitches=(dense - 8, 0, 0, 0))) == 1       # pitch below H * D
+    assert _call_fwd(L, _desc(pitches=(dense + 4, 0, 0, 0))) == 3       # not a multiple of 16 bytes
+    assert _call_fwd(L, _desc(pitches=(0, 0, 0, 1004))) == 3            # dO pitch checked too
+    assert _call_fwd(L, _desc(head_groups=2, hq=4, hkv=2, pitches=(1024, 0, 0, 0))) == 2   # head-split layout
+
+
 def test_workspace_size_grows_with_problem(L):
     small, big = _desc(), _desc(total_tokens=4096)
     assert 0 < ccg.workspace_size(small, False) < ccg.workspace_size(big, False)
