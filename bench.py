@@ -220,6 +220,20 @@ def dist_setup(n_gpus):
     return rank, local, world, pg
 
 
+def bench_config(w, args, world):
+    """The `config` object of the JSON line; the same for both arms."""
+    cfg = dict(w.describe())
+    cfg["workload"] = (f"{w.name}: B={w.batch} x S={max(w.seqlens)} packed THD, Hq{w.hq}/Hkv{w.hkv}, "
+                       f"D{w.head_dim}, causal, {w.cp} emulated CP ranks ({2 * w.cp} chunks)"
+                       + (", A2A head-split pack/unpack round trip" if w.pack_roundtrip else ""))
+    cfg["l2"] = "inputs larger than L2, no flush"
+    cfg["schedule"] = args.schedule
+    fused = args.fwd == "fused" or args.schedule == "a2a"
+    cfg["forward"] = "fused online softmax" if fused else "ring-step partials + LSE merge"
+    cfg["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU, CP emulated"
+    return cfg
+
+
 def run_reference(args):
     rank, _, world, pg = dist_setup(args.gpus)
     if rank != 0:
@@ -238,7 +252,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": dict(w.describe(), workload=w.name),
+            "config": bench_config(w, args, world),
             "cpu_baseline": {"kind": "oracle", "cores": host_threads(), "sample": sample, "value": value,
                              "unit": UNIT},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -371,14 +385,7 @@ def run_ccg(args):
                          f"(FP64 numpy oracle, {t:.1f} s)"}
 
     if rank == 0:
-        cfg = dict(w.describe())
-        cfg["workload"] = (f"{w.name}: B={w.batch} x S={max(w.seqlens)} packed THD, Hq{w.hq}/Hkv{w.hkv}, "
-                           f"D{w.head_dim}, causal, {w.cp} emulated CP ranks ({2 * w.cp} chunks)"
-                           + (", A2A head-split pack/unpack round trip" if w.pack_roundtrip else ""))
-        cfg["l2"] = "inputs larger than L2, no flush"
-        cfg["schedule"] = args.schedule
-        cfg["forward"] = "fused online softmax" if step.fused else "ring-step partials + LSE merge"
-        cfg["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU, CP emulated"
+        cfg = bench_config(w, args, world)
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(ms_max, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
