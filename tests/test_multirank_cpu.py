@@ -46,3 +46,19 @@ def test_single_process_identity():
     import bench
     assert bench.reduce_max(None, 7.5) == 7.5
     assert bench.job_throughput(2e12, 1, 1000.0) == pytest.approx(2.0)
+
+
+def test_both_bench_arms_report_the_same_config():
+    """The reference arm's JSON line describes the same workload object as the
+    library arm's, for every schedule and forward variant."""
+    import argparse
+    import bench
+    for schedule, fwd, world in (("ring", "partials", 1), ("ring", "fused", 2), ("a2a", "partials", 1)):
+        args = argparse.Namespace(schedule=schedule, fwd=fwd)
+        w = bench.get_workload("large")
+        cfg = bench.bench_config(w, args, world)
+        assert cfg == bench.bench_config(w, args, world)
+        assert cfg["workload"].startswith("large: B=64 x S=8192")
+        assert cfg["forward"] == ("fused online softmax" if (fwd == "fused" or schedule == "a2a")
+                                  else "ring-step partials + LSE merge")
+        assert cfg["parallelism"] == ("replicas x2" if world == 2 else "1 GPU, CP emulated")
