@@ -552,13 +552,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           };
           // max of the raw scores, scaled once (the scale is positive, and a
           // correctly rounded product preserves order)
-          float mxr = -INFINITY;
+          // four independent running maxima: a single chain of dependent
+          // max instructions would be latency-bound with one or two warps
+          // per SM sub-partition
+          float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int g0 = 0; g0 < BN; g0 += HOLD) {
             load_s(g0);
 #pragma unroll
-            for (int x = 0; x < HOLD; x += 2) mxr = fmax3(mxr, __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
+            for (int x = 0; x < HOLD; x += 2)
+              mq[(x >> 1) & 3] = fmax3(mq[(x >> 1) & 3], __uint_as_float(sr[x]), __uint_as_float(sr[x + 1]));
           }
+          const float mxr = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
           const float mx = mxr * p.scale_log2;
           float alpha = 1.f;
           if (mx > m) {
@@ -573,7 +578,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           // p = 2^(s * scale_log2 - m), two columns per packed FMA
           const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2);
           const uint64_t negm2 = f32x2(-m_use, -m_use);
-          uint64_t psum2 = f32x2(0.f, 0.f);
+          uint64_t psum2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};   // two independent sum chains
 #pragma unroll
           for (int g0 = 0; g0 < BN; g0 += HOLD) {
             if (HOLD < BN) load_s(g0);
@@ -587,7 +592,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[cl]), __uint_as_float(sr[cl + 1])), scale2, negm2), a0,
                             a1);
                 const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-                psum2 = add_f32x2(psum2, f32x2(p0, p1));
+                psum2[x & 1] = add_f32x2(psum2[x & 1], f32x2(p0, p1));
                 pk[x] = pack_bf16x2(p0, p1);
               }
               tmem_st16(t_s + (g0 + c * 32) / 2, pk);
@@ -595,7 +600,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
           tmem_wait_st();
           float ps0, ps1;
-          f32x2_split(psum2, ps0, ps1);
+          f32x2_split(add_f32x2(psum2[0], psum2[1]), ps0, ps1);
           l = l * alpha + (ps0 + ps1);
           // rescale the running O (rare: the reference max grew past the
           // threshold) once the previous P V product has landed
