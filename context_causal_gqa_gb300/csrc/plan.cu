@@ -3,8 +3,8 @@
 // step, dQ-pass items and dK/dV-pass items.
 //
 // TransformerEngine PR "Optimize context parallel attention layouts and
-// gradient accumulation", Changes: the promised sequence lengths and
-// physical offsets are checked on device on each execution.  Here a broken
+// gradient accumulation", Changes: the device re-validates the promised
+// sequence lengths and physical offsets at every call.  Here a broken
 // promise writes CCG_ERR_SEQLENS into the status word (no trap) and an
 // empty plan, so that every later kernel returns without writing.
 #include "common.cuh"

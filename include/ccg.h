@@ -213,7 +213,7 @@ ccg_status ccg_cp_lse_merge(int32_t nparts, const void* const* o_parts,
                             void* o, float* lse, ccg_stream_t stream);
 
 /* Delta[row] = sum_d O[row][d] * dO[row][d] in float (TransformerEngine PR,
- * CP8 AllGather composition: the "pitched O/dO dot" helper of the backward).
+ * CP8 AllGather composition: the backward's row dot of O and dO over pitched rows).
  *   o, dout: bf16 [rows][head_dim];  delta: float [rows], written. */
 ccg_status ccg_bwd_dot(const void* o, const void* dout, int64_t rows, int32_t head_dim,
                        float* delta, ccg_stream_t stream);

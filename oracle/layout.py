@@ -5,10 +5,10 @@ the CUDA path.
 
 Sources (TransformerEngine PR "Optimize context parallel attention layouts
 and gradient accumulation"):
-  * Changes: "vectorized A2A layout copies" -- an A2A pack/unpack fast path
-    inside the existing swap API (Description, Changes).
-  * Related optimization work / CP8 AllGather composition: the "pitched O/dO
-    dot" that computes the per-row Delta = sum_d O*dO for the backward.
+  * Changes: a fast path for the A2A pack/unpack layout copies inside the
+    existing swap API (Description, Changes).
+  * Related optimization work / CP8 AllGather composition: the backward's row
+    dot of O and dO over pitched rows, the per-row Delta = sum_d O*dO.
 
 Reading of the A2A layouts (the pages name the copies but not the layout):
   * rank-major local layout [T, H, D]: for rank r = 0..CP-1, for sequence b:
