@@ -12,8 +12,10 @@ Per-kernel durations come from events the library records around each of its
 launches inside the same timed region.  `e2e` repeats the measurement through
 the same public step API from pinned host buffers: every step's H2D of its
 inputs and D2H of its outputs are in the timed region, overlapped with the
-compute of the neighbouring steps (two device buffer sets, copy streams).  `cpu_baseline` times the FP64 oracle on a bounded sample
-on this host's cores.  Under torchrun (N > 1) every rank runs an independent
+compute of the neighbouring steps (two device buffer sets, copy streams).
+For the "large" workload, `d128` repeats the device-timed measurement on its
+D=128 companion (same shapes and protocol, head dim 128).  `cpu_baseline`
+times the FP64 oracle on a bounded sample on this host's cores.  Under torchrun (N > 1) every rank runs an independent
 replica (weak scaling, no data-path collective).
 
 --impl reference times the FP64 CPU oracle instead (one (sequence, q head)
@@ -41,6 +43,7 @@ UNIT = "TFLOP/s"
 EXTRA = {
     "ncu_small": W.custom_workload("ncu_small", [8192] * 2, 32, 8, 256, 8, index=9),
     "ncu_small_d128": W.custom_workload("ncu_small_d128", [8192] * 2, 32, 8, 128, 8, index=10),
+    "ncu_small_a2a": W.custom_workload("ncu_small_a2a", [8192] * 2, 32, 8, 256, 8, index=12, pack_roundtrip=True),
     "large_d128": W.custom_workload("large_d128", [8192] * 64, 32, 8, 128, 8, index=11, pack_roundtrip=True),
 }
 
@@ -260,15 +263,13 @@ def run_reference(args):
     return 0
 
 
-def run_ccg(args):
+def measure(w, args, dev, pg, world, rank, clocks_uuid=None):
+    """Device-timed steps of workload `w`: W warm-up steps, then K steps
+    between CUDA events on the launching stream, barrier + synchronize on
+    both sides, max over ranks; per-kernel events from the library.
+    Returns (step, result dict)."""
     import torch
-    rank, local, world, pg = dist_setup(args.gpus)
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    import context_causal_gqa_gb300 as ccg
     from context_causal_gqa_gb300.pipeline import AttentionStep, profile_begin, profile_end
-    ccg.load()
-    w = get_workload(args.workload)
     x = W.make_inputs(w, device=dev, seed=w.seed + 1000 * rank)
     step = AttentionStep(w, x, device=dev, schedule=args.schedule, fused=args.fwd == "fused")
     stream = torch.cuda.current_stream(dev)
@@ -281,15 +282,7 @@ def run_ccg(args):
         if pg is not None:
             pg.barrier()
 
-    def max_over_ranks(v):
-        return reduce_max(pg, v, dev)
-
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        pass
-    clocks = ClockSampler(uuid)
+    clocks = ClockSampler(clocks_uuid)
     per_step = step.launches_per_step
     profile_begin(per_step * args.steps + 8)
     barrier()
@@ -310,7 +303,7 @@ def run_ccg(args):
     prof = profile_end()
     step.check()
     ms = e0.elapsed_time(e1) / args.steps
-    ms_max = max_over_ranks(ms)
+    ms_max = reduce_max(pg, ms, dev)
     step_ms = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
     flops = w.flops_fwd_bwd()
     value = job_throughput(flops, world, ms_max)
@@ -353,6 +346,34 @@ def run_ccg(args):
                 "unit": dk["unit"], "frac": dk["frac"], "traffic": traffic, "kernel": dom,
                 "peak_source": pk["source"] + (" bf16 sustained (kernel timed inside a long step)"
                                                if dk["bound"] == "tensor" else " hbm copy")}
+    res = {"value": round(value, 2), "ms_per_step": round(ms_max, 3), "flops": flops,
+           "frac_of_peak": round(value / world / pk["bf16_sustained"], 4), "peak_tflops": pk["bf16_sustained"],
+           "roofline": roofline, "kernels": kernels, "clocks": clk, "gpu_launches": launches,
+           "step_ms": {"median": round(statistics.median(step_ms), 3), "min": round(min(step_ms), 3),
+                       "max": round(max(step_ms), 3)}}
+    return step, x, res
+
+
+def run_ccg(args):
+    import torch
+    rank, local, world, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import context_causal_gqa_gb300 as ccg
+    ccg.load()
+    w = get_workload(args.workload)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    stream = torch.cuda.current_stream(dev)
+    step, x, res = measure(w, args, dev, pg, world, rank, uuid)
+    flops = res["flops"]
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
 
     # end to end from pinned host buffers through the same step API: every
     # step copies its inputs in and its outputs out; the copies of one step
@@ -371,11 +392,26 @@ def run_ccg(args):
         torch.cuda.synchronize(dev)
         barrier()
         step.check()
-        ms_e2e = max_over_ranks(s0.elapsed_time(s1) / ke)
+        ms_e2e = reduce_max(pg, s0.elapsed_time(s1) / ke, dev)
         e2e = {"value": job_throughput(flops, world, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "ms_per_step": ms_e2e, "steps": ke,
                "copies": "H2D of step i+1 and D2H of step i-1 overlap the compute of step i"}
         del h_in, h_out
+    peak_mem = round(torch.cuda.max_memory_allocated(dev) / 1e9, 2)
+    del step, x
+    torch.cuda.empty_cache()
+
+    # the D=128 companion of the large workload, same protocol (device-timed)
+    d128 = None
+    if args.workload == "large" and not args.no_d128:
+        wd = get_workload("large_d128")
+        sd, xd, rd = measure(wd, args, dev, pg, world, rank, uuid)
+        del sd, xd
+        torch.cuda.empty_cache()
+        d128 = {"workload": bench_config(wd, args, world)["workload"], "value": rd["value"], "unit": UNIT,
+                "ms_per_step": rd["ms_per_step"], "frac_of_peak": rd["frac_of_peak"], "roofline": rd["roofline"],
+                "kernels": rd["kernels"], "clocks": rd["clocks"], "step_ms": rd["step_ms"],
+                "gpu_launches": rd["gpu_launches"]}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -386,15 +422,13 @@ def run_ccg(args):
 
     if rank == 0:
         cfg = bench_config(w, args, world)
-        line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": round(ms_max, 3), "higher_is_better": True,
+        line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": cfg, "frac_of_peak": round(value / world / pk["bf16_sustained"], 4),
-                "peak_tflops": pk["bf16_sustained"], "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches, "clocks": clk, "kernels": kernels,
-                "step_ms": {"median": round(statistics.median(step_ms), 3), "min": round(min(step_ms), 3),
-                            "max": round(max(step_ms), 3)},
-                "peak_mem_gb": round(torch.cuda.max_memory_allocated(dev) / 1e9, 2)}
+                "config": cfg, "frac_of_peak": res["frac_of_peak"],
+                "peak_tflops": res["peak_tflops"], "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "kernels": res["kernels"],
+                "step_ms": res["step_ms"], "peak_mem_gb": peak_mem, "d128": d128}
         print(json.dumps(line))
     if pg is not None:
         pg.destroy_process_group()
@@ -423,6 +457,7 @@ def main():
                     help="partials: ring-step partials + LSE merge (the measured path); fused: one online softmax")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-d128", action="store_true", help="skip the D=128 companion measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ccg":

@@ -11,7 +11,7 @@
 // so results are bitwise repeatable.
 //
 // dQ pass: one CTA per (128-row query tile, q head).  Q and dO tiles stay in
-//   SMEM; K/V tiles stream through single-tile slots.  Per KV tile:
+//   SMEM; K/V tiles stream through the slots.  Per KV tile:
 //   S = Q K^T, dP = dO V^T (TMEM), then dS = P (dP - Delta) * scale in
 //   registers (P = exp(S*scale - LSE) from the merged LSE), written back to
 //   TMEM as BF16, and dQ += dS K (TMEM accumulator).
@@ -19,9 +19,13 @@
 //   Q_i / dO_i tiles of every contributing (query chunk, tile, q head)
 //   stream through the slots.  Per contribution: S^T = K Q^T, dP^T = V dO^T,
 //   P^T and dS^T in registers -> TMEM (BF16), dV += P^T dO, dK += dS^T Q.
-//   At D = 256 the two 256-column FP32 accumulators alone fill TMEM, so the
-//   pass runs as two kernels: one accumulating dV, one accumulating dK.
+// At D = 256 the two 256-column FP32 accumulators alone fill TMEM, so the
+// dK/dV pass runs as two kernels (dV, then dK), and the dQ and dK kernels
+// stream their 128-row tiles as two 128-column halves so that every product
+// runs at full width with both resident tiles in shared memory.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -859,6 +863,370 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   if (warp == 2) tmem_dealloc(tmem, Cfg::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// D = 256 dQ pass and dK pass with full-width products.
+//
+// At D = 256 the two resident 128-row tiles (Q and dO, or K and V) take 128 KB
+// of shared memory, which leaves no room for a whole streamed 128-row tile
+// (64 KB) next to a second one.  Here every streamed tile is loaded as its
+// two 128-column halves (32 KB each) through three half-tile slots, so that
+// the products of S (S^T), dP (dP^T) and the gradient all run at N = 128 or
+// wider (full tensor-core rate) instead of N = 64:
+//   S  = sum_h R0[:, h] Y_h^T,  dP = sum_h R1[:, h] X_h^T   (K = 128 per half)
+//   G[:, h] += dS Y_h                                         (N = 128 per half)
+// with, for the dQ role, R0 = Q, R1 = dO, X = V_j, Y = K_j, G = dQ (one CTA per
+// 128-row query tile and q head, KV tiles in ring-step order), and for the dK
+// role R0 = K, R1 = V, X = dO_i, Y = Q_i, G = dK (one CTA per 128-row KV tile
+// and kv head, contributions in the canonical order, the first MMA of the
+// accumulator without accumulation).  TMEM: S at columns [0,128), dP at
+// [128,256), G at [256,512); the two softmax warpgroups split the 128 columns
+// of every unit and pack their BF16 dS over the first half of their own dP
+// columns (the A operand of the gradient product).  Half-tiles stream in the
+// order X0 X1 Y0 Y1 per unit; X_h is released after its dP product, Y_h after
+// its gradient product.
+enum class HalfRole { kDq = 0, kDk = 1 };
+
+struct HalfCfg {
+  static constexpr int D = 256;
+  static constexpr int BM = 128;                 // stationary rows (MMA M)
+  static constexpr int BN = 128;                 // streamed rows per unit
+  static constexpr int DH = 128;                 // columns of a half-tile
+  static constexpr int NSLOT = 3;
+  static constexpr int RES_BYTES = BM * D * 2;   // 64 KB
+  static constexpr int HALF_BYTES = BN * DH * 2; // 32 KB
+  static constexpr int SMEM_SLOT = 2 * RES_BYTES;
+  static constexpr int SMEM_VEC = SMEM_SLOT + NSLOT * HALF_BYTES;   // dK role: [WG][-lse2 64 | -Delta*scale 64]
+  static constexpr int VEC_BYTES = 2 * 2 * (BN / 2) * 4;
+  static constexpr int SMEM_BAR = SMEM_VEC + VEC_BYTES;
+  static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
+  static constexpr int T_S = 0, T_P = BN, T_ACC = 2 * BN;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(T_ACC + D <= TMEM_COLS, "TMEM");
+  static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
+};
+
+// D[tmem] (+)= A[smem, 128 rows, K-major] * B[smem, 128 rows, K-major]^T over
+// one 128-column half (8 K steps); a_desc already points at the half.
+__device__ __forceinline__ void mma_kk_half(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    umma_ss(d_tmem, a_desc + kmajor_step(128, k), b_desc + kmajor_step(128, k), idesc,
+            (accumulate || k > 0) ? 1u : 0u);
+}
+
+template <HalfRole ROLE>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdParams p) {
+  using Cfg = HalfCfg;
+  constexpr bool DQ = ROLE == HalfRole::kDq;
+  constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, D = Cfg::D;
+  using Iter = typename std::conditional<DQ, DqIter<BN>, KvIter<BN>>::type;
+  const int nheads = DQ ? p.hq : p.hkv;
+  const int item_idx = blockIdx.x / nheads;
+  if (item_idx >= (DQ ? p.hdr->n_dq : p.hdr->n_kv)) return;
+  if (status_bad(p.status)) return;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::SMEM_BAR);
+  uint64_t* res_full = bars;
+  uint64_t* full = bars + 1;              // [NSLOT]
+  uint64_t* empty = full + NSLOT;         // [NSLOT]
+  uint64_t* s_full = empty + NSLOT;       // S and dP of the unit complete
+  uint64_t* ds_full = s_full + 1;         // dS of the unit packed (both warpgroups)
+  uint64_t* acc_done = ds_full + 1;
+  uint64_t* vec_ready = acc_done + 1;     // [2 WG]
+  uint64_t* vec_free = vec_ready + 2;     // [2 WG]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_free + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* vec = reinterpret_cast<float*>(smem + Cfg::SMEM_VEC);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WorkItem it = p.items[item_idx];
+  const int head = blockIdx.x % nheads;        // q head (dQ role) or kv head (dK role)
+  const int G = p.hq / p.hkv;
+  const int g = DQ ? head / G : head;          // kv head
+  const SeqInfo si = seq_info(p, it.b);
+  const int r_lo = it.c * si.L + it.tile * BM;               // first stationary row (sequence position)
+  const int r_hi = min(r_lo + BM, (it.c + 1) * si.L);        // rows owned by this tile
+  const int r_valid_hi = min(r_hi, si.S);
+
+  auto iter_init = [&](Iter& itr) {
+    if constexpr (DQ) itr.init(p.cp, it.c, si.L, si.S, r_lo, r_valid_hi);
+    else itr.init(p.cp, it.c, si.L, si.S, r_lo, G, g);
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(res_full, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(ds_full, 256);
+    mbar_init(acc_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(vec_ready + b, 128);
+      mbar_init(vec_free + b, 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int kv_group_row = static_cast<int>((g / p.hpg_kv) * p.T) + si.start;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      Iter itr;
+      iter_init(itr);
+      int issued[NSLOT];
+      for (int s = 0; s < NSLOT; ++s) issued[s] = 0;
+      bool ok = true;
+      if (!itr.done) {
+        // resident tiles: Q and dO of (tile, q head), or K and V of (tile, kv head)
+        const CUtensorMap* r0 = DQ ? &tm_q : &tm_k;
+        const CUtensorMap* r1 = DQ ? &tm_do : &tm_v;
+        const int rhead = DQ ? head % p.hpg_q : g % p.hpg_kv;
+        const int rrow = DQ ? static_cast<int>((head / p.hpg_q) * p.T) + si.start + r_lo : kv_group_row + r_lo;
+        mbar_arrive_expect_tx(res_full, 2 * Cfg::RES_BYTES);
+        for (int kc = 0; kc < D / 64; ++kc) {
+          tma_load_3d(smem + kc * BM * 128, r0, kc * 64, rhead, rrow, res_full);
+          tma_load_3d(smem + Cfg::RES_BYTES + kc * BM * 128, r1, kc * 64, rhead, rrow, res_full);
+        }
+        // half-tiles X0 X1 Y0 Y1 of every unit, in the order the MMA warp uses them
+        for (int t = 0; !itr.done && ok; ++t) {
+          const int slot = t % NSLOT;
+          if (t >= NSLOT) ok = mbar_wait(empty + slot, ((t / NSLOT) - 1) & 1, abort_flag);
+          if (!ok) break;
+          const int part = t & 3, half = part & 1;
+          const bool is_x = part < 2;
+          const CUtensorMap* map;
+          int hc, row;
+          if constexpr (DQ) {
+            map = is_x ? &tm_v : &tm_k;
+            hc = g % p.hpg_kv;
+            row = kv_group_row + itr.k0();
+          } else {
+            const int hq = itr.head();
+            map = is_x ? &tm_do : &tm_q;
+            hc = hq % p.hpg_q;
+            row = static_cast<int>((hq / p.hpg_q) * p.T) + si.start + itr.q0();
+          }
+          mbar_arrive_expect_tx(full + slot, Cfg::HALF_BYTES);
+          uint8_t* dst = smem + Cfg::SMEM_SLOT + slot * Cfg::HALF_BYTES;
+          for (int kc = 0; kc < 2; ++kc)
+            tma_load_3d(dst + kc * BN * 128, map, (2 * half + kc) * 64, hc, row, full + slot);
+          issued[slot]++;
+          if (part == 3) itr.next();
+        }
+        if (!ok) {
+          raise_status(p.status, CCG_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        volatile int never = 0;
+        mbar_wait(res_full, 0, &never, 200000000ull);
+        for (int s = 0; s < NSLOT; ++s)
+          if (issued[s] > 0) mbar_wait(full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      Iter ahead;
+      iter_init(ahead);
+      bool ok = true;
+      if (!ahead.done) {
+        const uint32_t base = smem_u32(smem);
+        const uint64_t r0_desc = smem_desc_sw128(base, 16, 1024);
+        const uint64_t r1_desc = smem_desc_sw128(base + Cfg::RES_BYTES, 16, 1024);
+        const uint32_t slot_base = smem_u32(smem + Cfg::SMEM_SLOT);
+        const uint64_t slot_k0 = smem_desc_sw128(slot_base, 16, 1024);
+        const uint64_t slot_mn0 = smem_desc_sw128(slot_base, BN * 128, 1024);
+        constexpr uint32_t kSlotStep = Cfg::HALF_BYTES >> 4;
+        auto slot_k = [&](int s2) { return slot_k0 + s2 * kSlotStep; };
+        auto slot_mn = [&](int s2) { return slot_mn0 + s2 * kSlotStep; };
+        ok = mbar_wait(res_full, 0, abort_flag);
+        tc_fence_after();
+        // dP (from X0, X1) then S (from Y0, Y1) of unit j
+        auto issue_sp = [&](int j) -> bool {
+          for (int h = 0; h < 2; ++h) {
+            const int t = 4 * j + h, sl = t % NSLOT;
+            if (!mbar_wait(full + sl, (t / NSLOT) & 1, abort_flag)) return false;
+            tc_fence_after();
+            mma_kk_half(tmem + Cfg::T_P, r1_desc + kmajor_step(128, 8 * h), slot_k(sl), h > 0);
+            umma_commit(empty + sl);                  // X_h done
+          }
+          for (int h = 0; h < 2; ++h) {
+            const int t = 4 * j + 2 + h, sl = t % NSLOT;
+            if (!mbar_wait(full + sl, (t / NSLOT) & 1, abort_flag)) return false;
+            tc_fence_after();
+            mma_kk_half(tmem + Cfg::T_S, r0_desc + kmajor_step(128, 8 * h), slot_k(sl), h > 0);
+          }
+          umma_commit(s_full);
+          return true;
+        };
+        int j_sp = 0;
+        if (ok) {
+          ok = issue_sp(j_sp++);
+          ahead.next();
+        }
+        for (int j = 0; ok && j < j_sp; ++j) {
+          ok = mbar_wait(ds_full, j & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          for (int h = 0; h < 2; ++h) {
+            const int sl = (4 * j + 2 + h) % NSLOT;
+            mma_tn_split<BN, Cfg::DH, true>(tmem + Cfg::T_ACC + h * Cfg::DH, tmem + Cfg::T_P, slot_mn(sl), j > 0);
+            umma_commit(empty + sl);                  // Y_h done
+          }
+          if (!ahead.done) {
+            ok = issue_sp(j_sp++);
+            ahead.next();
+          }
+        }
+      }
+      if (!ok) {
+        raise_status(p.status, CCG_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit(acc_done);
+      volatile int never = 0;
+      mbar_wait(acc_done, 0, &never, 200000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int wg = (warp - 4) >> 2;                  // half of every unit's columns
+    const int row = ((warp & 3) << 5) + lane;        // stationary row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t0 = tmem + lane_base;
+    constexpr int NC = BN / 64;                       // 32-column chunks per warpgroup
+    const int c_first = wg * NC;
+    const int r_pos = r_lo + row;
+    const bool r_valid = r_pos < r_valid_hi;
+    const int64_t grow = DQ ? thd_row(si.start + r_pos, head, p.hpg_q, p.T)
+                            : thd_row(si.start + r_pos, g, p.hpg_kv, p.T);
+    // dQ role: this row's LSE (log2 units) and Delta
+    float lse2 = 0.f, dlt = 0.f;
+    if (DQ && r_valid) {
+      lse2 = __ldg(p.lse + grow) * kLog2e;
+      dlt = __ldg(p.delta + grow);
+    }
+    const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2), sc2 = f32x2(p.scale, p.scale);
+    const uint64_t row_nl2 = f32x2(-lse2, -lse2), row_nds = f32x2(-dlt * p.scale, -dlt * p.scale);
+    float* vb = vec + wg * BN;                        // dK role: [-lse2 x 64 | -Delta*scale x 64]
+    Iter itr;
+    iter_init(itr);
+    const bool any = !itr.done;
+    bool ok = true;
+    for (int j = 0; !itr.done; ++j, itr.next()) {
+      int c_lo = 0, c_hi = BN;                        // visible streamed columns of this row
+      if constexpr (DQ) {
+        const int k0 = itr.k0();
+        const int kend = itr.diag ? min(itr.kv_hi, r_pos + 1) : itr.kv_hi;
+        c_hi = r_valid ? kend - k0 : 0;
+      } else {
+        // LSE (log2 units) and Delta of this contribution's query columns -> SMEM
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(vec_free + wg, (j - 1) & 1, abort_flag));
+          if (!ok) break;
+        }
+        if (row < BN / 2) {
+          const int qp = itr.q0() + c_first * 32 + row;
+          const bool qv = qp < itr.q_valid_hi;
+          const int64_t gr = thd_row(si.start + qp, itr.head(), p.hpg_q, p.T);
+          vb[row] = qv ? -__ldg(p.lse + gr) * kLog2e : 0.f;
+          vb[BN / 2 + row] = qv ? -__ldg(p.delta + gr) * p.scale : 0.f;
+        }
+        mbar_arrive(vec_ready + wg);
+        ok = __all_sync(0xffffffffu, mbar_wait(vec_ready + wg, j & 1, abort_flag));
+        if (!ok) break;
+        const int q0 = itr.q0();
+        // query column c is visible to this key row iff q0+c >= r_pos and q0+c < q_valid_hi
+        c_lo = r_valid ? max(0, r_pos - q0) : BN;
+        c_hi = r_valid ? itr.q_valid_hi - q0 : 0;
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      // hidden columns only on units that cross the causal diagonal or a
+      // ragged end: their scores become -inf, so P and dS come out 0
+      const bool masked = __any_sync(0xffffffffu, c_lo > 0 || c_hi < BN);
+      uint32_t rs[32], rp[32];
+#pragma unroll
+      for (int c = c_first; c < c_first + NC; ++c) {
+        tmem_ld32(t0 + Cfg::T_S + c * 32, rs);
+        tmem_ld32(t0 + Cfg::T_P + c * 32, rp);
+        tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int col = c * 32 + x;
+            rs[x] = (col >= c_lo && col < c_hi) ? rs[x] : 0xff800000u;
+          }
+        }
+        const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(vb + (c - c_first) * 32);
+        const uint64_t* nds = reinterpret_cast<const uint64_t*>(vb + BN / 2 + (c - c_first) * 32);
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          // P = 2^(s * scale_log2 - lse2); dS = P * (dP * scale - Delta * scale)
+          float a0, a1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2,
+                                DQ ? row_nl2 : nl2[x]),
+                      a0, a1);
+          const uint64_t pv = f32x2(ex2_approx(a0), ex2_approx(a1));
+          const uint64_t t = fma_f32x2(f32x2(__uint_as_float(rp[2 * x]), __uint_as_float(rp[2 * x + 1])), sc2,
+                                       DQ ? row_nds : nds[x]);
+          float d0, d1;
+          f32x2_split(mul_f32x2(pv, t), d0, d1);
+          pk[x] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(t0 + Cfg::T_P + c_first * 32 + (c - c_first) * 16, pk);   // in place, own columns
+      }
+      if constexpr (!DQ) mbar_arrive(vec_free + wg);  // done reading this contribution's LSE/Delta
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    if (ok && any) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
+    if (!ok) {
+      raise_status(p.status, CCG_ERR_TIMEOUT);
+      *abort_flag = 1;
+    } else {
+      // each warpgroup writes half of the columns of the tile's rows: real
+      // rows get the gradient, padding rows 0
+      tc_fence_after();
+      const bool own = r_pos < r_hi;
+      __nv_bfloat16* dst = (DQ ? p.out0 : p.out1) + grow * D;
+      uint32_t r[32];
+#pragma unroll 1
+      for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
+        if (any) {                        // CTA-uniform: every lane loads
+          tmem_ld32(t0 + Cfg::T_ACC + c * 32, r);
+          tmem_wait_ld();
+        }
+        if (own) store_row_bf16(dst + c * 32, r, 1.f, !any || !r_valid);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+}
+
 template <class K>
 cudaError_t set_smem(K kern, int bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -888,13 +1256,24 @@ cudaError_t launch_kv(const CUtensorMap* m, const BwdParams& p, int grid_items, 
   return cudaGetLastError();
 }
 
-// Tile shapes.  D = 256 is limited by shared memory: the resident 128-row
-// tiles take 128 KB (Q, dO) or 128 KB (K, V), so streamed tiles are 32 rows.
+template <HalfRole ROLE>
+cudaError_t launch_half(const CUtensorMap* m, const BwdParams& p, int grid_items, cudaStream_t s) {
+  const int smem = HalfCfg::SMEM_TOTAL + 1024;
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_half_kernel<ROLE>, smem); });
+  if (e != cudaSuccess) return e;
+  const int64_t grid = static_cast<int64_t>(grid_items) * (ROLE == HalfRole::kDq ? p.hq : p.hkv);
+  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  attn_bwd_half_kernel<ROLE><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  return cudaGetLastError();
+}
+
+// Tile shapes.  D = 128: whole streamed tiles.  D = 256: the dQ and dK passes
+// stream 128-column halves of 128-row tiles (attn_bwd_half_kernel); the dV
+// pass keeps only K resident, so whole 128-row Q and dO tiles fit.
 using Dq128 = DqCfg<128, 128, 5, 1>;
-using Dq256 = DqCfg<256, 64, 3, 1>;
 using Kv128 = KvCfg<128, KvMode::kBoth, 128, 4, 1>;
 using Kv256V = KvCfg<256, KvMode::kDvOnly, 128, 2, 1>;
-using Kv256K = KvCfg<256, KvMode::kDkOnly, 64, 3, 1>;
 
 }  // namespace
 
@@ -902,14 +1281,8 @@ int bwd_q_tile_rows(int) { return 128; }
 int bwd_kv_tile_rows(int) { return 128; }
 // Box rows of the twelve tensor maps: 0..3 = q, k, v, dO for the dQ pass,
 // 4..7 = the same for the first dK/dV kernel, 8..11 for the second (D = 256).
-int bwd_map_rows(int which, int D) {
-  const int pass = which / 4, t = which % 4;
-  const bool is_kv_tensor = (t == 1 || t == 2);
-  if (pass == 0) return is_kv_tensor ? (D == 128 ? Dq128::BN : Dq256::BN) : 128;
-  if (is_kv_tensor) return 128;
-  if (D == 128) return Kv128::BN;
-  return pass == 1 ? Kv256V::BN : Kv256K::BN;
-}
+// Every pass moves 128-row boxes.
+int bwd_map_rows(int, int) { return 128; }
 
 cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, const WorkItem* kv_items,
                             const PlanHeader* hdr, const int32_t* cu, const int32_t* cu_pad, const float* lse,
@@ -937,7 +1310,7 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
   p.out0 = static_cast<__nv_bfloat16*>(dq);
   p.out1 = nullptr;
   prof_begin("attn_bwd_dq", stream);
-  e = D == 128 ? launch_dq<Dq128, 128>(maps, p, grid_q, stream) : launch_dq<Dq256, 256>(maps, p, grid_q, stream);
+  e = D == 128 ? launch_dq<Dq128, 128>(maps, p, grid_q, stream) : launch_half<HalfRole::kDq>(maps, p, grid_q, stream);
   prof_end(stream);
   if (e != cudaSuccess) return e;
   ++*launches;
@@ -958,7 +1331,7 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
     if (e != cudaSuccess) return e;
     ++*launches;
     prof_begin("attn_bwd_dk", stream);
-    e = launch_kv<Kv256K, 256, KvMode::kDkOnly>(maps + 8, p, grid_kv, stream);
+    e = launch_half<HalfRole::kDk>(maps + 8, p, grid_kv, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
     ++*launches;

@@ -14,9 +14,10 @@
 // library holds kNoAllocScratchBytes of device memory for it until the
 // process exits.  Host code cannot use the array's name as a device address
 // (in host code it names a host-side stand-in); the device address is
-// fetched once per device with cudaGetSymbolAddress, with that device
-// current, on the first call made on that device.  That first call should
-// therefore come before any stream capture begins.
+// fetched with cudaGetSymbolAddress, with that device current, on the first
+// call made on that device, and again on the first call after the device's
+// context changed (a device reset).  That first call should therefore come
+// before any stream capture begins.
 //
 // Every call on a device shares the one array and it keeps the previous
 // call's contents: the plan and Delta are fully rewritten by every call
@@ -27,6 +28,7 @@
 //
 // There is no counterpart of this entry point in the TransformerEngine pull
 // request the rest of the library follows.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -42,20 +44,55 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up once
-// per device); nullptr if the address could not be obtained.
+// The cached address of the array on one device, with the CUDA context it
+// was looked up in.  A device reset (cudaDeviceReset) or a destroyed and
+// re-created primary context reloads the library's device image, which may
+// place the array elsewhere: the address is looked up again whenever the
+// current context differs from the one it was taken in.
+struct ScratchCache {
+  CUcontext ctx = nullptr;
+  void* ptr = nullptr;
+};
+ScratchCache g_scratch[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry point (the library has
+// no link-time dependency on the driver library).
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of the scratch array on the current device, looked up with
+// that device current on its first use in the current context; nullptr if
+// the address could not be obtained.
 void* scratch_for_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (get_ctx == nullptr) return nullptr;
+  CUcontext ctx = nullptr;                       // null before the runtime's first use on this thread
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return nullptr;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = p;
-  }
-  return g_scratch_ptr[dev];
+  ScratchCache& c = g_scratch[dev];
+  if (ctx != nullptr && c.ptr != nullptr && c.ctx == ctx) return c.ptr;
+  // the lookup makes the device's primary context current if none was
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return nullptr;
+  c.ctx = ctx;
+  c.ptr = p;
+  return c.ptr;
 }
 
 }  // namespace

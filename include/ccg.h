@@ -175,10 +175,16 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
  *   no cudaFree).
  *   d_status: the caller's status word, as in ccg_attn_bwd; NULL selects a
  *   status word inside the fixed scratch that is cleared at the start of
- *   every call and cannot be read back.
+ *   every call and cannot be read back.  With d_status NULL, a failure the
+ *   device detects (a broken sequence-length promise, CCG_ERR_SEQLENS, or
+ *   a bounded wait that ran out, CCG_ERR_TIMEOUT) is NOT reported: the call
+ *   still returns CCG_OK and dq, dk, dv are left unwritten (they keep
+ *   whatever the caller had there).  Pass a status word unless the
+ *   sequence offsets are already known to be valid.
  *   The first call on a device looks up the array's device address on that
- *   device (cudaGetSymbolAddress, with the device current); make that first
- *   call before any stream capture.  All calls on a device share the one
+ *   device (cudaGetSymbolAddress, with the device current), and so does the
+ *   first call after the device's CUDA context changed (cudaDeviceReset);
+ *   make that first call before any stream capture.  All calls on a device share the one
  *   array, which keeps the previous call's contents (every call rewrites
  *   the plan and Delta before reading them): calls whose execution overlaps
  *   on the GPU race on it and must not be issued. */

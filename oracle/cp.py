@@ -16,7 +16,7 @@ and gradient accumulation"):
     r and 2CP-1-r (the load-balanced causal split that the page's "reorder"
     refers to).
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the pages are silent (the same readings as the CUDA path):
   * chunks are cut on the PADDED length P_b (P_b % 2CP must be 0); chunk c
     of sequence b covers physical rows [start_b + c*L_b, start_b+(c+1)*L_b),
     L_b = P_b / (2CP);

@@ -93,7 +93,7 @@ def test_bitwise_repeatable_under_poison_churn_and_changed_inputs(lib):
 
 
 def test_first_contribution_is_the_accumulator(lib):
-    """Outputs are written without any zero fill: poisoning dK/dV with NaN
+    """Outputs are written without any zero fill: poisoning dQ/dK/dV with NaN
     before the call must not leak into any element (every accumulator starts
     from its first contribution, padding rows are written as zeros)."""
     w = W.custom_workload("poison", [200, 56], 4, 2, 128, 4, pad_to=64)
@@ -106,3 +106,32 @@ def test_first_contribution_is_the_accumulator(lib):
                  dq=dq, dk=dk, dv=dv)
     for t in (dq, dk, dv):
         assert torch.isfinite(t).all()
+
+
+# Chunk lengths are multiples of 128 and there is no padding: no query tile
+# of the dK/dV pass reaches past its chunk.
+@pytest.mark.parametrize("w", [W.custom_workload("zero_d128_cp4", [1024, 2048], 4, 2, 128, 4),
+                               W.custom_workload("zero_d256_cp8", [2048], 4, 1, 256, 8)],
+                         ids=lambda w: w.name)
+def test_all_zero_contributions_give_exact_zeros(lib, w):
+    """dO = -0.0 everywhere with q, k, v non-negative: every product that
+    feeds dV (P * dO), dP (dO * V), dS and so dQ and dK is a zero, so every
+    element of dQ, dK and dV, written over NaN, must come back as an exact
+    zero.  The tensor core returns +0.0 for a sum of -0.0 products (measured
+    on GB300: dV, a plain P^T dO product sum, comes back +0.0), so the sign
+    of a zero cannot tell an accumulator that starts from its first
+    contribution from one that starts from a zero fill; the zeros are checked
+    bit for bit as +0.0."""
+    x = W.make_inputs(w, device="cuda")
+    for n in ("q", "k", "v"):
+        x[n] = x[n].abs()
+    x["do"] = torch.full_like(x["do"], -0.0)
+    cu, cpad = x["cu_seqlens"], x["cu_seqlens_padded"]
+    o, lse = lib.attn_fwd(x["q"], x["k"], x["v"], cu, cpad, w.cp)
+    outs = [torch.full_like(x[n], float("nan")) for n in ("q", "k", "v")]
+    lib.attn_bwd(x["q"], x["k"], x["v"], o, x["do"], lse, cu, cpad, w.cp, dq=outs[0], dk=outs[1], dv=outs[2])
+    for name, g in zip(("dQ", "dK", "dV"), outs):
+        bits = g.view(torch.int16)
+        n_zero = int((bits == 0).sum())
+        assert n_zero == bits.numel(), (f"{name}: {bits.numel() - n_zero} of {bits.numel()} elements are not +0.0 "
+                                        f"(distinct bit patterns: {torch.unique(bits)[:8].tolist()})")
