@@ -150,25 +150,26 @@ plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, 
     }
   }
   if (want & 2) {
-    // dQ pass: later query chunks see more keys, so they go first
+    // dQ pass: sequence-major; later query chunks see more keys, so they go first
     int slot = 0;
-    for (int c = C - 1; c >= 0; --c) {
-      auto count = [&](int b) { return all_tiles(b, bm); };
-      auto write = [&](int b, int first, int n) {
+    {
+      auto count = [&](int i) { return all_tiles(i / C, bm); };
+      auto write = [&](int i, int first, int n) {
+        const int b = i / C, c = C - 1 - i % C;
         for (int t = 0; t < n && first + t < cap_q; ++t) dq_items[first + t] = WorkItem{b, c, t, 0};
       };
-      slot = block_emit(B, slot, count, write);
+      slot = block_emit(B * C, 0, count, write);
     }
     if (slot > cap_q) overflow = 1;
     if (threadIdx.x == 0) hdr->n_dq = min(slot, cap_q);
-    // dK/dV pass: earlier KV chunks are seen by more queries, so they go first
-    slot = 0;
-    for (int j = 0; j < C; ++j) {
-      auto count = [&](int b) { return all_tiles(b, bn); };
-      auto write = [&](int b, int first, int n) {
+    // dK/dV pass: sequence-major; earlier KV chunks are seen by more queries, so they go first
+    {
+      auto count = [&](int i) { return all_tiles(i / C, bn); };
+      auto write = [&](int i, int first, int n) {
+        const int b = i / C, j = i % C;
         for (int t = 0; t < n && first + t < cap_kv; ++t) kv_items[first + t] = WorkItem{b, j, t, 0};
       };
-      slot = block_emit(B, slot, count, write);
+      slot = block_emit(B * C, 0, count, write);
     }
     if (slot > cap_kv) overflow = 1;
     if (threadIdx.x == 0) hdr->n_kv = min(slot, cap_kv);
