@@ -14,7 +14,10 @@ the same public step API from pinned host buffers: every step's H2D of its
 inputs and D2H of its outputs are in the timed region, overlapped with the
 compute of the neighbouring steps (two device buffer sets, copy streams).
 For the "large" workload, `d128` repeats the device-timed measurement on its
-D=128 companion (same shapes and protocol, head dim 128).  `cpu_baseline`
+D=128 companion (same shapes and protocol, head dim 128), and `head_parts`
+times the same step with the ring forward run over 4 head parts (native head
+partitioning) and reports its peak device memory next to the unpartitioned
+one.  `cpu_baseline`
 times the FP64 oracle on a bounded sample on this host's cores.  Under torchrun (N > 1) every rank runs an independent
 replica (weak scaling, no data-path collective).
 
@@ -263,7 +266,7 @@ def run_reference(args):
     return 0
 
 
-def measure(w, args, dev, pg, world, rank, clocks_uuid=None):
+def measure(w, args, dev, pg, world, rank, clocks_uuid=None, head_parts=0):
     """Device-timed steps of workload `w`: W warm-up steps, then K steps
     between CUDA events on the launching stream, barrier + synchronize on
     both sides, max over ranks; per-kernel events from the library.
@@ -271,7 +274,7 @@ def measure(w, args, dev, pg, world, rank, clocks_uuid=None):
     import torch
     from context_causal_gqa_gb300.pipeline import AttentionStep, profile_begin, profile_end
     x = W.make_inputs(w, device=dev, seed=w.seed + 1000 * rank)
-    step = AttentionStep(w, x, device=dev, schedule=args.schedule, fused=args.fwd == "fused")
+    step = AttentionStep(w, x, device=dev, schedule=args.schedule, fused=args.fwd == "fused", head_parts=head_parts)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         step.run()
@@ -368,7 +371,9 @@ def run_ccg(args):
     except Exception:
         pass
     stream = torch.cuda.current_stream(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
     step, x, res = measure(w, args, dev, pg, world, rank, uuid)
+    peak_timed = round(torch.cuda.max_memory_allocated(dev) / 1e9, 2)
     flops = res["flops"]
 
     def barrier():
@@ -401,6 +406,20 @@ def run_ccg(args):
     del step, x
     torch.cuda.empty_cache()
 
+    # native head partitioning of the ring forward: the same step with the
+    # partials and merge run over 4 head parts in turn (workspace for Hq/4)
+    head_parts = None
+    if args.workload == "large" and not args.no_head_parts and args.fwd == "partials" and args.schedule == "ring":
+        torch.cuda.reset_peak_memory_stats(dev)
+        sp, xp, rp = measure(w, args, dev, pg, world, rank, uuid, head_parts=4)
+        head_parts = {"parts": 4, "value": rp["value"], "ms_per_step": rp["ms_per_step"],
+                      "peak_mem_gb": round(torch.cuda.max_memory_allocated(dev) / 1e9, 2),
+                      "peak_mem_gb_parts1": peak_timed,
+                      "attn_fwd_ms": rp["kernels"].get("attn_fwd", {}).get("ms_per_launch"),
+                      "lse_merge_ms": rp["kernels"].get("lse_merge", {}).get("ms_per_launch")}
+        del sp, xp
+        torch.cuda.empty_cache()
+
     # the D=128 companion of the large workload, same protocol (device-timed)
     d128 = None
     if args.workload == "large" and not args.no_d128:
@@ -428,7 +447,8 @@ def run_ccg(args):
                 "config": cfg, "frac_of_peak": res["frac_of_peak"],
                 "peak_tflops": res["peak_tflops"], "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "kernels": res["kernels"],
-                "step_ms": res["step_ms"], "peak_mem_gb": peak_mem, "d128": d128}
+                "step_ms": res["step_ms"], "peak_mem_gb": peak_mem, "peak_mem_gb_device_timed": peak_timed,
+                "head_parts": head_parts, "d128": d128}
         print(json.dumps(line))
     if pg is not None:
         pg.destroy_process_group()
@@ -458,6 +478,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-d128", action="store_true", help="skip the D=128 companion measurement")
+    ap.add_argument("--no-head-parts", action="store_true", help="skip the 4-head-part forward measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ccg":

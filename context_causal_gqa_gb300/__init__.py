@@ -48,10 +48,12 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def make_desc(batch, hq, hkv, head_dim, cp, total_tokens, head_groups=1, scale=0.0, pitches=(0, 0, 0, 0)):
-    """pitches: row pitch in elements of q, k, v, dO (0 = dense)."""
+def make_desc(batch, hq, hkv, head_dim, cp, total_tokens, head_groups=1, scale=0.0, pitches=(0, 0, 0, 0),
+              head_parts=0):
+    """pitches: row pitch in elements of q, k, v, dO (0 = dense); head_parts:
+    P > 1 runs the ring forward and merge over P head parts in turn."""
     return AttnDesc(batch=batch, hq=hq, hkv=hkv, head_dim=head_dim, causal=1, cp=cp,
-                    head_groups=head_groups, reserved=0, total_tokens=total_tokens, softmax_scale=scale,
+                    head_groups=head_groups, head_parts=head_parts, total_tokens=total_tokens, softmax_scale=scale,
                     q_pitch=pitches[0], k_pitch=pitches[1], v_pitch=pitches[2], do_pitch=pitches[3])
 
 
@@ -99,7 +101,7 @@ def _pitch(t, name):
     return 0 if t.stride(0) == H * D or T <= 1 else t.stride(0)
 
 
-def _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=None, do=None):
+def _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=None, do=None, head_parts=0):
     hg = head_groups
     if q.dim() == 4:        # head-split [G][T][H/G][D]
         for t, name in ((q, "q"), (k, "k"), (v, "v"), (do, "do")):
@@ -112,16 +114,18 @@ def _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=None, do=None):
         T, hq, D = q.shape
         hkv = k.shape[1]
         pitches = (_pitch(q, "q"), _pitch(k, "k"), _pitch(v, "v"), _pitch(do, "do"))
-    return make_desc(cu_seqlens.numel() - 1, hq, hkv, D, cp, T, hg, scale, pitches)
+    return make_desc(cu_seqlens.numel() - 1, hq, hkv, D, cp, T, hg, scale, pitches, head_parts)
 
 
 def attn_fwd(q, k, v, cu_seqlens, cu_seqlens_padded, cp, *, head_groups=1, scale=0.0, out=None, lse=None,
-             workspace=None, status=None, stream=None, check=True, fused=False):
+             workspace=None, status=None, stream=None, check=True, fused=False, head_parts=0):
     """Forward: returns (o, lse).  q [T,Hq,D] (or [G,T,Hq/G,D]), k/v likewise, bf16 on cuda.
     q, k, v may be row-strided views (e.g. slices of a fused QKV buffer); o is dense.
-    fused=True runs ccg_attn_fwd_fused (one online softmax over all ring steps)."""
+    fused=True runs ccg_attn_fwd_fused (one online softmax over all ring steps).
+    head_parts=P > 1 runs the ring forward and merge over P head parts in turn
+    with a workspace sized for Hq/P heads (bitwise the same result)."""
     import torch
-    desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=v)
+    desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=v, head_parts=head_parts)
     o = torch.empty(q.shape, dtype=q.dtype, device=q.device) if out is None else _dense(out, "out")
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)

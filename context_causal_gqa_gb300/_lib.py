@@ -10,7 +10,7 @@ c_i32, c_i64, c_f32, c_vp, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
 
 class AttnDesc(ctypes.Structure):
     _fields_ = [("batch", c_i32), ("hq", c_i32), ("hkv", c_i32), ("head_dim", c_i32),
-                ("causal", c_i32), ("cp", c_i32), ("head_groups", c_i32), ("reserved", c_i32),
+                ("causal", c_i32), ("cp", c_i32), ("head_groups", c_i32), ("head_parts", c_i32),
                 ("total_tokens", c_i64), ("softmax_scale", c_f32),
                 ("q_pitch", c_i64), ("k_pitch", c_i64), ("v_pitch", c_i64), ("do_pitch", c_i64)]
 

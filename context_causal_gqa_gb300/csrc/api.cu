@@ -14,7 +14,7 @@
 namespace ccg {
 
 
-cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp, int bm,
+cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp, int hkv, int bm,
                         int bn, int cap_q, int cap_kv, int want, int step_only, PlanHeader* hdr,
                         WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items,
                         int32_t* status, cudaStream_t stream);
@@ -102,7 +102,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 ccg_status check_desc(const ccg_attn_desc* d) {
   if (d == nullptr) return CCG_ERR_INVALID_ARG;
-  if (d->batch < 1 || d->hq < 1 || d->hkv < 1 || d->total_tokens < 0 || d->reserved != 0)
+  if (d->batch < 1 || d->hq < 1 || d->hkv < 1 || d->total_tokens < 0 || d->head_parts < 0)
     return CCG_ERR_INVALID_ARG;
   if (d->causal != 1) return CCG_ERR_UNSUPPORTED;
   if (d->head_dim != 128 && d->head_dim != 256) return CCG_ERR_UNSUPPORTED;
@@ -110,10 +110,19 @@ ccg_status check_desc(const ccg_attn_desc* d) {
   if (d->cp < 1 || d->cp > kMaxCP) return CCG_ERR_UNSUPPORTED;
   if (d->head_groups < 1) return CCG_ERR_INVALID_ARG;
   if (d->hq % d->head_groups != 0 || d->hkv % d->head_groups != 0) return CCG_ERR_UNSUPPORTED;
+  // head partitioning: whole GQA groups per part, and in the head-split
+  // layout whole head groups (a part is then one contiguous sub-tensor)
+  if (d->head_parts > 1) {
+    if (d->hkv % d->head_parts != 0) return CCG_ERR_UNSUPPORTED;
+    if (d->head_groups > 1 && d->head_groups % d->head_parts != 0) return CCG_ERR_UNSUPPORTED;
+  }
   if (d->total_tokens % (2 * d->cp) != 0) return CCG_ERR_UNSUPPORTED;
   // 32-bit coordinates inside the kernels and TMA maps
   if (d->total_tokens * d->head_groups >= (int64_t(1) << 31)) return CCG_ERR_UNSUPPORTED;
   if (d->batch > (1 << 20)) return CCG_ERR_UNSUPPORTED;
+  // dK/dV work items (one per KV tile and kv head) are indexed with 32 bits
+  if ((d->total_tokens / 64 + int64_t(d->batch) * 2 * d->cp + 1) * d->hkv >= (int64_t(1) << 31))
+    return CCG_ERR_UNSUPPORTED;
   const int64_t pitches[4] = {d->q_pitch, d->k_pitch, d->v_pitch, d->do_pitch};
   const int64_t dense[4] = {int64_t(d->hq) * d->head_dim, int64_t(d->hkv) * d->head_dim,
                             int64_t(d->hkv) * d->head_dim, int64_t(d->hq) * d->head_dim};
@@ -139,6 +148,8 @@ float softmax_scale(const ccg_attn_desc* d) {
   return d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt(static_cast<float>(d->head_dim));
 }
 
+int head_parts_of(const ccg_attn_desc* d) { return d->head_parts > 1 ? d->head_parts : 1; }
+
 struct Layout {
   size_t hdr, fwd_items, dq_items, kv_items, o_parts, lse_parts, delta, total;
   int cap_q, cap_kv;
@@ -163,14 +174,15 @@ Layout workspace_layout(const ccg_attn_desc* d, int kind) {
   L.dq_items = off;
   off = align_up(off + (is_bwd ? size_t(L.cap_q) * sizeof(WorkItem) : 0), 256);
   L.kv_items = off;
-  off = align_up(off + (is_bwd ? size_t(L.cap_kv) * sizeof(WorkItem) : 0), 256);
-  const size_t rows = size_t(d->total_tokens) * d->hq;
+  off = align_up(off + (is_bwd ? size_t(L.cap_kv) * d->hkv * sizeof(WorkItem) : 0), 256);
+  // the partial slabs hold one head part (all heads without partitioning)
+  const size_t rows = size_t(d->total_tokens) * d->hq / head_parts_of(d);
   L.o_parts = off;
   off = align_up(off + (partials ? size_t(d->cp) * rows * d->head_dim * 2 : 0), 256);
   L.lse_parts = off;
   off = align_up(off + (partials ? size_t(d->cp) * rows * 4 : 0), 256);
   L.delta = off;
-  off = align_up(off + (is_bwd ? rows * 4 : 0), 256);
+  off = align_up(off + (is_bwd ? size_t(d->total_tokens) * d->hq * 4 : 0), 256);
   L.total = off;
   return L;
 }
@@ -409,17 +421,20 @@ ccg_status ccg_thd_unpack(const void* in_head_split, const int32_t* cu_seqlens_p
 // ring step into consecutive slabs of o_part / lse_part (one item per query
 // tile walks all steps of its rank); mode 2: every ring step in one online
 // softmax, the final O and LSE into o_part / lse_part.
-static ccg_status fwd_partials(const ccg_attn_desc* d, int step_only, const void* q, const void* k,
-                               const void* v, const int32_t* cu, const int32_t* cu_pad, void* o_part,
-                               int64_t o_slab, float* lse_part, int64_t lse_slab, void* workspace,
-                               const Layout& L, int32_t* status, cudaStream_t s, int* launches_out, int mode) {
+// Tensor maps and the launch of the forward attention kernel over the plan
+// already in the workspace.  mode 0: the partial of one ring step into
+// o_part / lse_part; mode 1: the partials of every ring step into
+// consecutive slabs of o_part / lse_part (one item per query tile walks all
+// steps of its rank); mode 2: every ring step in one online softmax, the
+// final O and LSE into o_part / lse_part.
+static ccg_status fwd_attention(const ccg_attn_desc* d, const void* q, const void* k, const void* v,
+                                const int32_t* cu, const int32_t* cu_pad, void* o_part, int64_t o_slab,
+                                float* lse_part, int64_t lse_slab, void* workspace, const Layout& L,
+                                int32_t* status, cudaStream_t s, int* launches_out, int mode) {
   int launches = *launches_out;
   auto* base = static_cast<uint8_t*>(workspace);
   auto* hdr = reinterpret_cast<PlanHeader*>(base + L.hdr);
   auto* items = reinterpret_cast<WorkItem*>(base + L.fwd_items);
-  CCG_LAUNCH("plan", s,
-             launch_plan(cu, cu_pad, d->batch, d->total_tokens, d->cp, kQTile, kMinKvTile, L.cap_q, L.cap_kv,
-                         mode == 0 ? 1 : 4, step_only, hdr, items, nullptr, nullptr, status, s));
   const int hg = d->head_groups;
   const int64_t rows = d->total_tokens * hg;
   const int bn = 128;                                   // forward K/V tile rows
@@ -434,6 +449,23 @@ static ccg_status fwd_partials(const ccg_attn_desc* d, int step_only, const void
                              num_sms_cached(), s));
   *launches_out = launches;
   return CCG_OK;
+}
+
+// The work plan (all ring steps, or step `step_only` in mode 0), then the
+// forward attention kernel.
+static ccg_status fwd_partials(const ccg_attn_desc* d, int step_only, const void* q, const void* k,
+                               const void* v, const int32_t* cu, const int32_t* cu_pad, void* o_part,
+                               int64_t o_slab, float* lse_part, int64_t lse_slab, void* workspace,
+                               const Layout& L, int32_t* status, cudaStream_t s, int* launches_out, int mode) {
+  int launches = *launches_out;
+  auto* base = static_cast<uint8_t*>(workspace);
+  CCG_LAUNCH("plan", s,
+             launch_plan(cu, cu_pad, d->batch, d->total_tokens, d->cp, d->hkv, kQTile, kMinKvTile, L.cap_q,
+                         L.cap_kv * d->hkv, mode == 0 ? 1 : 4, step_only, reinterpret_cast<PlanHeader*>(base + L.hdr),
+                         reinterpret_cast<WorkItem*>(base + L.fwd_items), nullptr, nullptr, status, s));
+  *launches_out = launches;
+  return fwd_attention(d, q, k, v, cu, cu_pad, o_part, o_slab, lse_part, lse_slab, workspace, L, status, s,
+                       launches_out, mode);
 }
 
 ccg_status ccg_attn_fwd_step(const ccg_attn_desc* desc, int32_t step, const void* q, const void* k,
@@ -469,31 +501,81 @@ ccg_status ccg_attn_fwd(const ccg_attn_desc* desc, const void* q, const void* k,
   if (desc->total_tokens == 0) return CCG_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   auto* base = static_cast<uint8_t*>(workspace);
-  const size_t rows = size_t(desc->total_tokens) * desc->hq;
-  const size_t o_stride = rows * desc->head_dim * 2, l_stride = rows * 4;
+  const int parts = head_parts_of(desc);
+  const int D = desc->head_dim;
+  const int64_t T = desc->total_tokens;
+  const size_t rows = size_t(T) * desc->hq / parts;          // partial rows of one head part
+  const size_t o_stride = rows * D * 2, l_stride = rows * 4;
   int launches = 0;
-  st = fwd_partials(desc, -1, q, k, v, cu_seqlens, cu_seqlens_padded, base + L.o_parts,
-                    static_cast<int64_t>(rows * desc->head_dim), reinterpret_cast<float*>(base + L.lse_parts),
-                    static_cast<int64_t>(rows), workspace, L, d_status, s, &launches, 1);
-  if (st != CCG_OK) return st;
-  MergeArgs a{};
-  for (int p = 0; p < desc->cp; ++p) {
-    a.o_parts[p] = base + L.o_parts + p * o_stride;
-    a.lse_parts[p] = reinterpret_cast<const float*>(base + L.lse_parts + p * l_stride);
+  // Head partitioning (TransformerEngine PR, native head partitioning): the
+  // ring forward and its merge run over one head part at a time, reusing the
+  // one set of partial slabs.  Each output row's partials and merge order
+  // are those of the unpartitioned run, so the results are bitwise equal.
+  for (int part = 0; part < parts; ++part) {
+    ccg_attn_desc pd = *desc;
+    const void *qp = q, *kp = k, *vp = v;
+    void* op = o;
+    float* lp = lse;
+    int out_heads = 0, out_h0 = 0;
+    if (parts > 1) {
+      pd.hq = desc->hq / parts;
+      pd.hkv = desc->hkv / parts;
+      pd.head_parts = 0;
+      if (desc->head_groups > 1) {
+        // whole head groups: the part is a contiguous [G_h/parts][T][H/G_h][D] sub-tensor
+        const int gpp = desc->head_groups / parts;
+        pd.head_groups = gpp;
+        const int64_t q_grp = T * (desc->hq / desc->head_groups), kv_grp = T * (desc->hkv / desc->head_groups);
+        qp = static_cast<const uint16_t*>(q) + int64_t(part) * gpp * q_grp * D;
+        kp = static_cast<const uint16_t*>(k) + int64_t(part) * gpp * kv_grp * D;
+        vp = static_cast<const uint16_t*>(v) + int64_t(part) * gpp * kv_grp * D;
+        op = static_cast<uint16_t*>(o) + int64_t(part) * gpp * q_grp * D;
+        lp = lse + int64_t(part) * gpp * q_grp;
+      } else {
+        // a head slice of every token row: the inputs keep their row pitch,
+        // the merge writes the part's heads of each output row
+        pd.q_pitch = input_pitch(desc, 0);
+        pd.k_pitch = input_pitch(desc, 1);
+        pd.v_pitch = input_pitch(desc, 2);
+        qp = static_cast<const uint16_t*>(q) + int64_t(part) * pd.hq * D;
+        kp = static_cast<const uint16_t*>(k) + int64_t(part) * pd.hkv * D;
+        vp = static_cast<const uint16_t*>(v) + int64_t(part) * pd.hkv * D;
+        out_heads = desc->hq;
+        out_h0 = part * pd.hq;
+      }
+    }
+    if (part == 0) {
+      CCG_LAUNCH("plan", s,
+                 launch_plan(cu_seqlens, cu_seqlens_padded, desc->batch, T, desc->cp, desc->hkv, kQTile,
+                             kMinKvTile, L.cap_q, L.cap_kv * desc->hkv, 4, -1,
+                             reinterpret_cast<PlanHeader*>(base + L.hdr),
+                             reinterpret_cast<WorkItem*>(base + L.fwd_items), nullptr, nullptr, d_status, s));
+    }
+    st = fwd_attention(&pd, qp, kp, vp, cu_seqlens, cu_seqlens_padded, base + L.o_parts,
+                       static_cast<int64_t>(rows * D), reinterpret_cast<float*>(base + L.lse_parts),
+                       static_cast<int64_t>(rows), workspace, L, d_status, s, &launches, 1);
+    if (st != CCG_OK) return st;
+    MergeArgs a{};
+    for (int p = 0; p < desc->cp; ++p) {
+      a.o_parts[p] = base + L.o_parts + p * o_stride;
+      a.lse_parts[p] = reinterpret_cast<const float*>(base + L.lse_parts + p * l_stride);
+    }
+    a.nparts = desc->cp;
+    a.cu = cu_seqlens;
+    a.cu_pad = cu_seqlens_padded;
+    a.B = desc->batch;
+    a.cp = desc->cp;
+    a.hpg = pd.hq / pd.head_groups;
+    a.T = T;
+    a.o = op;
+    a.lse = lp;
+    a.rows = static_cast<int64_t>(rows);
+    a.D = D;
+    a.status = d_status;
+    a.out_heads = out_heads;
+    a.out_h0 = out_h0;
+    CCG_LAUNCH("lse_merge", s, launch_lse_merge(a, num_sms_cached(), s));
   }
-  a.nparts = desc->cp;
-  a.cu = cu_seqlens;
-  a.cu_pad = cu_seqlens_padded;
-  a.B = desc->batch;
-  a.cp = desc->cp;
-  a.hpg = desc->hq / desc->head_groups;
-  a.T = desc->total_tokens;
-  a.o = o;
-  a.lse = lse;
-  a.rows = static_cast<int64_t>(rows);
-  a.D = desc->head_dim;
-  a.status = d_status;
-  CCG_LAUNCH("lse_merge", s, launch_lse_merge(a, num_sms_cached(), s));
   g_last_launches = launches;
   return CCG_OK;
 }
@@ -549,8 +631,8 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
   const int64_t rows = desc->total_tokens * hg;
   int launches = 0;
   CCG_LAUNCH("plan", s,
-             launch_plan(cu_seqlens, cu_seqlens_padded, desc->batch, desc->total_tokens, desc->cp,
-                         bwd_q_tile_rows(D), bwd_kv_tile_rows(D), L.cap_q, L.cap_kv, 2, -1, hdr, nullptr, dq_items,
+             launch_plan(cu_seqlens, cu_seqlens_padded, desc->batch, desc->total_tokens, desc->cp, desc->hkv,
+                         bwd_q_tile_rows(D), bwd_kv_tile_rows(D), L.cap_q, L.cap_kv * desc->hkv, 2, -1, hdr, nullptr, dq_items,
                          kv_items, d_status, s));
   CCG_LAUNCH("bwd_dot", s,
              launch_bwd_dot(o, dout, desc->total_tokens * desc->hq, D, desc->hq / desc->head_groups,

@@ -20,9 +20,9 @@
 //   stream through the slots.  Per contribution: S^T = K Q^T, dP^T = V dO^T,
 //   P^T and dS^T in registers -> TMEM (BF16), dV += P^T dO, dK += dS^T Q.
 // At D = 256 the two 256-column FP32 accumulators alone fill TMEM, so the
-// dK/dV pass runs as two kernels (dV, then dK), and the dQ and dK kernels
-// stream their 128-row tiles as two 128-column halves so that every product
-// runs at full width with both resident tiles in shared memory.
+// dK/dV pass runs as two kernels (dV, then dK), and every D = 256 kernel
+// streams its 128-row tiles as two 128-column halves, so that every product
+// runs at full width next to the resident tiles in shared memory.
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -35,8 +35,6 @@ namespace ccg {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-
-enum class KvMode { kBoth = 0, kDvOnly = 1, kDkOnly = 2 };
 
 struct BwdParams {
   const WorkItem* items;
@@ -91,15 +89,13 @@ struct DqCfg {
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
 };
 
-template <int D, KvMode M, int BN_, int NSLOT_, int NBUF_>
+template <int D, int BN_, int NSLOT_, int NBUF_>
 struct KvCfg {
   static constexpr int BM = 128;                 // key rows (MMA M)
   static constexpr int BN = BN_;                 // query rows per contribution tile
   static constexpr int NBUF = NBUF_;             // as in DqCfg
   static constexpr bool SPLIT = NBUF == 1;
-  static constexpr bool NEED_V = M != KvMode::kDvOnly;
-  static constexpr bool HAS_DP = M != KvMode::kDvOnly;
-  static constexpr int NRES = NEED_V ? 2 : 1;
+  static constexpr int NRES = 2;                 // K and V resident
   static constexpr int NSLOT = NSLOT_;
   static constexpr int RES_BYTES = BM * D * 2;
   static constexpr int SLOT_BYTES = BN * D * 2;
@@ -108,11 +104,11 @@ struct KvCfg {
   static constexpr int SMEM_VEC = SMEM_SLOT + NSLOT * SLOT_BYTES;   // [WG][-lse2 BN | -delta*scale BN]
   static constexpr int SMEM_BAR = SMEM_VEC + 2 * 2 * BN * 4;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
-  // TMEM: buffer b holds S^T at b*T_BUF and (if HAS_DP) dP^T at b*T_BUF + BN
-  static constexpr int T_BUF = HAS_DP ? 2 * BN : BN;
+  // TMEM: buffer b holds S^T at b*T_BUF and dP^T at b*T_BUF + BN
+  static constexpr int T_BUF = 2 * BN;
   static constexpr int T_DV = NBUF * T_BUF;
-  static constexpr int T_DK = M == KvMode::kBoth ? NBUF * T_BUF + D : NBUF * T_BUF;
-  static constexpr int ACC_END = NBUF * T_BUF + (M == KvMode::kBoth ? 2 * D : D);
+  static constexpr int T_DK = NBUF * T_BUF + D;
+  static constexpr int ACC_END = NBUF * T_BUF + 2 * D;
   // P^T / dS^T (BF16 A operands) are packed in place over S^T / dP^T: over
   // the tile's first BN/2 columns when one warpgroup owns the tile, over the
   // first half of each warpgroup's own columns when the columns are split
@@ -548,15 +544,13 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
 // ---------------------------------------------------------------------------
 // dK/dV pass
-template <class Cfg, int D, KvMode MODE>
+template <class Cfg, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const BwdParams p) {
   constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, KCH = D / 64;
-  constexpr bool DO_DV = MODE != KvMode::kDkOnly;
-  constexpr bool DO_DK = MODE != KvMode::kDvOnly;
-  const int item_idx = blockIdx.x / p.hkv;
+  const int item_idx = blockIdx.x;            // items carry their kv head
   if (item_idx >= p.hdr->n_kv) return;
   if (status_bad(p.status)) return;
 
@@ -578,7 +572,7 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WorkItem it = p.items[item_idx];
-  const int g = blockIdx.x % p.hkv;
+  const int g = it.step;                      // kv head of the item
   const int G = p.hq / p.hkv;
   const SeqInfo si = seq_info(p, it.b);
   const int k_lo = it.c * si.L + it.tile * BM;
@@ -612,9 +606,7 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // streamed tiles per contribution: kBoth: dO_i, Q_i; kDvOnly: Q_i (early), dO_i;
-  // kDkOnly: dO_i (early), Q_i
-  constexpr bool FIRST_IS_Q = MODE == KvMode::kDvOnly;
+  // streamed tiles per contribution: dO_i, then Q_i
 
   if (warp == 0) {
     if (lane == 0) {
@@ -628,16 +620,15 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_arrive_expect_tx(res_full, Cfg::NRES * Cfg::RES_BYTES);
         for (int kc = 0; kc < KCH; ++kc) {
           tma_load_3d(smem + Cfg::SMEM_RES + kc * BM * 128, &tm_k, kc * 64, g % p.hpg_kv, krow, res_full);
-          if (Cfg::NEED_V)
-            tma_load_3d(smem + Cfg::SMEM_RES + Cfg::RES_BYTES + kc * BM * 128, &tm_v, kc * 64, g % p.hpg_kv,
-                        krow, res_full);
+          tma_load_3d(smem + Cfg::SMEM_RES + Cfg::RES_BYTES + kc * BM * 128, &tm_v, kc * 64, g % p.hpg_kv,
+                      krow, res_full);
         }
         for (int t = 0; !itr.done && ok; ++t) {
           const int slot = t % NSLOT;
           if (t >= NSLOT) ok = mbar_wait(empty + slot, ((t / NSLOT) - 1) & 1, abort_flag);
           if (!ok) break;
           const bool first = (t & 1) == 0;
-          const bool is_q = first == FIRST_IS_Q;
+          const bool is_q = !first;
           const int hq = itr.head();
           const int qrow = static_cast<int>((hq / p.hpg_q) * p.T) + si.start + itr.q0();
           mbar_arrive_expect_tx(full + slot, Cfg::SLOT_BYTES);
@@ -674,28 +665,22 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         auto slot_mn = [&](int s2) { return slot_mn0 + s2 * kSlotStep; };
         ok = mbar_wait(res_full, 0, abort_flag);
         tc_fence_after();
-        auto slot_q = [&](int j) { return (FIRST_IS_Q ? 2 * j : 2 * j + 1); };
-        auto slot_do = [&](int j) { return (FIRST_IS_Q ? 2 * j + 1 : 2 * j); };
+        auto slot_q = [&](int j) { return 2 * j + 1; };
+        auto slot_do = [&](int j) { return 2 * j; };
         // S^T (and dP^T) of contribution j into buffer j % 2
         auto issue_sp = [&](int j) -> bool {
           const int tq = slot_q(j), tdo = slot_do(j);
           const int sq = tq % NSLOT, sdo = tdo % NSLOT;
           const int b = j % Cfg::NBUF;
           const uint32_t buf = tmem + b * Cfg::T_BUF;
-          // dP^T first: with dK only, dO_i is released right after it, so
-          // Q_{i+1} (which reuses dO_i's slot when slots are few) is loading
-          // for a whole contribution before S^T of i+1 needs it
-          if (DO_DK) {
-            if (!mbar_wait(full + sdo, (tdo / NSLOT) & 1, abort_flag)) return false;
-            tc_fence_after();
-            mma_kk<BM, BN, D>(buf + BN, v_desc, slot_k(sdo));
-            if (MODE == KvMode::kDkOnly) umma_commit(empty + sdo);  // dO_i done after dP^T
-          }
+          // dP^T first (dO_i arrives first)
+          if (!mbar_wait(full + sdo, (tdo / NSLOT) & 1, abort_flag)) return false;
+          tc_fence_after();
+          mma_kk<BM, BN, D>(buf + BN, v_desc, slot_k(sdo));
           if (!mbar_wait(full + sq, (tq / NSLOT) & 1, abort_flag)) return false;
           tc_fence_after();
           mma_kk<BM, BN, D>(buf, k_desc, slot_k(sq));
           umma_commit(s_full + b);
-          if (MODE == KvMode::kDvOnly) umma_commit(empty + sq);     // Q_i done after S^T
           return true;
         };
         int j_sp = 0;
@@ -710,15 +695,11 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           const uint32_t buf = tmem + b * Cfg::T_BUF;
           ok = mbar_wait(p_full + b, (j / Cfg::NBUF) & 1, abort_flag);
           if (!ok) break;
-          if (MODE == KvMode::kDvOnly) {
-            ok = mbar_wait(full + sdo, (tdo / NSLOT) & 1, abort_flag);
-            if (!ok) break;
-          }
           tc_fence_after();
-          if (DO_DV) mma_tn_split<BN, D, Cfg::SPLIT>(tmem + Cfg::T_DV, buf, slot_mn(sdo), j > 0);
-          if (DO_DK) mma_tn_split<BN, D, Cfg::SPLIT>(tmem + Cfg::T_DK, buf + BN, slot_mn(sq), j > 0);
-          if (MODE != KvMode::kDkOnly) umma_commit(empty + sdo);
-          if (MODE != KvMode::kDvOnly) umma_commit(empty + sq);
+          mma_tn_split<BN, D, Cfg::SPLIT>(tmem + Cfg::T_DV, buf, slot_mn(sdo), j > 0);
+          mma_tn_split<BN, D, Cfg::SPLIT>(tmem + Cfg::T_DK, buf + BN, slot_mn(sq), j > 0);
+          umma_commit(empty + sdo);
+          umma_commit(empty + sq);
           if (!ahead.done) {
             ok = issue_sp(j_sp++);
             ahead.next();
@@ -764,7 +745,7 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const bool qv = qp < itr.q_valid_hi;
         const int64_t gr = thd_row(si.start + qp, itr.head(), p.hpg_q, p.T);
         vb[col] = qv ? -__ldg(p.lse + gr) * kLog2e : 0.f;                 // -LSE in log2 units
-        vb[BN + col] = (qv && DO_DK) ? -__ldg(p.delta + gr) * p.scale : 0.f;  // -Delta * scale
+        vb[BN + col] = qv ? -__ldg(p.delta + gr) * p.scale : 0.f;  // -Delta * scale
       }
       mbar_arrive(vec_ready + wg);
       ok = __all_sync(0xffffffffu, mbar_wait(vec_ready + wg, k & 1, abort_flag));
@@ -785,7 +766,7 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
       for (int c = c_first; c < c_first + NC; ++c) {
         tmem_ld32(tb + c * 32, rs);
-        if (DO_DK) tmem_ld32(tb + BN + c * 32, rp);
+        tmem_ld32(tb + BN + c * 32, rp);
         tmem_wait_ld();
         if (masked) {
 #pragma unroll
@@ -805,16 +786,14 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                       a0, a1);
           const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
           pk[x] = pack_bf16x2(p0, p1);
-          if (DO_DK) {
-            const uint64_t t = fma_f32x2(f32x2(__uint_as_float(rp[2 * x]), __uint_as_float(rp[2 * x + 1])), sc2, nds[x]);
-            float d0, d1;
-            f32x2_split(mul_f32x2(f32x2(p0, p1), t), d0, d1);
-            dk[x] = pack_bf16x2(d0, d1);
-          }
+          const uint64_t t = fma_f32x2(f32x2(__uint_as_float(rp[2 * x]), __uint_as_float(rp[2 * x + 1])), sc2, nds[x]);
+          float d0, d1;
+          f32x2_split(mul_f32x2(f32x2(p0, p1), t), d0, d1);
+          dk[x] = pack_bf16x2(d0, d1);
         }
         const int packed = c_first * 32 + (c - c_first) * 16;   // in place, own columns
-        if (DO_DV) tmem_st16(tb + packed, pk);
-        if (DO_DK) tmem_st16(tb + BN + packed, dk);
+        tmem_st16(tb + packed, pk);
+        tmem_st16(tb + BN + packed, dk);
       }
       mbar_arrive(vec_free + wg);          // done reading this contribution's LSE/Delta
       tmem_wait_st();
@@ -830,11 +809,11 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const bool own = k_pos < k_hi;     // rows of this tile inside the chunk
       const int64_t grow = thd_row(si.start + k_pos, g, p.hpg_kv, p.T);
       uint32_t r[32];
-      // kBoth: warpgroup 0 writes dV, warpgroup 1 dK; single-output modes split the columns
-      const bool write_dv = DO_DV && (MODE != KvMode::kBoth || wg == 0);
-      const bool write_dk = DO_DK && (MODE != KvMode::kBoth || wg == 1);
-      const int c_begin = MODE == KvMode::kBoth ? 0 : wg * (D / 64);
-      const int c_end = MODE == KvMode::kBoth ? D / 32 : (wg + 1) * (D / 64);
+      // warpgroup 0 writes dV, warpgroup 1 dK
+      const bool write_dv = wg == 0;
+      const bool write_dk = wg == 1;
+      const int c_begin = 0;
+      const int c_end = D / 32;
       if (write_dv) {
 #pragma unroll 1
         for (int c = c_begin; c < c_end; ++c) {
@@ -924,8 +903,8 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   constexpr bool DQ = ROLE == HalfRole::kDq;
   constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, D = Cfg::D;
   using Iter = typename std::conditional<DQ, DqIter<BN>, KvIter<BN>>::type;
-  const int nheads = DQ ? p.hq : p.hkv;
-  const int item_idx = blockIdx.x / nheads;
+  // dQ role: one CTA per (item, q head); dK role: the items carry their kv head
+  const int item_idx = DQ ? blockIdx.x / p.hq : blockIdx.x;
   if (item_idx >= (DQ ? p.hdr->n_dq : p.hdr->n_kv)) return;
   if (status_bad(p.status)) return;
 
@@ -947,7 +926,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WorkItem it = p.items[item_idx];
-  const int head = blockIdx.x % nheads;        // q head (dQ role) or kv head (dK role)
+  const int head = DQ ? blockIdx.x % p.hq : it.step;   // q head (dQ role) or kv head (dK role)
   const int G = p.hq / p.hkv;
   const int g = DQ ? head / G : head;          // kv head
   const SeqInfo si = seq_info(p, it.b);
@@ -1227,6 +1206,300 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   if (warp == 2) tmem_dealloc(tmem, Cfg::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// D = 256 dV pass: one CTA per (128-row KV tile, kv head) with only K
+// resident (64 KB), so five half-tile slots stream the 128-column halves of
+// Q_i (for S^T = sum_h K[:, h] Q_i,h^T) and dO_i (for dV[:, h] += P^T dO_i,h)
+// of every contribution in the canonical order, and TMEM holds two S^T
+// buffers next to the 256-column dV accumulator: S^T of contribution i+1 is
+// computed while the softmax warpgroups form P^T of contribution i (they
+// split its 128 columns and pack P^T in place, over the first half of their
+// own columns).  Stream order: Q_0, then Q_{i+1}, dO_i for i = 0, 1, ...
+// (two halves each), which is the order the MMA warp uses them in.
+struct DvCfg {
+  static constexpr int D = 256;
+  static constexpr int BM = 128;                 // key rows (MMA M)
+  static constexpr int BN = 128;                 // query rows per contribution
+  static constexpr int DH = 128;
+  static constexpr int NSLOT = 5;
+  static constexpr int RES_BYTES = BM * D * 2;   // K
+  static constexpr int HALF_BYTES = BN * DH * 2;
+  static constexpr int SMEM_SLOT = RES_BYTES;
+  static constexpr int SMEM_VEC = SMEM_SLOT + NSLOT * HALF_BYTES;  // [WG][-lse2 x 64]
+  static constexpr int VEC_BYTES = 2 * (BN / 2) * 4;
+  static constexpr int SMEM_BAR = SMEM_VEC + VEC_BYTES;
+  static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
+  static constexpr int T_BUF = BN;               // S^T buffer b at b * T_BUF
+  static constexpr int T_ACC = 2 * BN;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(T_ACC + D <= TMEM_COLS, "TMEM");
+  static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_dv256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                      const BwdParams p) {
+  using Cfg = DvCfg;
+  constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, D = Cfg::D;
+  const int item_idx = blockIdx.x;              // items carry their kv head
+  if (item_idx >= p.hdr->n_kv) return;
+  if (status_bad(p.status)) return;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::SMEM_BAR);
+  uint64_t* res_full = bars;
+  uint64_t* full = bars + 1;              // [NSLOT]
+  uint64_t* empty = full + NSLOT;         // [NSLOT]
+  uint64_t* s_full = empty + NSLOT;       // [2]: S^T of the contribution in buffer b complete
+  uint64_t* p_full = s_full + 2;          // [2]: P^T packed in buffer b (both warpgroups)
+  uint64_t* acc_done = p_full + 2;
+  uint64_t* vec_ready = acc_done + 1;     // [2 WG]
+  uint64_t* vec_free = vec_ready + 2;     // [2 WG]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_free + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* vec = reinterpret_cast<float*>(smem + Cfg::SMEM_VEC);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WorkItem it = p.items[item_idx];
+  const int g = it.step;                       // kv head of the item
+  const int G = p.hq / p.hkv;
+  const SeqInfo si = seq_info(p, it.b);
+  const int k_lo = it.c * si.L + it.tile * BM;
+  const int k_hi = min(k_lo + BM, (it.c + 1) * si.L);
+  const int k_valid_hi = min(k_hi, si.S);
+
+  if (threadIdx.x == 0) {
+    mbar_init(res_full, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(p_full + b, 256);
+    }
+    mbar_init(acc_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(vec_ready + b, 128);
+      mbar_init(vec_free + b, 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int kv_group_row = static_cast<int>((g / p.hpg_kv) * p.T) + si.start;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      KvIter<BN> qi, di;                         // Q runs one contribution ahead of dO
+      qi.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
+      di.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
+      int issued[NSLOT];
+      for (int s = 0; s < NSLOT; ++s) issued[s] = 0;
+      bool ok = true;
+      int t = 0;                                 // stream position
+      auto load = [&](const KvIter<BN>& itr, const CUtensorMap* map) -> bool {
+        const int hq = itr.head();
+        const int row = static_cast<int>((hq / p.hpg_q) * p.T) + si.start + itr.q0();
+        for (int hf = 0; hf < 2; ++hf, ++t) {
+          const int slot = t % NSLOT;
+          if (t >= NSLOT && !mbar_wait(empty + slot, ((t / NSLOT) - 1) & 1, abort_flag)) return false;
+          mbar_arrive_expect_tx(full + slot, Cfg::HALF_BYTES);
+          uint8_t* dst = smem + Cfg::SMEM_SLOT + slot * Cfg::HALF_BYTES;
+          for (int kc = 0; kc < 2; ++kc)
+            tma_load_3d(dst + kc * BN * 128, map, (2 * hf + kc) * 64, hq % p.hpg_q, row, full + slot);
+          issued[slot]++;
+        }
+        return true;
+      };
+      if (!qi.done) {
+        mbar_arrive_expect_tx(res_full, Cfg::RES_BYTES);
+        for (int kc = 0; kc < D / 64; ++kc)
+          tma_load_3d(smem + kc * BM * 128, &tm_k, kc * 64, g % p.hpg_kv, kv_group_row + k_lo, res_full);
+        ok = load(qi, &tm_q);
+        qi.next();
+        while (ok && !di.done) {
+          if (!qi.done) {
+            ok = load(qi, &tm_q);
+            qi.next();
+            if (!ok) break;
+          }
+          ok = load(di, &tm_do);
+          di.next();
+        }
+        if (!ok) {
+          raise_status(p.status, CCG_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        volatile int never = 0;
+        mbar_wait(res_full, 0, &never, 200000000ull);
+        for (int s = 0; s < NSLOT; ++s)
+          if (issued[s] > 0) mbar_wait(full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      KvIter<BN> ahead;
+      ahead.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
+      bool ok = true;
+      if (!ahead.done) {
+        const uint64_t k_desc = smem_desc_sw128(smem_u32(smem), 16, 1024);
+        const uint32_t slot_base = smem_u32(smem + Cfg::SMEM_SLOT);
+        const uint64_t slot_k0 = smem_desc_sw128(slot_base, 16, 1024);
+        const uint64_t slot_mn0 = smem_desc_sw128(slot_base, BN * 128, 1024);
+        constexpr uint32_t kSlotStep = Cfg::HALF_BYTES >> 4;
+        int u = 0;                                // stream position consumed
+        ok = mbar_wait(res_full, 0, abort_flag);
+        tc_fence_after();
+        auto issue_st = [&](int j) -> bool {      // S^T of contribution j -> buffer j % 2
+          const uint32_t buf = tmem + (j & 1) * Cfg::T_BUF;
+          for (int hf = 0; hf < 2; ++hf, ++u) {
+            const int sl = u % NSLOT;
+            if (!mbar_wait(full + sl, (u / NSLOT) & 1, abort_flag)) return false;
+            tc_fence_after();
+            mma_kk_half(buf, k_desc + kmajor_step(128, 8 * hf), slot_k0 + sl * kSlotStep, hf > 0);
+            umma_commit(empty + sl);              // Q half done
+          }
+          umma_commit(s_full + (j & 1));
+          return true;
+        };
+        int j_st = 0;
+        while (ok && !ahead.done && j_st < 2) {
+          ok = issue_st(j_st++);
+          ahead.next();
+        }
+        for (int j = 0; ok && j < j_st; ++j) {
+          const int b = j & 1;
+          ok = mbar_wait(p_full + b, (j >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          for (int hf = 0; hf < 2 && ok; ++hf, ++u) {
+            const int sl = u % NSLOT;
+            ok = mbar_wait(full + sl, (u / NSLOT) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            mma_tn_split<BN, Cfg::DH, true>(tmem + Cfg::T_ACC + hf * Cfg::DH, tmem + b * Cfg::T_BUF,
+                                            slot_mn0 + sl * kSlotStep, j > 0);
+            umma_commit(empty + sl);              // dO half done
+          }
+          if (ok && !ahead.done) {
+            ok = issue_st(j_st++);
+            ahead.next();
+          }
+        }
+      }
+      if (!ok) {
+        raise_status(p.status, CCG_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit(acc_done);
+      volatile int never = 0;
+      mbar_wait(acc_done, 0, &never, 200000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax: P^T
+    const int wg = (warp - 4) >> 2;
+    const int row = ((warp & 3) << 5) + lane;        // key row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t0 = tmem + lane_base;
+    constexpr int NC = BN / 64;
+    const int c_first = wg * NC;
+    const int k_pos = k_lo + row;
+    const bool k_valid = k_pos < k_valid_hi;
+    float* vb = vec + wg * (BN / 2);                 // -LSE (log2 units) of this warpgroup's columns
+    const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2);
+    KvIter<BN> itr;
+    itr.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
+    const bool any = !itr.done;
+    bool ok = true;
+    for (int j = 0; !itr.done; ++j, itr.next()) {
+      const int b = j & 1;
+      const uint32_t tb = t0 + b * Cfg::T_BUF;
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(vec_free + wg, (j - 1) & 1, abort_flag));
+        if (!ok) break;
+      }
+      if (row < BN / 2) {
+        const int qp = itr.q0() + c_first * 32 + row;
+        const bool qv = qp < itr.q_valid_hi;
+        const int64_t gr = thd_row(si.start + qp, itr.head(), p.hpg_q, p.T);
+        vb[row] = qv ? -__ldg(p.lse + gr) * kLog2e : 0.f;
+      }
+      mbar_arrive(vec_ready + wg);
+      ok = __all_sync(0xffffffffu, mbar_wait(vec_ready + wg, j & 1, abort_flag));
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      const int q0 = itr.q0();
+      const int c_lo = k_valid ? max(0, k_pos - q0) : BN;
+      const int c_hi = k_valid ? itr.q_valid_hi - q0 : 0;
+      const bool masked = __any_sync(0xffffffffu, c_lo > 0 || c_hi < BN);
+      uint32_t rs[32];
+#pragma unroll
+      for (int c = c_first; c < c_first + NC; ++c) {
+        tmem_ld32(tb + c * 32, rs);
+        tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int col = c * 32 + x;
+            rs[x] = (col >= c_lo && col < c_hi) ? rs[x] : 0xff800000u;
+          }
+        }
+        const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(vb + (c - c_first) * 32);
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          float a0, a1;   // P = 2^(s * scale_log2 - lse2)
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2, nl2[x]),
+                      a0, a1);
+          pk[x] = pack_bf16x2(ex2_approx(a0), ex2_approx(a1));
+        }
+        tmem_st16(tb + c_first * 32 + (c - c_first) * 16, pk);   // in place, own columns
+      }
+      mbar_arrive(vec_free + wg);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full + b);
+    }
+    if (ok && any) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
+    if (!ok) {
+      raise_status(p.status, CCG_ERR_TIMEOUT);
+      *abort_flag = 1;
+    } else {
+      tc_fence_after();
+      const bool own = k_pos < k_hi;
+      const int64_t grow = thd_row(si.start + k_pos, g, p.hpg_kv, p.T);
+      uint32_t r[32];
+#pragma unroll 1
+      for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
+        if (any) {
+          tmem_ld32(t0 + Cfg::T_ACC + c * 32, r);
+          tmem_wait_ld();
+        }
+        if (own) store_row_bf16(p.out0 + grow * D + c * 32, r, 1.f, !any || !k_valid);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+}
+
 template <class K>
 cudaError_t set_smem(K kern, int bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -1244,15 +1517,15 @@ cudaError_t launch_dq(const CUtensorMap* m, const BwdParams& p, int grid_items, 
   return cudaGetLastError();
 }
 
-template <class Cfg, int D, KvMode MODE>
+template <class Cfg, int D>
 cudaError_t launch_kv(const CUtensorMap* m, const BwdParams& p, int grid_items, cudaStream_t s) {
   const int smem = Cfg::SMEM_TOTAL + 1024;
   static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_kv_kernel<Cfg, D, MODE>, smem); });
+  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_kv_kernel<Cfg, D>, smem); });
   if (e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(grid_items) * p.hkv;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  attn_bwd_kv_kernel<Cfg, D, MODE><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  attn_bwd_kv_kernel<Cfg, D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(m[0], m[1], m[2], m[3], p);
   return cudaGetLastError();
 }
 
@@ -1268,12 +1541,22 @@ cudaError_t launch_half(const CUtensorMap* m, const BwdParams& p, int grid_items
   return cudaGetLastError();
 }
 
-// Tile shapes.  D = 128: whole streamed tiles.  D = 256: the dQ and dK passes
-// stream 128-column halves of 128-row tiles (attn_bwd_half_kernel); the dV
-// pass keeps only K resident, so whole 128-row Q and dO tiles fit.
+cudaError_t launch_dv256(const CUtensorMap* m, const BwdParams& p, int grid_items, cudaStream_t s) {
+  const int smem = DvCfg::SMEM_TOTAL + 1024;
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_dv256_kernel, smem); });
+  if (e != cudaSuccess) return e;
+  const int64_t grid = static_cast<int64_t>(grid_items) * p.hkv;
+  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  attn_bwd_dv256_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  return cudaGetLastError();
+}
+
+// Tile shapes.  D = 128: whole streamed tiles, dK and dV in one kernel.
+// D = 256: the dQ and dK passes (attn_bwd_half_kernel) and the dV pass
+// (attn_bwd_dv256_kernel) stream 128-column halves of 128-row tiles.
 using Dq128 = DqCfg<128, 128, 5, 1>;
-using Kv128 = KvCfg<128, KvMode::kBoth, 128, 4, 1>;
-using Kv256V = KvCfg<256, KvMode::kDvOnly, 128, 2, 1>;
+using Kv128 = KvCfg<128, 128, 4, 1>;
 
 }  // namespace
 
@@ -1320,13 +1603,13 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
   p.out1 = static_cast<__nv_bfloat16*>(dk);
   if (D == 128) {
     prof_begin("attn_bwd_dkdv", stream);
-    e = launch_kv<Kv128, 128, KvMode::kBoth>(maps + 4, p, grid_kv, stream);
+    e = launch_kv<Kv128, 128>(maps + 4, p, grid_kv, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
     ++*launches;
   } else {
     prof_begin("attn_bwd_dv", stream);
-    e = launch_kv<Kv256V, 256, KvMode::kDvOnly>(maps + 4, p, grid_kv, stream);
+    e = launch_dv256(maps + 4, p, grid_kv, stream);
     prof_end(stream);
     if (e != cudaSuccess) return e;
     ++*launches;

@@ -27,7 +27,8 @@ struct PlanHeader {
 static_assert(sizeof(PlanHeader) == kPlanHeaderBytes, "plan header size");
 
 // One unit of work: sequence b, chunk c, tile index inside the chunk; for
-// forward items `step` is the ring step (0 in the backward lists).
+// forward items `step` is the ring step, for dK/dV items the kv head (0 in
+// the dQ list).
 struct WorkItem {
   int32_t b, c, tile, step;
 };
@@ -43,11 +44,15 @@ struct MergeArgs {
   const int32_t* cu_pad;
   int B, cp, hpg;
   int64_t T;
-  void* o;                        // bf16 [rows][D]
+  void* o;                        // bf16 [rows][D], or strided (out_heads > 0)
   float* lse;
   int64_t rows;
   int D;
   const int32_t* status;          // may be null
+  // out_heads > 0: the partials hold hpg heads per token and row r (token
+  // r / hpg, head r % hpg) is written to output row (r / hpg) * out_heads +
+  // out_h0 + r % hpg (a head subset of a [T][out_heads] tensor); 0: row r
+  int out_heads, out_h0;
 };
 
 // Sizes shared by host and device.

@@ -111,8 +111,9 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(MergeArgs a, int64_t row
       outv.z = pack_bf16x2(acc[4], acc[5]);
       outv.w = pack_bf16x2(acc[6], acc[7]);
     }
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + off) = outv;
-    if (sub == 0) a.lse[r] = lse_out;
+    const int64_t ro = a.out_heads > 0 ? (r / a.hpg) * a.out_heads + a.out_h0 + r % a.hpg : r;
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + ro * a.D + sub * 8) = outv;
+    if (sub == 0) a.lse[ro] = lse_out;
   }
 }
 

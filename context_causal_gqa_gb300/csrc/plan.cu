@@ -64,7 +64,7 @@ __device__ int block_emit(int n, int base, CountF count, WriteF write) {
 
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, int B, int64_t T,
-            int cp, int bm, int bn, int cap_q, int cap_kv, int want, int step_only, PlanHeader* hdr,
+            int cp, int hkv, int bm, int bn, int cap_q, int cap_kv, int want, int step_only, PlanHeader* hdr,
             WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items, int32_t* status) {
   __shared__ int bad;
   const int C = 2 * cp;
@@ -162,14 +162,16 @@ plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, 
     }
     if (slot > cap_q) overflow = 1;
     if (threadIdx.x == 0) hdr->n_dq = min(slot, cap_q);
-    // dK/dV pass: sequence-major; earlier KV chunks are seen by more queries, so they go first
+    // dK/dV pass: one item per (KV tile, kv head), (sequence, kv head)-major,
+    // so that the CTAs in flight stream the Q/dO of few kv heads' groups;
+    // earlier KV chunks are seen by more queries, so they go first
     {
-      auto count = [&](int i) { return all_tiles(i / C, bn); };
+      auto count = [&](int i) { return all_tiles(i / (hkv * C), bn); };
       auto write = [&](int i, int first, int n) {
-        const int b = i / C, j = i % C;
-        for (int t = 0; t < n && first + t < cap_kv; ++t) kv_items[first + t] = WorkItem{b, j, t, 0};
+        const int b = i / (hkv * C), g = (i / C) % hkv, j = i % C;
+        for (int t = 0; t < n && first + t < cap_kv; ++t) kv_items[first + t] = WorkItem{b, j, t, g};
       };
-      slot = block_emit(B * C, 0, count, write);
+      slot = block_emit(B * hkv * C, 0, count, write);
     }
     if (slot > cap_kv) overflow = 1;
     if (threadIdx.x == 0) hdr->n_kv = min(slot, cap_kv);
@@ -218,11 +220,11 @@ cudaError_t launch_bounded_wait_selftest(int32_t* status, uint32_t limit_us, cud
   return cudaGetLastError();
 }
 
-cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp, int bm,
+cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp, int hkv, int bm,
                         int bn, int cap_q, int cap_kv, int want, int step_only, PlanHeader* hdr,
                         WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items,
                         int32_t* status, cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(cu, cu_pad, B, T, cp, bm, bn, cap_q, cap_kv, want, step_only,
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(cu, cu_pad, B, T, cp, hkv, bm, bn, cap_q, cap_kv, want, step_only,
                                                hdr, fwd_items, dq_items, kv_items, status);
   return cudaGetLastError();
 }

@@ -69,13 +69,15 @@ class AttentionStep:
     pack to w.cp head groups, full-sequence attention per head group (CP = 1,
     no partials, no merge), unpack.  fused: forward with one online softmax
     over all ring steps (ccg_attn_fwd_fused) instead of partials + merge.
+    head_parts: P > 1 runs the ring forward and merge over P head parts in
+    turn (a workspace sized for Hq/P heads).
 
     The caller-facing buffers (inputs, o, lse, dq, dk, dv) form an IOSet; a
     second set is allocated on demand for the host pipeline, in which the
     copies of one step overlap the compute of its neighbours.
     """
 
-    def __init__(self, w, inputs, device="cuda", schedule="ring", fused=False):
+    def __init__(self, w, inputs, device="cuda", schedule="ring", fused=False, head_parts=0):
         load()
         if schedule not in ("ring", "a2a"):
             raise ValueError(schedule)
@@ -84,6 +86,7 @@ class AttentionStep:
         self.device = device
         self.schedule = schedule
         self.fused = fused or schedule == "a2a"
+        self.head_parts = head_parts
         self.attn_cp = 1 if schedule == "a2a" else w.cp
         T, hq, hkv, D, cp = w.total_tokens, w.hq, w.hkv, w.head_dim, w.cp
         self.split = bool(w.pack_roundtrip) or schedule == "a2a"
@@ -138,7 +141,7 @@ class AttentionStep:
             q, k, v, do, hg = x["q"], x["k"], x["v"], x["do"], 1
             o, dq, dk, dv = io.o, io.dq, io.dk, io.dv
         attn_fwd(q, k, v, cu, cpad, self.attn_cp, head_groups=hg, out=o, lse=io.lse, workspace=self.ws_f,
-                 fused=self.fused, **kw)
+                 fused=self.fused, head_parts=self.head_parts, **kw)
         n += last_launch_count()
         attn_bwd(q, k, v, o, do, io.lse, cu, cpad, self.attn_cp, head_groups=hg, dq=dq, dk=dk, dv=dv,
                  workspace=self.ws_b, **kw)

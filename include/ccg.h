@@ -81,7 +81,14 @@ typedef struct {
   int32_t cp;             /* emulated context-parallel ranks, 1..16                    */
   int32_t head_groups;    /* G_h >= 1: 1 = plain THD, >1 = head-split layout (e.g. the
                              A2A layout of ccg_thd_pack); hq, hkv divisible by it    */
-  int32_t reserved;       /* must be 0                                                 */
+  int32_t head_parts;     /* 0 or 1: no head partitioning; P > 1: ccg_attn_fwd runs the
+                             ring forward and merge over P head parts in turn (the
+                             PR's native head partitioning, Description and Native
+                             head partitioning: bounded workspace), reusing one set
+                             of partial slabs sized for hq/P heads; results are
+                             bitwise equal to P = 1.  hkv % P == 0, and with
+                             head_groups > 1, head_groups % P == 0.  The other
+                             entry points ignore it.                                  */
   int64_t total_tokens;   /* T = cu_seqlens_padded[B]                                  */
   float softmax_scale;    /* <= 0 selects 1/sqrt(D)                                    */
   /* Physical row pitch of the THD inputs: elements from one token's row to the
@@ -97,9 +104,10 @@ typedef struct {
 /* Bytes of device workspace needed for `desc` by ccg_attn_fwd (kind = 0),
  * ccg_attn_bwd (kind = 1) or ccg_attn_fwd_fused (kind = 2); 0 if `desc` or
  * `kind` is invalid.  The forward workspace holds the work plan plus CP
- * per-step partial outputs (CP x T x Hq x D BF16) and their LSE (CP x T x Hq
- * float); the backward workspace holds the work plan and Delta (T x Hq
- * float); the fused forward workspace holds only the work plan. */
+ * per-step partial outputs (CP x T x Hq/P x D BF16, P = head_parts or 1) and
+ * their LSE (CP x T x Hq/P float); the backward workspace holds the work plans
+ * and Delta (T x Hq float); the fused forward workspace holds only the work
+ * plan. */
 size_t ccg_workspace_size(const ccg_attn_desc* desc, int kind);
 
 /* Forward: O = softmax(scale Q K^T + causal mask) V and its row LSE, computed

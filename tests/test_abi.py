@@ -97,3 +97,22 @@ def test_host_side_rejections_need_no_gpu(L):
                           ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1000), None) == 2   # H % cp
     big = _desc(hq=32, hkv=8, total_tokens=1 << 20, cp=1)
     assert L.ccg_attn_bwd_noalloc(ctypes.byref(big), *([null] * 12), null) == 4
+
+
+def test_head_parts_shrink_the_forward_workspace_and_are_validated(L):
+    import context_causal_gqa_gb300 as ccg
+    T, hq, hkv, D, cp = 4096, 32, 8, 256, 8
+    base = ccg.workspace_size(ccg.make_desc(1, hq, hkv, D, cp, T), 0)
+    partial_bytes = cp * T * hq * (D * 2 + 4)              # CP partial O (bf16) and LSE (float) slabs
+    for P in (2, 4, 8):
+        ws = ccg.workspace_size(ccg.make_desc(1, hq, hkv, D, cp, T, head_parts=P), 0)
+        assert abs((base - ws) - partial_bytes * (1 - 1 / P)) <= 2 * 256
+    # the backward and fused-forward workspaces hold no partials
+    assert ccg.workspace_size(ccg.make_desc(1, hq, hkv, D, cp, T, head_parts=4), 1) == \
+        ccg.workspace_size(ccg.make_desc(1, hq, hkv, D, cp, T), 1)
+    # whole GQA groups per part; whole head groups per part in the head-split layout
+    assert ccg.workspace_size(ccg.make_desc(1, hq, hkv, D, cp, T, head_parts=3), 0) == 0
+    assert ccg.workspace_size(ccg.make_desc(1, hq, hkv, D, cp, T, head_parts=16), 0) == 0
+    assert ccg.workspace_size(ccg.make_desc(1, hq, hkv, D, cp, T, head_groups=2, head_parts=4), 0) == 0
+    assert ccg.workspace_size(ccg.make_desc(1, hq, hkv, D, cp, T, head_groups=8, head_parts=4), 0) > 0
+    assert ccg.workspace_size(ccg.make_desc(1, hq, hkv, D, cp, T, head_parts=-1), 0) == 0
