@@ -282,6 +282,19 @@ __device__ __forceinline__ void mma_tn_split(uint32_t d_tmem, uint32_t a_tmem, u
             (accumulate || k > 0) ? 1u : 0u);
 }
 
+// As mma_tn_split, with A packed by NWG warpgroups that split the KROWS
+// columns: warpgroup w's KROWS/NWG keys at a_tmem + w * KROWS/NWG, packed.
+template <int KROWS, int N, int NWG>
+__device__ __forceinline__ void mma_tn_wg(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, N, false, true);
+  constexpr int KPW = KROWS / (16 * NWG);          // k-steps per warpgroup's packed run
+  static_assert(KPW >= 1, "a warpgroup owns at least one 16-key step");
+#pragma unroll
+  for (int k = 0; k < KROWS / 16; ++k)
+    umma_ts(d_tmem, a_tmem + (k / KPW) * (KROWS / NWG) + (k % KPW) * 8, b_desc + mnmajor_step(k), idesc,
+            (accumulate || k > 0) ? 1u : 0u);
+}
+
 // D[tmem, M=128 x N=D] (+)= A[tmem bf16, 128 x KROWS] * B[smem tile KROWS rows x D, MN-major];
 // b_desc is the base descriptor of B built with LBO = KROWS*128.
 template <int KROWS, int D>
@@ -775,21 +788,29 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             rs[x] = (col >= c_lo && col < c_hi) ? rs[x] : 0xff800000u;
           }
         }
-        const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(vb + c * 32);        // -LSE2 pairs
-        const uint64_t* nds = reinterpret_cast<const uint64_t*>(vb + BN + c * 32);   // -Delta*scale pairs
+        // the columns' -LSE2 and -Delta*scale, four columns per 16-byte load
+        const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(vb + c * 32);
+        const ulonglong2* nd4 = reinterpret_cast<const ulonglong2*>(vb + BN + c * 32);
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          // P = 2^(s * scale_log2 - lse2); dS = P * (dP * scale - Delta * scale)
-          float a0, a1;
-          f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2, nl2[x]),
-                      a0, a1);
-          const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-          pk[x] = pack_bf16x2(p0, p1);
-          const uint64_t t = fma_f32x2(f32x2(__uint_as_float(rp[2 * x]), __uint_as_float(rp[2 * x + 1])), sc2, nds[x]);
-          float d0, d1;
-          f32x2_split(mul_f32x2(f32x2(p0, p1), t), d0, d1);
-          dk[x] = pack_bf16x2(d0, d1);
+        for (int x2 = 0; x2 < 8; ++x2) {
+          const ulonglong2 lv = nl4[x2], dv = nd4[x2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int x = 2 * x2 + e;
+            // P = 2^(s * scale_log2 - lse2); dS = P * (dP * scale - Delta * scale)
+            float a0, a1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2,
+                                  e ? lv.y : lv.x),
+                        a0, a1);
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            pk[x] = pack_bf16x2(p0, p1);
+            const uint64_t t = fma_f32x2(f32x2(__uint_as_float(rp[2 * x]), __uint_as_float(rp[2 * x + 1])), sc2,
+                                         e ? dv.y : dv.x);
+            float d0, d1;
+            f32x2_split(mul_f32x2(f32x2(p0, p1), t), d0, d1);
+            dk[x] = pack_bf16x2(d0, d1);
+          }
         }
         const int packed = c_first * 32 + (c - c_first) * 16;   // in place, own columns
         tmem_st16(tb + packed, pk);
@@ -865,7 +886,10 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 // its gradient product.
 enum class HalfRole { kDq = 0, kDk = 1 };
 
+template <int NWG_>
 struct HalfCfg {
+  static constexpr int NWG = NWG_;               // softmax warpgroups (they split every unit's columns)
+  static constexpr int THREADS = 128 + 128 * NWG;
   static constexpr int D = 256;
   static constexpr int BM = 128;                 // stationary rows (MMA M)
   static constexpr int BN = 128;                 // streamed rows per unit
@@ -874,14 +898,17 @@ struct HalfCfg {
   static constexpr int RES_BYTES = BM * D * 2;   // 64 KB
   static constexpr int HALF_BYTES = BN * DH * 2; // 32 KB
   static constexpr int SMEM_SLOT = 2 * RES_BYTES;
-  static constexpr int SMEM_VEC = SMEM_SLOT + NSLOT * HALF_BYTES;   // dK role: [WG][-lse2 64 | -Delta*scale 64]
-  static constexpr int VEC_BYTES = 2 * 2 * (BN / 2) * 4;
+  static constexpr int WCOLS = BN / NWG;         // columns of a unit per warpgroup
+  static constexpr int SMEM_VEC = SMEM_SLOT + NSLOT * HALF_BYTES;   // dK role: [WG][-lse2 | -Delta*scale] x WCOLS
+  static constexpr int VEC_BYTES = 2 * BN * 4;
   static constexpr int SMEM_BAR = SMEM_VEC + VEC_BYTES;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
   static constexpr int T_S = 0, T_P = BN, T_ACC = 2 * BN;
   static constexpr int TMEM_COLS = 512;
   static_assert(T_ACC + D <= TMEM_COLS, "TMEM");
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
+  static_assert(WCOLS % 32 == 0, "whole 32-column chunks per warpgroup");
+  static_assert(7 + 3 * 2 + 2 * NWG <= 30, "barrier region");
 };
 
 // D[tmem] (+)= A[smem, 128 rows, K-major] * B[smem, 128 rows, K-major]^T over
@@ -894,12 +921,12 @@ __device__ __forceinline__ void mma_kk_half(uint32_t d_tmem, uint64_t a_desc, ui
             (accumulate || k > 0) ? 1u : 0u);
 }
 
-template <HalfRole ROLE>
-__global__ void __launch_bounds__(kThreads, 1)
+template <HalfRole ROLE, int NWG>
+__global__ void __launch_bounds__(HalfCfg<NWG>::THREADS, 1)
 attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const BwdParams p) {
-  using Cfg = HalfCfg;
+  using Cfg = HalfCfg<NWG>;
   constexpr bool DQ = ROLE == HalfRole::kDq;
   constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, D = Cfg::D;
   using Iter = typename std::conditional<DQ, DqIter<BN>, KvIter<BN>>::type;
@@ -916,11 +943,11 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   uint64_t* full = bars + 1;              // [NSLOT]
   uint64_t* empty = full + NSLOT;         // [NSLOT]
   uint64_t* s_full = empty + NSLOT;       // S and dP of the unit complete
-  uint64_t* ds_full = s_full + 1;         // dS of the unit packed (both warpgroups)
+  uint64_t* ds_full = s_full + 1;         // dS of the unit packed (every warpgroup)
   uint64_t* acc_done = ds_full + 1;
-  uint64_t* vec_ready = acc_done + 1;     // [2 WG]
-  uint64_t* vec_free = vec_ready + 2;     // [2 WG]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_free + 2);
+  uint64_t* vec_ready = acc_done + 1;     // [NWG]
+  uint64_t* vec_free = vec_ready + NWG;   // [NWG]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_free + NWG);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* vec = reinterpret_cast<float*>(smem + Cfg::SMEM_VEC);
 
@@ -946,9 +973,9 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       mbar_init(empty + s, 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(ds_full, 256);
+    mbar_init(ds_full, 128 * NWG);
     mbar_init(acc_done, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NWG; ++b) {
       mbar_init(vec_ready + b, 128);
       mbar_init(vec_free + b, 128);
     }
@@ -1067,7 +1094,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           tc_fence_after();
           for (int h = 0; h < 2; ++h) {
             const int sl = (4 * j + 2 + h) % NSLOT;
-            mma_tn_split<BN, Cfg::DH, true>(tmem + Cfg::T_ACC + h * Cfg::DH, tmem + Cfg::T_P, slot_mn(sl), j > 0);
+            mma_tn_wg<BN, Cfg::DH, NWG>(tmem + Cfg::T_ACC + h * Cfg::DH, tmem + Cfg::T_P, slot_mn(sl), j > 0);
             umma_commit(empty + sl);                  // Y_h done
           }
           if (!ahead.done) {
@@ -1086,11 +1113,11 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int wg = (warp - 4) >> 2;                  // half of every unit's columns
+    const int wg = (warp - 4) >> 2;                  // the warpgroup's share of every unit's columns
     const int row = ((warp & 3) << 5) + lane;        // stationary row of the tile
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t0 = tmem + lane_base;
-    constexpr int NC = BN / 64;                       // 32-column chunks per warpgroup
+    constexpr int NC = Cfg::WCOLS / 32;               // 32-column chunks per warpgroup
     const int c_first = wg * NC;
     const int r_pos = r_lo + row;
     const bool r_valid = r_pos < r_valid_hi;
@@ -1104,7 +1131,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2), sc2 = f32x2(p.scale, p.scale);
     const uint64_t row_nl2 = f32x2(-lse2, -lse2), row_nds = f32x2(-dlt * p.scale, -dlt * p.scale);
-    float* vb = vec + wg * BN;                        // dK role: [-lse2 x 64 | -Delta*scale x 64]
+    float* vb = vec + wg * 2 * Cfg::WCOLS;            // dK role: [-lse2 | -Delta*scale] x WCOLS
     Iter itr;
     iter_init(itr);
     const bool any = !itr.done;
@@ -1121,12 +1148,12 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           ok = __all_sync(0xffffffffu, mbar_wait(vec_free + wg, (j - 1) & 1, abort_flag));
           if (!ok) break;
         }
-        if (row < BN / 2) {
+        if (row < Cfg::WCOLS) {
           const int qp = itr.q0() + c_first * 32 + row;
           const bool qv = qp < itr.q_valid_hi;
           const int64_t gr = thd_row(si.start + qp, itr.head(), p.hpg_q, p.T);
           vb[row] = qv ? -__ldg(p.lse + gr) * kLog2e : 0.f;
-          vb[BN / 2 + row] = qv ? -__ldg(p.delta + gr) * p.scale : 0.f;
+          vb[Cfg::WCOLS + row] = qv ? -__ldg(p.delta + gr) * p.scale : 0.f;
         }
         mbar_arrive(vec_ready + wg);
         ok = __all_sync(0xffffffffu, mbar_wait(vec_ready + wg, j & 1, abort_flag));
@@ -1155,22 +1182,35 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             rs[x] = (col >= c_lo && col < c_hi) ? rs[x] : 0xff800000u;
           }
         }
-        const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(vb + (c - c_first) * 32);
-        const uint64_t* nds = reinterpret_cast<const uint64_t*>(vb + BN / 2 + (c - c_first) * 32);
+        // dK role: the columns' -LSE2 and -Delta*scale, four columns per 16-byte load
+        const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(vb + (c - c_first) * 32);
+        const ulonglong2* nd4 = reinterpret_cast<const ulonglong2*>(vb + Cfg::WCOLS + (c - c_first) * 32);
         uint32_t pk[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          // P = 2^(s * scale_log2 - lse2); dS = P * (dP * scale - Delta * scale)
-          float a0, a1;
-          f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2,
-                                DQ ? row_nl2 : nl2[x]),
-                      a0, a1);
-          const uint64_t pv = f32x2(ex2_approx(a0), ex2_approx(a1));
-          const uint64_t t = fma_f32x2(f32x2(__uint_as_float(rp[2 * x]), __uint_as_float(rp[2 * x + 1])), sc2,
-                                       DQ ? row_nds : nds[x]);
-          float d0, d1;
-          f32x2_split(mul_f32x2(pv, t), d0, d1);
-          pk[x] = pack_bf16x2(d0, d1);
+        for (int x2 = 0; x2 < 8; ++x2) {
+          ulonglong2 lv, dv;
+          if constexpr (DQ) {
+            lv = make_ulonglong2(row_nl2, row_nl2);
+            dv = make_ulonglong2(row_nds, row_nds);
+          } else {
+            lv = nl4[x2];
+            dv = nd4[x2];
+          }
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int x = 2 * x2 + e;
+            // P = 2^(s * scale_log2 - lse2); dS = P * (dP * scale - Delta * scale)
+            float a0, a1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2,
+                                  e ? lv.y : lv.x),
+                        a0, a1);
+            const uint64_t pv = f32x2(ex2_approx(a0), ex2_approx(a1));
+            const uint64_t t = fma_f32x2(f32x2(__uint_as_float(rp[2 * x]), __uint_as_float(rp[2 * x + 1])), sc2,
+                                         e ? dv.y : dv.x);
+            float d0, d1;
+            f32x2_split(mul_f32x2(pv, t), d0, d1);
+            pk[x] = pack_bf16x2(d0, d1);
+          }
         }
         tmem_st16(t0 + Cfg::T_P + c_first * 32 + (c - c_first) * 16, pk);   // in place, own columns
       }
@@ -1191,7 +1231,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       __nv_bfloat16* dst = (DQ ? p.out0 : p.out1) + grow * D;
       uint32_t r[32];
 #pragma unroll 1
-      for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
+      for (int c = wg * (D / 32 / NWG); c < (wg + 1) * (D / 32 / NWG); ++c) {
         if (any) {                        // CTA-uniform: every lane loads
           tmem_ld32(t0 + Cfg::T_ACC + c * 32, r);
           tmem_wait_ld();
@@ -1459,14 +1499,20 @@ attn_bwd_dv256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             rs[x] = (col >= c_lo && col < c_hi) ? rs[x] : 0xff800000u;
           }
         }
-        const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(vb + (c - c_first) * 32);
+        const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(vb + (c - c_first) * 32);
         uint32_t pk[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          float a0, a1;   // P = 2^(s * scale_log2 - lse2)
-          f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2, nl2[x]),
-                      a0, a1);
-          pk[x] = pack_bf16x2(ex2_approx(a0), ex2_approx(a1));
+        for (int x2 = 0; x2 < 8; ++x2) {
+          const ulonglong2 lv = nl4[x2];                   // four columns' -LSE2 per 16-byte load
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int x = 2 * x2 + e;
+            float a0, a1;   // P = 2^(s * scale_log2 - lse2)
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2,
+                                  e ? lv.y : lv.x),
+                        a0, a1);
+            pk[x] = pack_bf16x2(ex2_approx(a0), ex2_approx(a1));
+          }
         }
         tmem_st16(tb + c_first * 32 + (c - c_first) * 16, pk);   // in place, own columns
       }
@@ -1529,15 +1575,23 @@ cudaError_t launch_kv(const CUtensorMap* m, const BwdParams& p, int grid_items, 
   return cudaGetLastError();
 }
 
+// Softmax warpgroups of the D = 256 dQ and dK passes: two, each thread
+// forming 64 of every unit's 128 columns (four warpgroups, at 96 registers a
+// thread, measured 3-6% slower).
+constexpr int kHalfWarpgroups = 2;
+
 template <HalfRole ROLE>
 cudaError_t launch_half(const CUtensorMap* m, const BwdParams& p, int grid_items, cudaStream_t s) {
-  const int smem = HalfCfg::SMEM_TOTAL + 1024;
+  using Cfg = HalfCfg<kHalfWarpgroups>;
+  const int smem = Cfg::SMEM_TOTAL + 1024;
   static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_half_kernel<ROLE>, smem); });
+  cudaError_t e = once_per_device(
+      attr_done, [&] { return set_smem(attn_bwd_half_kernel<ROLE, kHalfWarpgroups>, smem); });
   if (e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(grid_items) * (ROLE == HalfRole::kDq ? p.hq : p.hkv);
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  attn_bwd_half_kernel<ROLE><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  attn_bwd_half_kernel<ROLE, kHalfWarpgroups>
+      <<<static_cast<unsigned>(grid), Cfg::THREADS, smem, s>>>(m[0], m[1], m[2], m[3], p);
   return cudaGetLastError();
 }
 

@@ -147,6 +147,9 @@ bwd_dot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restr
 // range of such rows: copies hpg*D contiguous 16-bit elements between the
 // rank-major row and the head-split row.  Rank-major row of sequence row t:
 // rank r = owner of t's chunk; r*T/CP + start_b/CP + (chunk is r ? 0 : L_b) + i.
+// Every lane keeps four 16-byte loads in flight: rows of 128 vectors or more
+// are copied one at a time, shorter rows (one head of 256 or 128 columns)
+// several per warp iteration, each lane loading from its own row.
 template <bool kPack>
 __global__ void __launch_bounds__(256)
 thd_permute_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
@@ -156,30 +159,29 @@ thd_permute_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
   const int lane = threadIdx.x & 31;
   const int C = 2 * cp;
   const int hpg = H / cp;
-  const int64_t w16 = static_cast<int64_t>(hpg) * D / 8;   // uint4 per head-split row
+  const int w16 = hpg * D / 8;                               // uint4 per head-split row
   const int64_t row_w16 = static_cast<int64_t>(H) * D / 8;  // uint4 per rank-major row
   const int64_t nrows = static_cast<int64_t>(cp) * T;
   const int64_t warp_id = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t w_begin = warp_id * rows_per_warp;
   const int64_t w_end = min(nrows, w_begin + rows_per_warp);
-  SeqCache sc;
-  for (int64_t w = w_begin; w < w_end; ++w) {
+  SeqCache sc;                    // rows are visited in ascending order by every lane
+  // source and destination of head-split row w, and the number of rows from
+  // w on that stay in w's chunk (their rank-major rows are consecutive too);
+  // false if w's sequence breaks the promise
+  auto row_ptrs = [&](int64_t w, const uint4*& s, uint4*& d, int& run) -> bool {
     const int g = static_cast<int>(w / T);
-    const int64_t t = w % T;
+    const int64_t t = w - static_cast<int64_t>(g) * T;
     sc.get(cu_pad, B, t);
     const int start = static_cast<int>(sc.lo);
     const int P = static_cast<int>(sc.hi) - start;
-    if (P % C != 0 || P <= 0) {
-      if (lane == 0) raise_status(status, CCG_ERR_SEQLENS);
-      return;
-    }
+    if (P % C != 0 || P <= 0) return false;
     const int L = P / C;
     const int pos = static_cast<int>(t - start);
-    const int c = pos / L, i = pos % L;
+    const int c = pos / L, i = pos - c * L;
     const int r = chunk_owner(c, cp);
     const int64_t pr = static_cast<int64_t>(r) * (T / cp) + start / cp + (c == r ? 0 : L) + i;
-    const uint4* s;
-    uint4* d;
+    run = L - i;
     if (kPack) {
       s = src + pr * row_w16 + static_cast<int64_t>(g) * w16;
       d = dst + w * w16;
@@ -187,15 +189,68 @@ thd_permute_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
       s = src + w * w16;
       d = dst + pr * row_w16 + static_cast<int64_t>(g) * w16;
     }
-    int64_t u = lane;
-    for (; u + 96 < w16; u += 128) {             // four 16-byte loads in flight per lane
-      const uint4 x0 = __ldg(s + u), x1 = __ldg(s + u + 32), x2 = __ldg(s + u + 64), x3 = __ldg(s + u + 96);
-      d[u] = x0;
-      d[u + 32] = x1;
-      d[u + 64] = x2;
-      d[u + 96] = x3;
+    return true;
+  };
+  if (w16 >= 128) {
+    for (int64_t w = w_begin; w < w_end; ++w) {
+      const uint4* s;
+      uint4* d;
+      int run;
+      if (!row_ptrs(w, s, d, run)) {
+        if (lane == 0) raise_status(status, CCG_ERR_SEQLENS);
+        return;
+      }
+      int u = lane;
+      for (; u + 96 < w16; u += 128) {
+        const uint4 x0 = __ldg(s + u), x1 = __ldg(s + u + 32), x2 = __ldg(s + u + 64), x3 = __ldg(s + u + 96);
+        d[u] = x0;
+        d[u + 32] = x1;
+        d[u + 64] = x2;
+        d[u + 96] = x3;
+      }
+      for (; u < w16; u += 32) d[u] = __ldg(s + u);
     }
-    for (; u < w16; u += 32) d[u] = __ldg(s + u);
+    return;
+  }
+  const int nb = 128 / w16;                                  // rows per warp iteration
+  const int span = nb * w16;                                 // vectors per warp iteration (<= 128)
+  // strides between consecutive rows of one chunk on the source / destination side
+  const int64_t s_step = kPack ? row_w16 : w16, d_step = kPack ? w16 : row_w16;
+  for (int64_t w = w_begin; w < w_end; w += nb) {
+    const uint4* s0;
+    uint4* d0;
+    int run;
+    if (!row_ptrs(w, s0, d0, run)) {                          // the same for every lane
+      if (lane == 0) raise_status(status, CCG_ERR_SEQLENS);
+      return;
+    }
+    uint4 x[4];
+    uint4* dp[4];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int f = lane + 32 * j;
+      const int k = f / w16, u = f - k * w16;
+      dp[j] = nullptr;
+      if (f < span && w + k < w_end) {
+        const uint4* s = s0 + k * s_step;
+        uint4* d = d0 + k * d_step;
+        int run2;
+        if (k >= run && !row_ptrs(w + k, s, d, run2)) {      // the batch crosses a chunk end
+          bad = true;
+        } else {
+          x[j] = __ldg(s + u);
+          dp[j] = d + u;
+        }
+      }
+    }
+    if (__any_sync(0xffffffffu, bad)) {
+      if (lane == 0) raise_status(status, CCG_ERR_SEQLENS);
+      return;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (dp[j] != nullptr) *dp[j] = x[j];
   }
 }
 
