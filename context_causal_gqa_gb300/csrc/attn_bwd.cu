@@ -899,16 +899,13 @@ struct HalfCfg {
   static constexpr int HALF_BYTES = BN * DH * 2; // 32 KB
   static constexpr int SMEM_SLOT = 2 * RES_BYTES;
   static constexpr int WCOLS = BN / NWG;         // columns of a unit per warpgroup
-  static constexpr int SMEM_VEC = SMEM_SLOT + NSLOT * HALF_BYTES;   // dK role: [WG][-lse2 | -Delta*scale] x WCOLS
-  static constexpr int VEC_BYTES = 2 * BN * 4;
-  static constexpr int SMEM_BAR = SMEM_VEC + VEC_BYTES;
+  static constexpr int SMEM_BAR = SMEM_SLOT + NSLOT * HALF_BYTES;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
   static constexpr int T_S = 0, T_P = BN, T_ACC = 2 * BN;
   static constexpr int TMEM_COLS = 512;
   static_assert(T_ACC + D <= TMEM_COLS, "TMEM");
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
-  static_assert(WCOLS % 32 == 0, "whole 32-column chunks per warpgroup");
-  static_assert(7 + 3 * 2 + 2 * NWG <= 30, "barrier region");
+  static_assert(WCOLS == 64, "a lane holds two of its warpgroup's columns (dK role)");
 };
 
 // D[tmem] (+)= A[smem, 128 rows, K-major] * B[smem, 128 rows, K-major]^T over
@@ -945,11 +942,8 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   uint64_t* s_full = empty + NSLOT;       // S and dP of the unit complete
   uint64_t* ds_full = s_full + 1;         // dS of the unit packed (every warpgroup)
   uint64_t* acc_done = ds_full + 1;
-  uint64_t* vec_ready = acc_done + 1;     // [NWG]
-  uint64_t* vec_free = vec_ready + NWG;   // [NWG]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_free + NWG);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* vec = reinterpret_cast<float*>(smem + Cfg::SMEM_VEC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WorkItem it = p.items[item_idx];
@@ -975,10 +969,6 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     mbar_init(s_full, 1);
     mbar_init(ds_full, 128 * NWG);
     mbar_init(acc_done, 1);
-    for (int b = 0; b < NWG; ++b) {
-      mbar_init(vec_ready + b, 128);
-      mbar_init(vec_free + b, 128);
-    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1131,11 +1121,11 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2), sc2 = f32x2(p.scale, p.scale);
     const uint64_t row_nl2 = f32x2(-lse2, -lse2), row_nds = f32x2(-dlt * p.scale, -dlt * p.scale);
-    float* vb = vec + wg * 2 * Cfg::WCOLS;            // dK role: [-lse2 | -Delta*scale] x WCOLS
     Iter itr;
     iter_init(itr);
     const bool any = !itr.done;
     bool ok = true;
+    uint64_t col_l = 0, col_d = 0;
     for (int j = 0; !itr.done; ++j, itr.next()) {
       int c_lo = 0, c_hi = BN;                        // visible streamed columns of this row
       if constexpr (DQ) {
@@ -1143,21 +1133,26 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int kend = itr.diag ? min(itr.kv_hi, r_pos + 1) : itr.kv_hi;
         c_hi = r_valid ? kend - k0 : 0;
       } else {
-        // LSE (log2 units) and Delta of this contribution's query columns -> SMEM
-        if (j > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(vec_free + wg, (j - 1) & 1, abort_flag));
-          if (!ok) break;
+        // -LSE (log2 units) and -Delta * scale of this contribution's query
+        // columns: every lane holds two of its warpgroup's 64 columns (2*lane
+        // and 2*lane + 1) and hands them to the other lanes by shuffles, so
+        // that the softmax reads no shared memory (which the products keep busy)
+        {
+          const int qp0 = itr.q0() + c_first * 32 + 2 * lane;
+          float l0 = 0.f, l1 = 0.f, e0 = 0.f, e1 = 0.f;
+          if (qp0 < itr.q_valid_hi) {
+            const int64_t gr = thd_row(si.start + qp0, itr.head(), p.hpg_q, p.T);
+            l0 = -__ldg(p.lse + gr) * kLog2e;
+            e0 = -__ldg(p.delta + gr) * p.scale;
+          }
+          if (qp0 + 1 < itr.q_valid_hi) {
+            const int64_t gr = thd_row(si.start + qp0 + 1, itr.head(), p.hpg_q, p.T);
+            l1 = -__ldg(p.lse + gr) * kLog2e;
+            e1 = -__ldg(p.delta + gr) * p.scale;
+          }
+          col_l = f32x2(l0, l1);
+          col_d = f32x2(e0, e1);
         }
-        if (row < Cfg::WCOLS) {
-          const int qp = itr.q0() + c_first * 32 + row;
-          const bool qv = qp < itr.q_valid_hi;
-          const int64_t gr = thd_row(si.start + qp, itr.head(), p.hpg_q, p.T);
-          vb[row] = qv ? -__ldg(p.lse + gr) * kLog2e : 0.f;
-          vb[Cfg::WCOLS + row] = qv ? -__ldg(p.delta + gr) * p.scale : 0.f;
-        }
-        mbar_arrive(vec_ready + wg);
-        ok = __all_sync(0xffffffffu, mbar_wait(vec_ready + wg, j & 1, abort_flag));
-        if (!ok) break;
         const int q0 = itr.q0();
         // query column c is visible to this key row iff q0+c >= r_pos and q0+c < q_valid_hi
         c_lo = r_valid ? max(0, r_pos - q0) : BN;
@@ -1182,9 +1177,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             rs[x] = (col >= c_lo && col < c_hi) ? rs[x] : 0xff800000u;
           }
         }
-        // dK role: the columns' -LSE2 and -Delta*scale, four columns per 16-byte load
-        const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(vb + (c - c_first) * 32);
-        const ulonglong2* nd4 = reinterpret_cast<const ulonglong2*>(vb + Cfg::WCOLS + (c - c_first) * 32);
+        // dK role: the columns' -LSE2 and -Delta*scale, from the lanes that hold them
         uint32_t pk[16];
 #pragma unroll
         for (int x2 = 0; x2 < 8; ++x2) {
@@ -1193,8 +1186,11 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             lv = make_ulonglong2(row_nl2, row_nl2);
             dv = make_ulonglong2(row_nds, row_nds);
           } else {
-            lv = nl4[x2];
-            dv = nd4[x2];
+            const int src = (c - c_first) * 16 + 2 * x2;
+            lv.x = __shfl_sync(0xffffffffu, col_l, src);
+            lv.y = __shfl_sync(0xffffffffu, col_l, src + 1);
+            dv.x = __shfl_sync(0xffffffffu, col_d, src);
+            dv.y = __shfl_sync(0xffffffffu, col_d, src + 1);
           }
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
@@ -1214,7 +1210,6 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         tmem_st16(t0 + Cfg::T_P + c_first * 32 + (c - c_first) * 16, pk);   // in place, own columns
       }
-      if constexpr (!DQ) mbar_arrive(vec_free + wg);  // done reading this contribution's LSE/Delta
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(ds_full);

@@ -21,6 +21,8 @@ SMALL = [
     W.custom_workload("cp1_d128", [640], 4, 2, 128, 1),
     W.custom_workload("cp8_d128", [2048], 2, 1, 128, 8),
     W.custom_workload("cp8_d256_pad", [700, 1500], 4, 1, 256, 8, pad_to=128),
+    W.custom_workload("mha_d256_cp2_pad", [384, 200], 2, 2, 256, 2, pad_to=64),
+    W.custom_workload("gqa8_d256_cp4_ragged", [1100, 36], 8, 1, 256, 4, pad_to=8),
 ]
 
 
