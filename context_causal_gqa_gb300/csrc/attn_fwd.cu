@@ -62,9 +62,16 @@ struct FwdCfg {
   // At D=256 only two slots fit: K_{t+1} reloads while softmax(t) runs and
   // V_{t+1} while S(t+2) and softmax(t+1) run.
   static constexpr int NSLOT = (227 * 1024 - 2048 - NH * Q_BYTES) / KV_BYTES;
+  // D=256: the shared memory left over by the two K/V slots stages half of a
+  // finished segment's O rows (128 columns, 256 B a row), so that O can be
+  // released to the next segment's first P V product before the global
+  // stores of the partial are issued
+  static constexpr bool STAGE = (D == 256 && NH == 1);
+  static constexpr int STAGE_BYTES = STAGE ? kBM * (D / 2) * 2 : 0;
   static constexpr int SMEM_Q = 0;
   static constexpr int SMEM_KV = SMEM_Q + NH * Q_BYTES;
-  static constexpr int SMEM_BAR = SMEM_KV + NSLOT * KV_BYTES;
+  static constexpr int SMEM_STAGE = SMEM_KV + NSLOT * KV_BYTES;
+  static constexpr int SMEM_BAR = SMEM_STAGE + STAGE_BYTES;
   static constexpr int BAR_WORDS = 3 + 2 * NSLOT + 2 * NH * SBUF + 5 * NH;  // mbarriers (8 bytes each)
   static constexpr int SMEM_TOTAL = SMEM_BAR + 512;
   static constexpr int TMEM_HEAD = SBUF * BN + D;  // S buffers, then O
@@ -470,6 +477,60 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const float inv_l = lseg > 0.f ? 1.f / lseg : 0.f;
         const int64_t slab = p.mode == 2 ? 0 : step;
         uint4* dst = reinterpret_cast<uint4*>(p.o + slab * p.o_slab + orow * D);
+        if constexpr (Cfg::STAGE) {
+          // Each half of the row (128 columns) goes from TMEM to this thread's
+          // own 256-byte staging row (16-byte slot k at k ^ (row & 15), so that
+          // a warp's accesses hit every bank); each warp then stores its 32
+          // rows from the staging area two whole 256-byte row halves per
+          // instruction (coalesced).  O is free after the second half's TMEM
+          // loads.
+          uint4* stage = reinterpret_cast<uint4*>(smem + Cfg::SMEM_STAGE);
+          uint4* srow = stage + row * 16;
+          const int swz = row & 15;
+          const int wrow0 = (warp & 3) * 32;
+          const int u = lane & 15;
+          __nv_bfloat16* obase = p.o + slab * p.o_slab;
+          auto stage_half = [&](int c0) {
+#pragma unroll
+            for (int c = c0; c < c0 + D / 64; ++c) {
+              uint32_t r[32];
+              tmem_ld32(t_o + c * 32, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                uint4 w4;
+                w4.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * inv_l, __uint_as_float(r[8 * v4 + 1]) * inv_l);
+                w4.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * inv_l, __uint_as_float(r[8 * v4 + 3]) * inv_l);
+                w4.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * inv_l, __uint_as_float(r[8 * v4 + 5]) * inv_l);
+                w4.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * inv_l, __uint_as_float(r[8 * v4 + 7]) * inv_l);
+                srow[((c - c0) * 4 + v4) ^ swz] = w4;
+              }
+            }
+            __syncwarp();
+          };
+          // lane l stores slot (l & 15) of row 2k + (l >> 4) of this warp's rows
+          auto store_half = [&](int col0) {
+#pragma unroll 2
+            for (int k = 0; k < 16; ++k) {
+              const int r = 2 * k + (lane >> 4);
+              const int qp = ir.q_lo + wrow0 + r;
+              const uint4 v = stage[(wrow0 + r) * 16 + (u ^ ((wrow0 + r) & 15))];
+              if (qp < ir.q_hi) {
+                const int64_t orr = thd_row(ir.seq_start + qp, h0 + h, p.hpg_q, p.T);
+                reinterpret_cast<uint4*>(obase + orr * D + col0)[u] = v;
+              }
+            }
+            __syncwarp();
+          };
+          stage_half(0);
+          store_half(0);
+          stage_half(D / 64);
+          tc_fence_before();
+          mbar_arrive(o_free + h);
+          store_half(D / 2);
+          if (valid) p.lse[slab * p.lse_slab + orow] = (mseg + __log2f(lseg)) * kLn2;
+          return true;
+        }
         uint32_t r[32];
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
