@@ -259,6 +259,48 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
   }
 }
 
+// Writes one warp's 32 rows of 128 BF16 columns (four 32-column TMEM chunks
+// from t_col on, scaled by `mul`; zeros where `zero`) to global memory
+// through a 8 KB staging block in shared memory: each thread converts its own
+// row into its 256-byte staging row (16-byte slot k at k ^ (lane & 15), so
+// that the warp's accesses hit every bank), then the warp stores whole rows,
+// sixteen lanes per row (coalesced).  row_ptr(r) gives the destination of
+// the warp's row r, or nullptr for a row the tile does not own.
+template <class RowPtr>
+__device__ __forceinline__ void store_rows_staged(uint4* stage, uint32_t t_col, bool load, bool zero, float mul,
+                                                  int lane, RowPtr row_ptr) {
+  uint4* srow = stage + lane * 16;
+  const int swz = lane & 15;
+  uint32_t r[32];
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    if (load) {                       // warp-uniform
+      tmem_ld32(t_col + c * 32, r);
+      tmem_wait_ld();
+    }
+#pragma unroll
+    for (int v4 = 0; v4 < 4; ++v4) {
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (!zero) {
+        u.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * mul, __uint_as_float(r[8 * v4 + 1]) * mul);
+        u.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * mul, __uint_as_float(r[8 * v4 + 3]) * mul);
+        u.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * mul, __uint_as_float(r[8 * v4 + 5]) * mul);
+        u.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul);
+      }
+      srow[(c * 4 + v4) ^ swz] = u;
+    }
+  }
+  __syncwarp();
+  const int u = lane & 15;
+#pragma unroll 2
+  for (int k = 0; k < 16; ++k) {
+    const int rr = 2 * k + (lane >> 4);
+    uint4* d = row_ptr(rr);
+    if (d != nullptr) d[u] = stage[rr * 16 + (u ^ (rr & 15))];
+  }
+  __syncwarp();
+}
+
 // Issue the K-major (x) K-major product D[tmem] = A[smem tile, M rows] * B[smem tile, N rows]^T
 // over a contraction of length KD (both tiles TMA SW128 layout, 64-column chunks);
 // a_desc / b_desc are the tiles' base descriptors.
@@ -1219,20 +1261,21 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       raise_status(p.status, CCG_ERR_TIMEOUT);
       *abort_flag = 1;
     } else {
-      // each warpgroup writes half of the columns of the tile's rows: real
-      // rows get the gradient, padding rows 0
+      // each warpgroup writes its share of the columns of the tile's rows
+      // (real rows get the gradient, padding rows 0), through a staging
+      // block in the slot area, idle now that every product is done
       tc_fence_after();
-      const bool own = r_pos < r_hi;
-      __nv_bfloat16* dst = (DQ ? p.out0 : p.out1) + grow * D;
-      uint32_t r[32];
-#pragma unroll 1
-      for (int c = wg * (D / 32 / NWG); c < (wg + 1) * (D / 32 / NWG); ++c) {
-        if (any) {                        // CTA-uniform: every lane loads
-          tmem_ld32(t0 + Cfg::T_ACC + c * 32, r);
-          tmem_wait_ld();
-        }
-        if (own) store_row_bf16(dst + c * 32, r, 1.f, !any || !r_valid);
-      }
+      static_assert(D / NWG == 128, "a warpgroup writes 128 columns");
+      __nv_bfloat16* outp = (DQ ? p.out0 : p.out1) + wg * (D / NWG);
+      uint4* stage = reinterpret_cast<uint4*>(smem + Cfg::SMEM_SLOT) + (warp - 4) * 32 * 16;
+      const int wrow0 = r_lo + (warp & 3) * 32;
+      const int rhead = DQ ? head : g, rhpg = DQ ? p.hpg_q : p.hpg_kv;
+      store_rows_staged(stage, t0 + Cfg::T_ACC + wg * (D / NWG), any, !any || !r_valid, 1.f, lane,
+                        [&](int rr) -> uint4* {
+                          const int pos = wrow0 + rr;
+                          if (pos >= r_hi) return nullptr;
+                          return reinterpret_cast<uint4*>(outp + thd_row(si.start + pos, rhead, rhpg, p.T) * D);
+                        });
     }
   }
   tc_fence_before();
@@ -1521,18 +1564,18 @@ attn_bwd_dv256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       raise_status(p.status, CCG_ERR_TIMEOUT);
       *abort_flag = 1;
     } else {
+      // each warpgroup writes 128 of the tile rows' dV columns (padding rows
+      // 0) through a staging block in the idle slot area
       tc_fence_after();
-      const bool own = k_pos < k_hi;
-      const int64_t grow = thd_row(si.start + k_pos, g, p.hpg_kv, p.T);
-      uint32_t r[32];
-#pragma unroll 1
-      for (int c = wg * (D / 64); c < (wg + 1) * (D / 64); ++c) {
-        if (any) {
-          tmem_ld32(t0 + Cfg::T_ACC + c * 32, r);
-          tmem_wait_ld();
-        }
-        if (own) store_row_bf16(p.out0 + grow * D + c * 32, r, 1.f, !any || !k_valid);
-      }
+      __nv_bfloat16* outp = p.out0 + wg * (D / 2);
+      uint4* stage = reinterpret_cast<uint4*>(smem + Cfg::SMEM_SLOT) + (warp - 4) * 32 * 16;
+      const int wrow0 = k_lo + (warp & 3) * 32;
+      store_rows_staged(stage, t0 + Cfg::T_ACC + wg * (D / 2), any, !any || !k_valid, 1.f, lane,
+                        [&](int rr) -> uint4* {
+                          const int pos = wrow0 + rr;
+                          if (pos >= k_hi) return nullptr;
+                          return reinterpret_cast<uint4*>(outp + thd_row(si.start + pos, g, p.hpg_kv, p.T) * D);
+                        });
     }
   }
   tc_fence_before();
