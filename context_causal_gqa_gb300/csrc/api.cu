@@ -26,8 +26,8 @@ cudaError_t launch_bwd_dot(const void* o, const void* dout, int64_t rows, int D,
 cudaError_t launch_thd_permute(bool pack, const void* src, void* dst, const int32_t* cu_pad, int B,
                                int64_t T, int H, int D, int cp, int32_t* status, int num_sms,
                                cudaStream_t stream);
-cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
+cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tk2,
+                            const CUtensorMap& tv, const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
                             const int32_t* cu_pad, void* o, float* lse, int64_t o_slab, int64_t lse_slab,
                             int32_t* status, int cp, int hq, int hkv, int head_groups, int64_t T, int D,
                             float scale, int mode, int num_sms, cudaStream_t stream);
@@ -438,13 +438,15 @@ static ccg_status fwd_attention(const ccg_attn_desc* d, const void* q, const voi
   const int hg = d->head_groups;
   const int64_t rows = d->total_tokens * hg;
   const int bn = 128;                                   // forward K/V tile rows
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tk2, tv;
+  // tk2: half-tile boxes (bn/2 key rows), for the CTA pairs of the D = 256 kernel
   if (!make_thd_map(&tq, q, d->head_dim, d->hq / hg, rows, kQTile, input_pitch(d, 0)) ||
       !make_thd_map(&tk, k, d->head_dim, d->hkv / hg, rows, bn, input_pitch(d, 1)) ||
+      !make_thd_map(&tk2, k, d->head_dim, d->hkv / hg, rows, bn / 2, input_pitch(d, 1)) ||
       !make_thd_map(&tv, v, d->head_dim, d->hkv / hg, rows, bn, input_pitch(d, 2)))
     return CCG_ERR_CUDA;
   CCG_LAUNCH("attn_fwd", s,
-             launch_attn_fwd(tq, tk, tv, items, hdr, cu, cu_pad, o_part, lse_part, o_slab, lse_slab, status, d->cp,
+             launch_attn_fwd(tq, tk, tk2, tv, items, hdr, cu, cu_pad, o_part, lse_part, o_slab, lse_slab, status, d->cp,
                              d->hq, d->hkv, hg, d->total_tokens, d->head_dim, softmax_scale(d), mode,
                              num_sms_cached(), s));
   *launches_out = launches;

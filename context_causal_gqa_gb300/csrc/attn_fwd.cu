@@ -41,7 +41,7 @@ constexpr int kBM = 128;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale only past 2^8 growth
 
-template <int D, int NH>
+template <int D, int NH, bool PAIR = false>
 struct FwdCfg {
   // 128-key tiles: the S = Q K^T products run at N = 128 (full tensor rate;
   // N = 64 issues at two thirds of it) and the MMA warp's per-tile
@@ -56,21 +56,30 @@ struct FwdCfg {
   static constexpr int KCH = D / 64;                       // 64-wide (128-byte) column chunks
   static constexpr int Q_BYTES = kBM * D * 2;              // one head
   static constexpr int KV_BYTES = BN * D * 2;              // one K (or V) tile
-  // K and V tiles stream through NSLOT single-tile slots in the order the MMA
-  // warp consumes them (per item: K_0..K_{LA-1}, then K_{j+LA} and V_j for
-  // j = 0, 1, ...); a slot is released when its S or P V product is done.
-  // At D=256 only two slots fit: K_{t+1} reloads while softmax(t) runs and
-  // V_{t+1} while S(t+2) and softmax(t+1) run.
-  static constexpr int NSLOT = (227 * 1024 - 2048 - NH * Q_BYTES) / KV_BYTES;
-  // D=256: the shared memory left over by the two K/V slots stages half of a
-  // finished segment's O rows (128 columns, 256 B a row), so that O can be
-  // released to the next segment's first P V product before the global
-  // stores of the partial are issued
+  // A CTA pair (two q heads of one kv group, one per CTA, in M = 256
+  // products) holds half of every K tile in each CTA (BN/2 keys, all D
+  // columns: the N half of S = Q K^T) and half of every V tile (all BN keys,
+  // D/2 columns: the N half of O += P V).
+  static constexpr int SLOT_BYTES = PAIR ? KV_BYTES / 2 : KV_BYTES;
+  static constexpr int K_ROWS = PAIR ? BN / 2 : BN;        // key rows of a K slot
+  static constexpr int V_CH = PAIR ? KCH / 2 : KCH;        // 64-column chunks of a V slot
+  // D=256: shared memory beside the K/V slots stages half of a finished
+  // segment's O rows (128 columns, 256 B a row), so that O can be released
+  // to the next segment's first P V product before the global stores of
+  // the partial are issued
   static constexpr bool STAGE = (D == 256 && NH == 1);
   static constexpr int STAGE_BYTES = STAGE ? kBM * (D / 2) * 2 : 0;
+  // K and V tiles stream through NSLOT slots in the order the MMA warp
+  // consumes them (per item: K_0..K_{LA-1}, then K_{j+LA} and V_j for
+  // j = 0, 1, ...); a slot is released when its S or P V product is done.
+  // At D=256 one CTA holds only two whole-tile slots: K_{t+1} reloads while
+  // softmax(t) runs and V_{t+1} while S(t+2) and softmax(t+1) run.  A pair
+  // holds four half-tile slots in each CTA: V_t loads as soon as P V of tile
+  // t-2 is done, K_{t+1} as soon as S(t-1) is.
+  static constexpr int NSLOT = (227 * 1024 - 2048 - NH * Q_BYTES - (PAIR ? STAGE_BYTES : 0)) / SLOT_BYTES;
   static constexpr int SMEM_Q = 0;
   static constexpr int SMEM_KV = SMEM_Q + NH * Q_BYTES;
-  static constexpr int SMEM_STAGE = SMEM_KV + NSLOT * KV_BYTES;
+  static constexpr int SMEM_STAGE = SMEM_KV + NSLOT * SLOT_BYTES;
   static constexpr int SMEM_BAR = SMEM_STAGE + STAGE_BYTES;
   static constexpr int BAR_WORDS = 3 + 2 * NSLOT + 2 * NH * SBUF + 5 * NH;  // mbarriers (8 bytes each)
   static constexpr int SMEM_TOTAL = SMEM_BAR + 512;
@@ -79,6 +88,7 @@ struct FwdCfg {
   static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : (TMEM_USED <= 256 ? 256 : 512);
   static constexpr int THREADS = 128 + 128 * NH;
   static_assert(NSLOT >= 2, "K and V slots");
+  static_assert(!PAIR || (D == 256 && NH == 1), "CTA pairs: D = 256, one head per CTA");
   static_assert(BAR_WORDS * 8 + 8 + 4 * NH * SBUF <= 512, "barrier region");
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM budget");
@@ -198,17 +208,29 @@ __device__ __forceinline__ int count_tiles(const FwdParams& p, const WorkItem& i
   return n;
 }
 
-template <int D, int NH>
-__global__ void __launch_bounds__(FwdCfg<D, NH>::THREADS, 1)
+// PAIR: launched as (2,1,1) clusters; the two CTAs of a cluster take two q
+// heads of one kv group (heads 2i and 2i+1) of the same work item and run
+// every product as one M = 256 tcgen05 product issued by rank 0, each CTA
+// loading its half of every K and V tile (tm_k2: boxes of BN/2 key rows).
+template <int D, int NH, bool PAIR>
+__global__ void __launch_bounds__(FwdCfg<D, NH, PAIR>::THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using Cfg = FwdCfg<D, NH>;
+                const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v,
+                const FwdParams p) {
+  using Cfg = FwdCfg<D, NH, PAIR>;
   constexpr int BN = Cfg::BN, SBUF = Cfg::SBUF, NSLOT = Cfg::NSLOT, KCH = Cfg::KCH;
 
-  const int nhg = p.hq / NH;                           // head groups per item
+  // PAIR: work unit w = (item, head pair); this CTA's head is 2 (w % nhg) + rank
+  const int nhg = p.hq / (PAIR ? 2 : NH);              // work units per item
   const int64_t n_work = static_cast<int64_t>(p.hdr->n_fwd_all) * nhg;
-  if (static_cast<int64_t>(blockIdx.x) >= n_work) return;
-  if (status_bad(p.status)) return;
+  const int64_t w_first = PAIR ? blockIdx.x / 2 : blockIdx.x;
+  const int64_t w_step = PAIR ? gridDim.x / 2 : gridDim.x;
+  if (w_first >= n_work) return;                       // both CTAs of a pair, or neither
+  // (a pair never returns on the status word: its two reads could differ)
+  if (!PAIR && status_bad(p.status)) return;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  auto head_of = [&](int64_t w) { return PAIR ? static_cast<int>(w % nhg) * 2 + static_cast<int>(rank)
+                                              : static_cast<int>(w % nhg) * NH; };
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -245,24 +267,35 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(kv_full + s, 1);
       mbar_init(kv_empty + s, 1);
     }
+    // P ready / O read out: every softmax thread of the CTA, or (pair) one
+    // lane of each of the four softmax warps of both CTAs, on rank 0's barrier
+    const uint32_t n_soft = PAIR ? 8 : 128;
     for (int i = 0; i < NH * SBUF; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 128);
+      mbar_init(p_full + i, n_soft);
     }
     for (int h = 0; h < NH; ++h) {
       for (int i = 0; i < 4; ++i) mbar_init(o_done + h * 4 + i, 1);
-      mbar_init(o_free + h, 128);
+      mbar_init(o_free + h, n_soft);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  // a pair: the other CTA's barriers are initialised before anything arrives on them
+  if constexpr (PAIR) cluster_sync_all();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -270,7 +303,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(PAIR ? &tm_k2 : &tm_k);
       tma_prefetch_desc(&tm_v);
       int issued[NSLOT];
       for (int s = 0; s < NSLOT; ++s) issued[s] = 0;
@@ -278,21 +311,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       bool ok = true;
       int64_t u = 0;                                   // K/V tile positions streamed by this CTA
       int item_k = 0;
-      for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item_k) {
+      // a pair counts both CTAs' copies on rank 0's q_full / kv_full, which
+      // rank 0 alone arms with the bytes of both halves
+      const bool arm = !PAIR || rank == 0;
+      constexpr uint32_t kArmQ = (PAIR ? 2 : NH) * Cfg::Q_BYTES;
+      constexpr uint32_t kArmKV = PAIR ? 2 * Cfg::SLOT_BYTES : Cfg::SLOT_BYTES;
+      for (int64_t w = w_first; w < n_work && ok; w += w_step, ++item_k) {
         const WorkItem it = p.items[w / nhg];
-        const int h0 = static_cast<int>(w % nhg) * NH;
+        const int h0 = head_of(w);
         const int g = h0 / (p.hq / p.hkv);
         const ItemRows ir = item_rows(p, it);
         if (item_k > 0) ok = mbar_wait(q_free, (item_k - 1) & 1, abort_flag);
         if (!ok) break;
         const int qrow_base = ir.seq_start + ir.q_lo;
-        mbar_arrive_expect_tx(q_full, NH * Cfg::Q_BYTES);
+        if (arm) mbar_arrive_expect_tx(q_full, kArmQ);
         for (int h = 0; h < NH; ++h) {
           const int hq = h0 + h;
           const int row = static_cast<int>((hq / p.hpg_q) * p.T) + qrow_base;
-          for (int kc = 0; kc < KCH; ++kc)
-            tma_load_3d(smem + Cfg::SMEM_Q + h * Cfg::Q_BYTES + kc * kBM * 128, &tm_q, kc * 64,
-                        hq % p.hpg_q, row, q_full);
+          for (int kc = 0; kc < KCH; ++kc) {
+            uint8_t* dst = smem + Cfg::SMEM_Q + h * Cfg::Q_BYTES + kc * kBM * 128;
+            if constexpr (PAIR) tma_load_3d_pair(dst, &tm_q, kc * 64, hq % p.hpg_q, row, mapa_u32(q_full, 0));
+            else tma_load_3d(dst, &tm_q, kc * 64, hq % p.hpg_q, row, q_full);
+          }
         }
         ++q_loads;
         const int kv_group_row = static_cast<int>((g / p.hpg_kv) * p.T) + ir.seq_start;
@@ -300,11 +340,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const int sl = static_cast<int>(u % NSLOT);
           if (u >= NSLOT && !mbar_wait(kv_empty + sl, static_cast<uint32_t>((u / NSLOT) - 1) & 1, abort_flag))
             return false;
-          mbar_arrive_expect_tx(kv_full + sl, Cfg::KV_BYTES);
-          uint8_t* dst = smem + Cfg::SMEM_KV + sl * Cfg::KV_BYTES;
-          for (int kc = 0; kc < KCH; ++kc)
-            tma_load_3d(dst + kc * BN * 128, which == 0 ? &tm_k : &tm_v, kc * 64, g % p.hpg_kv,
-                        kv_group_row + k0, kv_full + sl);
+          if (arm) mbar_arrive_expect_tx(kv_full + sl, kArmKV);
+          uint8_t* dst = smem + Cfg::SMEM_KV + sl * Cfg::SLOT_BYTES;
+          if constexpr (PAIR) {
+            const uint32_t bar = mapa_u32(kv_full + sl, 0);
+            if (which == 0) {
+              // K: this CTA's BN/2 keys, every column
+              for (int kc = 0; kc < KCH; ++kc)
+                tma_load_3d_pair(dst + kc * Cfg::K_ROWS * 128, &tm_k2, kc * 64, g % p.hpg_kv,
+                                 kv_group_row + k0 + static_cast<int>(rank) * Cfg::K_ROWS, bar);
+            } else {
+              // V: every key, this CTA's D/2 columns
+              for (int kc = 0; kc < Cfg::V_CH; ++kc)
+                tma_load_3d_pair(dst + kc * BN * 128, &tm_v, (static_cast<int>(rank) * Cfg::V_CH + kc) * 64,
+                                 g % p.hpg_kv, kv_group_row + k0, bar);
+            }
+          } else {
+            for (int kc = 0; kc < KCH; ++kc)
+              tma_load_3d(dst + kc * BN * 128, which == 0 ? &tm_k : &tm_v, kc * 64, g % p.hpg_kv,
+                          kv_group_row + k0, kv_full + sl);
+          }
           issued[sl]++;
           ++u;
           return true;
@@ -326,24 +381,43 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         raise_status(p.status, CCG_ERR_TIMEOUT);
         *abort_flag = 1;
       }
-      // never leave a copy in flight into shared memory we are about to release
+      // never leave a copy in flight into shared memory we are about to
+      // release (a pair: rank 0's barriers count both CTAs' copies, and the
+      // CTAs leave together)
       volatile int never = 0;
-      if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, &never, 200000000ull);
-      for (int s = 0; s < NSLOT; ++s)
-        if (issued[s] > 0) mbar_wait(kv_full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+      if (arm) {
+        if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, &never, 200000000ull);
+        for (int s = 0; s < NSLOT; ++s)
+          if (issued[s] > 0) mbar_wait(kv_full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, BN, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
+    // (a pair: rank 0 issues for both CTAs; M = 256, each CTA's TMEM gets its
+    // 128 rows, and every completion is signalled in both CTAs)
+    if (lane == 0 && rank == 0) {
+      constexpr int MM = PAIR ? 2 * kBM : kBM;
+      constexpr uint32_t idesc_s = idesc_bf16_f32(MM, BN, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(MM, D, false, true);
+      auto mma_ss = [](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (PAIR) umma_ss_pair(d, a, b, id, acc);
+        else umma_ss(d, a, b, id, acc);
+      };
+      auto mma_ts = [](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (PAIR) umma_ts_pair(d, a, b, id, acc);
+        else umma_ts(d, a, b, id, acc);
+      };
+      auto commit = [](uint64_t* bar) {
+        if constexpr (PAIR) umma_commit_pair_both(bar);
+        else umma_commit(bar);
+      };
       const uint32_t q_base = smem_u32(smem + Cfg::SMEM_Q);
       const uint32_t kv_base = smem_u32(smem + Cfg::SMEM_KV);
       // base descriptors in registers; head h / slot sl are constant offsets
       const uint64_t q_desc0 = smem_desc_sw128(q_base, 16, 1024);
       const uint64_t k_desc0 = smem_desc_sw128(kv_base, 16, 1024);
       const uint64_t v_desc0 = smem_desc_sw128(kv_base, BN * 128, 1024);
-      constexpr uint32_t kQStep = Cfg::Q_BYTES >> 4, kKVStep = Cfg::KV_BYTES >> 4;
+      constexpr uint32_t kQStep = Cfg::Q_BYTES >> 4, kKVStep = Cfg::SLOT_BYTES >> 4;
       int64_t u = 0;     // K/V stream positions consumed (same order as the producer's)
       int64_t gs = 0;    // S tiles computed (S buffers, P and O barriers)
       bool ok = true;
@@ -358,9 +432,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t d_tmem = tmem + h * Cfg::TMEM_HEAD + buf * BN;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          umma_ss(d_tmem, q_desc0 + h * kQStep + kmajor_step(kBM, k), k_desc0 + sl * kKVStep + kmajor_step(BN, k),
-                  idesc_s, k > 0 ? 1u : 0u);
-        umma_commit(s_full + h * SBUF + buf);
+          mma_ss(d_tmem, q_desc0 + h * kQStep + kmajor_step(kBM, k),
+                 k_desc0 + sl * kKVStep + kmajor_step(Cfg::K_ROWS, k), idesc_s, k > 0 ? 1u : 0u);
+        commit(s_full + h * SBUF + buf);
       };
       auto issue_pv = [&](int h, int64_t t, int sl, bool first) {
         const int buf = static_cast<int>(t % SBUF);
@@ -368,22 +442,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t p_tmem = tmem + h * Cfg::TMEM_HEAD + buf * BN;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          umma_ts(d_tmem, p_tmem + k * 8, v_desc0 + sl * kKVStep + mnmajor_step(k), idesc_o,
-                  (!first || k > 0) ? 1u : 0u);
-        umma_commit(o_done + h * 4 + static_cast<int>(t % 4));
+          mma_ts(d_tmem, p_tmem + k * 8, v_desc0 + sl * kKVStep + mnmajor_step(k), idesc_o,
+                 (!first || k > 0) ? 1u : 0u);
+        commit(o_done + h * 4 + static_cast<int>(t % 4));
       };
       // all NH heads' S of tile t, K at the next stream position; then K is free
       auto issue_s_all = [&](int64_t t) -> bool {
         if (!wait_pos(u)) return false;
         const int sl = static_cast<int>(u % NSLOT);
         for (int h = 0; h < NH; ++h) issue_s(h, t, sl);
-        umma_commit(kv_empty + sl);
+        commit(kv_empty + sl);
         ++u;
         return true;
       };
       int item_k = 0;
       int64_t segs = 0;  // softmax segments opened by this CTA (one O read-out each)
-      for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x, ++item_k) {
+      for (int64_t w = w_first; w < n_work && ok; w += w_step, ++item_k) {
         const WorkItem it = p.items[w / nhg];
         const int n = count_tiles<BN>(p, it, item_rows(p, it));
         ok = mbar_wait(q_full, item_k & 1, abort_flag);
@@ -392,14 +466,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int a = min(Cfg::LA, n);
         for (int j = 0; j < a && ok; ++j) ok = issue_s_all(gs + j);
         if (!ok) break;
-        if (n <= Cfg::LA) umma_commit(q_free);          // every S of the item issued
+        if (n <= Cfg::LA) commit(q_free);               // every S of the item issued
         for (int j = 0; j < n && ok; ++j) {
           const int64_t t = gs + j;
           const bool ahead = j + Cfg::LA < n;
           if (SBUF > 1 && ahead) {
             ok = issue_s_all(t + Cfg::LA);               // S LA tiles ahead of this P V
             if (!ok) break;
-            if (j + Cfg::LA == n - 1) umma_commit(q_free);
+            if (j + Cfg::LA == n - 1) commit(q_free);
           }
           int64_t k_next = -1;                           // NH = 2: K of the next tile
           if (SBUF == 1 && ahead) {
@@ -429,10 +503,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (SBUF == 1 && ahead) issue_s(h, t + 1, static_cast<int>(k_next % NSLOT));
           }
           if (!ok) break;
-          umma_commit(kv_empty + vsl);
+          commit(kv_empty + vsl);
           if (SBUF == 1 && ahead) {
-            umma_commit(kv_empty + static_cast<int>(k_next % NSLOT));
-            if (j + 2 == n) umma_commit(q_free);
+            commit(kv_empty + static_cast<int>(k_next % NSLOT));
+            if (j + 2 == n) commit(q_free);
           }
         }
         gs += n;
@@ -441,7 +515,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         raise_status(p.status, CCG_ERR_TIMEOUT);
         *abort_flag = 1;
       }
-      umma_commit(mma_done);
+      if constexpr (PAIR) umma_commit_pair_own(mma_done);
+      else umma_commit(mma_done);
       volatile int never = 0;
       mbar_wait(mma_done, 0, &never, 200000000ull);
     }
@@ -454,9 +529,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t t_o = t_head + SBUF * BN;
     int64_t gs = 0;
     bool ok = true;
-    for (int64_t w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+    // P ready / O read out, to the MMA issuer (a pair: on rank 0's barrier,
+    // one lane per warp once the whole warp's TMEM accesses are done)
+    auto arrive_mma = [&](uint64_t* bar) {
+      if constexpr (PAIR) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_u32(bar, 0));
+      } else {
+        mbar_arrive(bar);
+      }
+    };
+    for (int64_t w = w_first; w < n_work && ok; w += w_step) {
       const WorkItem it = p.items[w / nhg];
-      const int h0 = static_cast<int>(w % nhg) * NH;
+      const int h0 = head_of(w);
       const ItemRows ir = item_rows(p, it);
       KvTileIter<BN> kt_it;
       kt_it.init(p, it, ir);
@@ -526,7 +611,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           store_half(0);
           stage_half(D / 64);
           tc_fence_before();
-          mbar_arrive(o_free + h);
+          arrive_mma(o_free + h);
           store_half(D / 2);
           if (valid) p.lse[slab * p.lse_slab + orow] = (mseg + __log2f(lseg)) * kLn2;
           return true;
@@ -538,7 +623,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_wait_ld();
           if (c == D / 32 - 1) {
             tc_fence_before();
-            mbar_arrive(o_free + h);
+            arrive_mma(o_free + h);
           }
           if (valid) {
 #pragma unroll
@@ -684,7 +769,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
           if (row == 0) seg_flag[h * SBUF + buf] = seg_open ? 1 : 0;
           tc_fence_before();
-          mbar_arrive(p_full + h * SBUF + buf);
+          arrive_mma(p_full + h * SBUF + buf);
         }
         if (pend) {
           pend = false;
@@ -706,33 +791,80 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  // a pair: neither CTA leaves (nor frees TMEM) while the other may still
+  // touch its shared memory or TMEM; rank 0's MMA thread has seen every
+  // product complete before it arrives
+  if constexpr (PAIR) cluster_sync_all();
+  else __syncthreads();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  if (warp == 2) {
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, Cfg::TMEM_COLS);
+    else tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  }
 }
 
-template <int D, int NH>
-cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FwdParams& p, int grid, cudaStream_t stream) {
-  using Cfg = FwdCfg<D, NH>;
-  auto kern = attn_fwd_kernel<D, NH>;
+template <int D, int NH, bool PAIR>
+cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tk2,
+                            const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t stream) {
+  using Cfg = FwdCfg<D, NH, PAIR>;
+  auto kern = attn_fwd_kernel<D, NH, PAIR>;
   static std::atomic<uint64_t> attr_done{0};
   const int smem = Cfg::SMEM_TOTAL + 1024;
   cudaError_t e = once_per_device(
       attr_done, [&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); });
   if (e != cudaSuccess) return e;
-  kern<<<grid, Cfg::THREADS, smem, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // persistent: as many pairs as can be resident at once (not every SM
+    // need belong to a usable pair)
+    static std::atomic<uint64_t> pairs_done{0};
+    static int max_pairs[64] = {};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = once_per_device(pairs_done, [&] {
+      cfg.gridDim = dim3(static_cast<unsigned>(grid / 2 * 2));
+      int n = 0;
+      const cudaError_t r = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (dev < 64) max_pairs[dev] = n;
+      return r;
+    });
+    if (e != cudaSuccess) return e;
+    const int pairs = min(grid / 2, dev < 64 && max_pairs[dev] > 0 ? max_pairs[dev] : grid / 2);
+    if (pairs < 1) return cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tk2, tv, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  } else {
+    kern<<<grid, Cfg::THREADS, smem, stream>>>(tq, tk, tk2, tv, p);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
 
 int fwd_heads_per_cta(int D, int group) { return (D == 128 && group % 2 == 0) ? 2 : 1; }
 
+// D = 256 with an even q-head group: CTA pairs, two q heads of one kv group
+// sharing every K/V tile load (each CTA loads half of it)
+bool fwd_uses_pairs(int D, int group) { return D == 256 && group % 2 == 0; }
+
 // Persistent launch over the combined work list: one CTA per SM (the work
 // count is only known on the device; CTAs with nothing to do exit at once).
-cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
+cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tk2,
+                            const CUtensorMap& tv, const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
                             const int32_t* cu_pad, void* o, float* lse, int64_t o_slab, int64_t lse_slab,
                             int32_t* status, int cp, int hq, int hkv, int head_groups, int64_t T, int D,
                             float scale, int mode, int num_sms, cudaStream_t stream) {
@@ -755,9 +887,10 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
   p.T = T;
   p.scale_log2 = scale * 1.4426950408889634f;
   const int nh = fwd_heads_per_cta(D, hq / hkv);
-  if (D == 128 && nh == 2) return launch_fwd_impl<128, 2>(tq, tk, tv, p, num_sms, stream);
-  if (D == 128) return launch_fwd_impl<128, 1>(tq, tk, tv, p, num_sms, stream);
-  if (D == 256) return launch_fwd_impl<256, 1>(tq, tk, tv, p, num_sms, stream);
+  if (D == 128 && nh == 2) return launch_fwd_impl<128, 2, false>(tq, tk, tk, tv, p, num_sms, stream);
+  if (D == 128) return launch_fwd_impl<128, 1, false>(tq, tk, tk, tv, p, num_sms, stream);
+  if (D == 256 && fwd_uses_pairs(D, hq / hkv)) return launch_fwd_impl<256, 1, true>(tq, tk, tk2, tv, p, num_sms, stream);
+  if (D == 256) return launch_fwd_impl<256, 1, false>(tq, tk, tk, tv, p, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 

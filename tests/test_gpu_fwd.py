@@ -38,6 +38,11 @@ SMALL = [
     W.custom_workload("ragged_d128_cp4", [1000, 24, 1], 4, 2, 128, 4, pad_to=8),
     W.custom_workload("cp1_d128", [640], 4, 2, 128, 1),
     W.custom_workload("cp8_d128", [2048], 2, 1, 128, 8),
+    # D = 256, one q head per kv head: the single-CTA kernel (no head pairs)
+    W.custom_workload("mha_d256_cp2", [384, 130], 2, 2, 256, 2, pad_to=4),
+    # D = 256, groups of 4 over 2 kv heads: CTA pairs on (0,1), (2,3), ... of
+    # each group, ragged sequences, every ring step of CP 8
+    W.custom_workload("gqa4_d256_cp8_ragged", [2048, 700, 33], 8, 2, 256, 8, pad_to=16),
 ]
 
 
