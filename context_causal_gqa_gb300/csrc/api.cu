@@ -27,7 +27,7 @@ cudaError_t launch_thd_permute(bool pack, const void* src, void* dst, const int3
                                int64_t T, int H, int D, int cp, int32_t* status, int num_sms,
                                cudaStream_t stream);
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tk2,
-                            const CUtensorMap& tv, const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
+                            const CUtensorMap& tv, const CUtensorMap& to, const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
                             const int32_t* cu_pad, void* o, float* lse, int64_t o_slab, int64_t lse_slab,
                             int32_t* status, int cp, int hq, int hkv, int head_groups, int64_t T, int D,
                             float scale, int mode, int num_sms, cudaStream_t stream);
@@ -222,6 +222,25 @@ bool make_thd_map(CUtensorMap* m, const void* base, int D, int hpg, int64_t rows
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 4-D map over an output in the head-grouped THD layout, `nslab` copies of it
+// `slab` elements apart (the ring steps' partials): dims (D, H/G_h, G_h*T,
+// nslab), rows H/G_h * D elements apart, 128-byte swizzled boxes of 64
+// columns x 1 head x 128 rows x 1 slab, for TMA stores.
+bool make_out_map(CUtensorMap* m, void* base, int D, int hpg, int64_t rows, int nslab, int64_t slab) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const int64_t pitch = static_cast<int64_t>(hpg) * D;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hpg), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(nslab)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(pitch) * 2,
+                           static_cast<cuuint64_t>(nslab > 1 ? slab : rows * pitch) * 2};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 #define CCG_LAUNCH(name, stream, expr)       \
@@ -438,15 +457,19 @@ static ccg_status fwd_attention(const ccg_attn_desc* d, const void* q, const voi
   const int hg = d->head_groups;
   const int64_t rows = d->total_tokens * hg;
   const int bn = 128;                                   // forward K/V tile rows
-  CUtensorMap tq, tk, tk2, tv;
-  // tk2: half-tile boxes (bn/2 key rows), for the CTA pairs of the D = 256 kernel
+  CUtensorMap tq, tk, tk2, tv, to;
+  // tk2: half-tile boxes (bn/2 key rows), for the CTA pairs of the D = 256
+  // kernel; to: the output (the steps' partials, o_slab apart), for its TMA
+  // stores of O (mode 0 and 2: one slab)
+  const int nslab = o_slab > 0 ? d->cp : 1;
   if (!make_thd_map(&tq, q, d->head_dim, d->hq / hg, rows, kQTile, input_pitch(d, 0)) ||
       !make_thd_map(&tk, k, d->head_dim, d->hkv / hg, rows, bn, input_pitch(d, 1)) ||
       !make_thd_map(&tk2, k, d->head_dim, d->hkv / hg, rows, bn / 2, input_pitch(d, 1)) ||
-      !make_thd_map(&tv, v, d->head_dim, d->hkv / hg, rows, bn, input_pitch(d, 2)))
+      !make_thd_map(&tv, v, d->head_dim, d->hkv / hg, rows, bn, input_pitch(d, 2)) ||
+      !make_out_map(&to, o_part, d->head_dim, d->hq / hg, rows, nslab, o_slab))
     return CCG_ERR_CUDA;
   CCG_LAUNCH("attn_fwd", s,
-             launch_attn_fwd(tq, tk, tk2, tv, items, hdr, cu, cu_pad, o_part, lse_part, o_slab, lse_slab, status, d->cp,
+             launch_attn_fwd(tq, tk, tk2, tv, to, items, hdr, cu, cu_pad, o_part, lse_part, o_slab, lse_slab, status, d->cp,
                              d->hq, d->hkv, hg, d->total_tokens, d->head_dim, softmax_scale(d), mode,
                              num_sms_cached(), s));
   *launches_out = launches;

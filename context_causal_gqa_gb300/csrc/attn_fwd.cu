@@ -212,11 +212,13 @@ __device__ __forceinline__ int count_tiles(const FwdParams& p, const WorkItem& i
 // heads of one kv group (heads 2i and 2i+1) of the same work item and run
 // every product as one M = 256 tcgen05 product issued by rank 0, each CTA
 // loading its half of every K and V tile (tm_k2: boxes of BN/2 key rows).
+// tm_o (D = 256): the output (partials) as (D, heads of a group, rows, step
+// slab), boxes of 64 columns x 128 rows, for the TMA stores of O.
 template <int D, int NH, bool PAIR>
 __global__ void __launch_bounds__(FwdCfg<D, NH, PAIR>::THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v,
-                const FwdParams p) {
+                const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   using Cfg = FwdCfg<D, NH, PAIR>;
   constexpr int BN = Cfg::BN, SBUF = Cfg::SBUF, NSLOT = Cfg::NSLOT, KCH = Cfg::KCH;
 
@@ -563,6 +565,57 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int64_t slab = p.mode == 2 ? 0 : step;
         uint4* dst = reinterpret_cast<uint4*>(p.o + slab * p.o_slab + orow * D);
         if constexpr (Cfg::STAGE) {
+          if (ir.q_hi - ir.q_lo == kBM) {
+            // A whole tile: each 64-column quarter of O goes from TMEM through
+            // this thread's row of a 16 KB box (128-byte swizzle: a warp's
+            // 16-byte writes to 32 rows hit every bank) and leaves by one TMA
+            // store issued by one thread; the two boxes alternate, so the
+            // softmax threads never wait on global stores, only (rarely) on a
+            // box's previous store having read it.
+            const bool issuer = warp == 4 && lane == 0;
+            uint8_t* sbox = smem + Cfg::SMEM_STAGE;
+            const int grow = static_cast<int>(((h0 + h) / p.hpg_q) * p.T) + ir.seq_start + ir.q_lo;
+            const int hc = (h0 + h) % p.hpg_q;
+            const int slab_c = p.o_slab > 0 ? static_cast<int>(slab) : 0;   // one-slab outputs: slab 0
+            const int swz = row & 7;
+#pragma unroll 1
+            for (int qq = 0; qq < D / 64; ++qq) {
+              uint8_t* box = sbox + (qq & 1) * (kBM * 128);
+              if (issuer) bulk_wait_group_read<1>();    // the box's previous store has read it
+              named_bar_sync(1, 128);
+              uint32_t r0[32], r1[32];
+              tmem_ld32(t_o + qq * 64, r0);
+              tmem_ld32(t_o + qq * 64 + 32, r1);
+              tmem_wait_ld();
+              if (qq == D / 64 - 1) {
+                tc_fence_before();
+                arrive_mma(o_free + h);                 // O is free for the next segment's first P V
+              }
+              uint4* brow = reinterpret_cast<uint4*>(box + row * 128);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t* r = j < 4 ? r0 + 8 * j : r1 + 8 * (j - 4);
+                uint4 w4;
+                w4.x = pack_bf16x2(__uint_as_float(r[0]) * inv_l, __uint_as_float(r[1]) * inv_l);
+                w4.y = pack_bf16x2(__uint_as_float(r[2]) * inv_l, __uint_as_float(r[3]) * inv_l);
+                w4.z = pack_bf16x2(__uint_as_float(r[4]) * inv_l, __uint_as_float(r[5]) * inv_l);
+                w4.w = pack_bf16x2(__uint_as_float(r[6]) * inv_l, __uint_as_float(r[7]) * inv_l);
+                brow[j ^ swz] = w4;
+              }
+              fence_proxy_async_smem();
+              named_bar_sync(1, 128);
+              if (issuer) {
+                tma_store_4d(&tm_o, box, qq * 64, hc, grow, slab_c);
+                bulk_commit_group();
+              }
+            }
+            if (valid) p.lse[slab * p.lse_slab + orow] = (mseg + __log2f(lseg)) * kLn2;
+            return true;
+          }
+          // (a partial tile) the staging area is free once the TMA stores of
+          // earlier whole tiles have read it
+          if (warp == 4 && lane == 0) bulk_wait_group_read<0>();
+          named_bar_sync(1, 128);
           // Each half of the row (128 columns) goes from TMEM to this thread's
           // own 256-byte staging row (16-byte slot k at k ^ (row & 15), so that
           // a warp's accesses hit every bank); each warp then stores its 32
@@ -789,6 +842,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       raise_status(p.status, CCG_ERR_TIMEOUT);
       *abort_flag = 1;
     }
+    // the TMA stores of O have read their boxes and written global memory
+    if (Cfg::STAGE && warp == 4 && lane == 0) bulk_wait_group<0>();
   }
   tc_fence_before();
   __syncwarp();
@@ -806,7 +861,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 template <int D, int NH, bool PAIR>
 cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tk2,
-                            const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t stream) {
+                            const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p, int grid,
+                            cudaStream_t stream) {
   using Cfg = FwdCfg<D, NH, PAIR>;
   auto kern = attn_fwd_kernel<D, NH, PAIR>;
   static std::atomic<uint64_t> attr_done{0};
@@ -844,11 +900,11 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
     const int pairs = min(grid / 2, dev < 64 && max_pairs[dev] > 0 ? max_pairs[dev] : grid / 2);
     if (pairs < 1) return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tk2, tv, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tk2, tv, to, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   } else {
-    kern<<<grid, Cfg::THREADS, smem, stream>>>(tq, tk, tk2, tv, p);
+    kern<<<grid, Cfg::THREADS, smem, stream>>>(tq, tk, tk2, tv, to, p);
     return cudaGetLastError();
   }
 }
@@ -864,7 +920,7 @@ bool fwd_uses_pairs(int D, int group) { return D == 256 && group % 2 == 0; }
 // Persistent launch over the combined work list: one CTA per SM (the work
 // count is only known on the device; CTAs with nothing to do exit at once).
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tk2,
-                            const CUtensorMap& tv, const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
+                            const CUtensorMap& tv, const CUtensorMap& to, const WorkItem* items, const PlanHeader* hdr, const int32_t* cu,
                             const int32_t* cu_pad, void* o, float* lse, int64_t o_slab, int64_t lse_slab,
                             int32_t* status, int cp, int hq, int hkv, int head_groups, int64_t T, int D,
                             float scale, int mode, int num_sms, cudaStream_t stream) {
@@ -887,10 +943,11 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
   p.T = T;
   p.scale_log2 = scale * 1.4426950408889634f;
   const int nh = fwd_heads_per_cta(D, hq / hkv);
-  if (D == 128 && nh == 2) return launch_fwd_impl<128, 2, false>(tq, tk, tk, tv, p, num_sms, stream);
-  if (D == 128) return launch_fwd_impl<128, 1, false>(tq, tk, tk, tv, p, num_sms, stream);
-  if (D == 256 && fwd_uses_pairs(D, hq / hkv)) return launch_fwd_impl<256, 1, true>(tq, tk, tk2, tv, p, num_sms, stream);
-  if (D == 256) return launch_fwd_impl<256, 1, false>(tq, tk, tk, tv, p, num_sms, stream);
+  if (D == 128 && nh == 2) return launch_fwd_impl<128, 2, false>(tq, tk, tk, tv, to, p, num_sms, stream);
+  if (D == 128) return launch_fwd_impl<128, 1, false>(tq, tk, tk, tv, to, p, num_sms, stream);
+  if (D == 256 && fwd_uses_pairs(D, hq / hkv))
+    return launch_fwd_impl<256, 1, true>(tq, tk, tk2, tv, to, p, num_sms, stream);
+  if (D == 256) return launch_fwd_impl<256, 1, false>(tq, tk, tk, tv, to, p, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 
