@@ -236,6 +236,8 @@ def bench_config(w, args, world):
     cfg["schedule"] = args.schedule
     fused = args.fwd == "fused" or args.schedule == "a2a"
     cfg["forward"] = "fused online softmax" if fused else "ring-step partials + LSE merge"
+    cfg["backward"] = ("dQ pass keeps dS, dK pass reads it back (D=256)" if getattr(args, "bwd", "") == "keep-ds"
+                       else "dK pass recomputes S^T and dP^T")
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU, CP emulated"
     return cfg
 
@@ -274,7 +276,8 @@ def measure(w, args, dev, pg, world, rank, clocks_uuid=None, head_parts=0):
     import torch
     from context_causal_gqa_gb300.pipeline import AttentionStep, profile_begin, profile_end
     x = W.make_inputs(w, device=dev, seed=w.seed + 1000 * rank)
-    step = AttentionStep(w, x, device=dev, schedule=args.schedule, fused=args.fwd == "fused", head_parts=head_parts)
+    step = AttentionStep(w, x, device=dev, schedule=args.schedule, fused=args.fwd == "fused", head_parts=head_parts,
+                         keep_ds=args.bwd == "keep-ds")
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         step.run()
@@ -475,6 +478,9 @@ def main():
                     help="ring: CP-emulated ring (the measured path); a2a: A2A head-split schedule")
     ap.add_argument("--fwd", default="partials", choices=["partials", "fused"],
                     help="partials: ring-step partials + LSE merge (the measured path); fused: one online softmax")
+    ap.add_argument("--bwd", default="keep-ds", choices=["keep-ds", "recompute"],
+                    help="keep-ds (the measured path): the D=256 backward keeps dS (the dQ pass writes it, the dK "
+                         "pass reads it back); recompute: the dK pass recomputes S^T and dP^T")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-d128", action="store_true", help="skip the D=128 companion measurement")

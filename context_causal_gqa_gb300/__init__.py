@@ -49,12 +49,15 @@ def _stream(stream=None):
 
 
 def make_desc(batch, hq, hkv, head_dim, cp, total_tokens, head_groups=1, scale=0.0, pitches=(0, 0, 0, 0),
-              head_parts=0):
+              head_parts=0, max_seqlen=0):
     """pitches: row pitch in elements of q, k, v, dO (0 = dense); head_parts:
-    P > 1 runs the ring forward and merge over P head parts in turn."""
+    P > 1 runs the ring forward and merge over P head parts in turn;
+    max_seqlen > 0 (a bound on every padded sequence length) selects the
+    D = 256 backward that keeps dS for the dK pass."""
     return AttnDesc(batch=batch, hq=hq, hkv=hkv, head_dim=head_dim, causal=1, cp=cp,
                     head_groups=head_groups, head_parts=head_parts, total_tokens=total_tokens, softmax_scale=scale,
-                    q_pitch=pitches[0], k_pitch=pitches[1], v_pitch=pitches[2], do_pitch=pitches[3])
+                    q_pitch=pitches[0], k_pitch=pitches[1], v_pitch=pitches[2], do_pitch=pitches[3],
+                    max_seqlen=max_seqlen)
 
 
 def workspace_size(desc, kind):
@@ -101,7 +104,7 @@ def _pitch(t, name):
     return 0 if t.stride(0) == H * D or T <= 1 else t.stride(0)
 
 
-def _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=None, do=None, head_parts=0):
+def _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=None, do=None, head_parts=0, max_seqlen=0):
     hg = head_groups
     if q.dim() == 4:        # head-split [G][T][H/G][D]
         for t, name in ((q, "q"), (k, "k"), (v, "v"), (do, "do")):
@@ -114,7 +117,7 @@ def _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=None, do=None, head_pa
         T, hq, D = q.shape
         hkv = k.shape[1]
         pitches = (_pitch(q, "q"), _pitch(k, "k"), _pitch(v, "v"), _pitch(do, "do"))
-    return make_desc(cu_seqlens.numel() - 1, hq, hkv, D, cp, T, hg, scale, pitches, head_parts)
+    return make_desc(cu_seqlens.numel() - 1, hq, hkv, D, cp, T, hg, scale, pitches, head_parts, max_seqlen)
 
 
 def attn_fwd(q, k, v, cu_seqlens, cu_seqlens_padded, cp, *, head_groups=1, scale=0.0, out=None, lse=None,
@@ -157,11 +160,12 @@ def attn_fwd_step(q, k, v, cu_seqlens, cu_seqlens_padded, cp, step, o_part, lse_
 
 
 def attn_bwd(q, k, v, o, do, lse, cu_seqlens, cu_seqlens_padded, cp, *, head_groups=1, scale=0.0,
-             dq=None, dk=None, dv=None, workspace=None, status=None, stream=None, check=True):
+             dq=None, dk=None, dv=None, workspace=None, status=None, stream=None, check=True, max_seqlen=0):
     """Backward: returns (dq, dk, dv).  q, k, v, do may be row-strided views; o and the
-    gradients are dense."""
+    gradients are dense.  max_seqlen > 0: a bound on every padded sequence length,
+    which at D = 256 selects the backward that keeps dS (a larger workspace)."""
     import torch
-    desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=v, do=do)
+    desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=v, do=do, max_seqlen=max_seqlen)
     dense = lambda t: torch.empty(t.shape, dtype=t.dtype, device=t.device)  # noqa: E731
     dq = dense(q) if dq is None else _dense(dq, "dq")
     dk = dense(k) if dk is None else _dense(dk, "dk")

@@ -12,7 +12,8 @@ class AttnDesc(ctypes.Structure):
     _fields_ = [("batch", c_i32), ("hq", c_i32), ("hkv", c_i32), ("head_dim", c_i32),
                 ("causal", c_i32), ("cp", c_i32), ("head_groups", c_i32), ("head_parts", c_i32),
                 ("total_tokens", c_i64), ("softmax_scale", c_f32),
-                ("q_pitch", c_i64), ("k_pitch", c_i64), ("v_pitch", c_i64), ("do_pitch", c_i64)]
+                ("q_pitch", c_i64), ("k_pitch", c_i64), ("v_pitch", c_i64), ("do_pitch", c_i64),
+                ("max_seqlen", c_i64)]
 
 
 # name -> (restype, argtypes)

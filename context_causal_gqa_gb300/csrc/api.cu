@@ -17,7 +17,7 @@ namespace ccg {
 cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp, int hkv, int bm,
                         int bn, int cap_q, int cap_kv, int want, int step_only, PlanHeader* hdr,
                         WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items,
-                        int32_t* status, cudaStream_t stream);
+                        int32_t* status, cudaStream_t stream, int64_t max_pad = 0, int64_t* ds_base = nullptr);
 cudaError_t launch_chunk_table(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp,
                                int32_t* table, int32_t* status, cudaStream_t stream);
 cudaError_t launch_bwd_dot(const void* o, const void* dout, int64_t rows, int D, int dout_heads,
@@ -38,7 +38,8 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items,
                             const int32_t* cu_pad, const float* lse, const float* delta, void* dq,
                             void* dk, void* dv, int32_t* status, int cp, int hq, int hkv,
                             int head_groups, int64_t T, int D, float scale, int grid_q,
-                            int grid_kv, int* launches, cudaStream_t stream);
+                            int grid_kv, int* launches, cudaStream_t stream, void* ds = nullptr,
+                            const int64_t* ds_base = nullptr, int64_t ds_cap = 0);
 int bwd_kv_tile_rows(int D);
 int bwd_q_tile_rows(int D);
 int bwd_map_rows(int which, int D);
@@ -102,7 +103,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 ccg_status check_desc(const ccg_attn_desc* d) {
   if (d == nullptr) return CCG_ERR_INVALID_ARG;
-  if (d->batch < 1 || d->hq < 1 || d->hkv < 1 || d->total_tokens < 0 || d->head_parts < 0)
+  if (d->batch < 1 || d->hq < 1 || d->hkv < 1 || d->total_tokens < 0 || d->head_parts < 0 || d->max_seqlen < 0)
     return CCG_ERR_INVALID_ARG;
   if (d->causal != 1) return CCG_ERR_UNSUPPORTED;
   if (d->head_dim != 128 && d->head_dim != 256) return CCG_ERR_UNSUPPORTED;
@@ -151,9 +152,25 @@ float softmax_scale(const ccg_attn_desc* d) {
 int head_parts_of(const ccg_attn_desc* d) { return d->head_parts > 1 ? d->head_parts : 1; }
 
 struct Layout {
-  size_t hdr, fwd_items, dq_items, kv_items, o_parts, lse_parts, delta, total;
+  size_t hdr, fwd_items, dq_items, kv_items, o_parts, lse_parts, delta, ds_base, ds, total;
   int cap_q, cap_kv;
+  int64_t ds_cap_tiles;     // dS tiles of one q head the dS region holds (0: no dS backward)
 };
+
+// The D = 256 backward that keeps dS (a padded-length bound in the
+// descriptor): one 128 x 128 BF16 dS tile per (query tile, visible KV tile)
+// of each q head of one GQA group.  Per sequence and head the tiles number
+// t^2 * 2CP(2CP+1)/2 (t = 128-row tiles of a chunk), and
+// sum_b t_b^2 <= t_max * sum_b t_b <= t_max * (T / (128 * 2CP) + B).
+bool bwd_keeps_ds(const ccg_attn_desc* d) { return d->head_dim == 256 && d->max_seqlen > 0; }
+int64_t ds_cap_tiles(const ccg_attn_desc* d) {
+  if (!bwd_keeps_ds(d)) return 0;
+  const int64_t C = 2 * d->cp;
+  const int64_t t_max = (d->max_seqlen / C + 127) / 128;
+  const int64_t sum_t = d->total_tokens / (128 * C) + d->batch;
+  return t_max * sum_t * (C * (C + 1) / 2);
+}
+constexpr int64_t kDsTileBytes = 128 * 128 * 2;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -175,6 +192,13 @@ Layout workspace_layout(const ccg_attn_desc* d, int kind) {
   off = align_up(off + (is_bwd ? size_t(L.cap_q) * sizeof(WorkItem) : 0), 256);
   L.kv_items = off;
   off = align_up(off + (is_bwd ? size_t(L.cap_kv) * d->hkv * sizeof(WorkItem) : 0), 256);
+  // dS backward: per-sequence first tile of the dS region, then the region
+  // (one GQA group's q heads)
+  L.ds_cap_tiles = is_bwd ? ds_cap_tiles(d) : 0;
+  L.ds_base = off;
+  off = align_up(off + (L.ds_cap_tiles > 0 ? size_t(d->batch + 1) * sizeof(int64_t) : 0), 256);
+  L.ds = off;
+  off = align_up(off + size_t(L.ds_cap_tiles) * (d->hq / d->hkv) * kDsTileBytes, 256);
   // the partial slabs hold one head part (all heads without partitioning)
   const size_t rows = size_t(d->total_tokens) * d->hq / head_parts_of(d);
   L.o_parts = off;
@@ -658,7 +682,8 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
   CCG_LAUNCH("plan", s,
              launch_plan(cu_seqlens, cu_seqlens_padded, desc->batch, desc->total_tokens, desc->cp, desc->hkv,
                          bwd_q_tile_rows(D), bwd_kv_tile_rows(D), L.cap_q, L.cap_kv * desc->hkv, 2, -1, hdr, nullptr, dq_items,
-                         kv_items, d_status, s));
+                         kv_items, d_status, s, desc->max_seqlen,
+                         L.ds_cap_tiles > 0 ? reinterpret_cast<int64_t*>(base + L.ds_base) : nullptr));
   CCG_LAUNCH("bwd_dot", s,
              launch_bwd_dot(o, dout, desc->total_tokens * desc->hq, D, desc->hq / desc->head_groups,
                             input_pitch(desc, 3), delta,
@@ -674,7 +699,8 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
   int kl = 0;
   if (launch_attn_bwd(maps, dq_items, kv_items, hdr, cu_seqlens, cu_seqlens_padded, lse, delta, dq, dk, dv,
                       d_status, desc->cp, desc->hq, desc->hkv, hg, desc->total_tokens, D,
-                      softmax_scale(desc), L.cap_q, L.cap_kv, &kl, s) != cudaSuccess)
+                      softmax_scale(desc), L.cap_q, L.cap_kv, &kl, s, L.ds_cap_tiles > 0 ? base + L.ds : nullptr,
+                      reinterpret_cast<const int64_t*>(base + L.ds_base), L.ds_cap_tiles) != cudaSuccess)
     return CCG_ERR_CUDA;
   launches += kl;
   g_last_launches = launches;

@@ -49,7 +49,27 @@ struct BwdParams {
   int cp, hq, hkv, hpg_q, hpg_kv;
   int64_t T;
   float scale, scale_log2;
+  // q heads of the dQ pass: head0 .. head0 + nheads - 1 (the grid is items x nheads)
+  int head0, nheads;
+  // dS backward (ds != null): the dQ pass also writes every unit's dS tile
+  // and the dK pass of kv head kv_head reads them.  Tile of (sequence b, q
+  // tile (cq, tq), KV tile j of the sequence, q head h of the kv head's
+  // group): ds + ((h % G) * ds_cap + ds_base[b] + t^2 cq(cq+1)/2 +
+  // tq (cq+1) t + j) * 128 * 128, t = 128-row tiles a chunk.  A tile holds,
+  // for each 8-column (16-byte) piece of the KV columns, the piece of all 128
+  // query rows: element (q row r, KV column c) at ((c / 8) * 128 + r) * 8 + c % 8.
+  __nv_bfloat16* ds;
+  const int64_t* ds_base;
+  int64_t ds_cap;
+  int kv_head;
 };
+
+__device__ __forceinline__ int64_t ds_tile_index(const BwdParams& p, int b, int L, int cq, int tq, int kv_tile,
+                                                 int head_in_group) {
+  const int64_t t = (L + 127) / 128;
+  return head_in_group * p.ds_cap + __ldg(p.ds_base + b) + t * t * cq * (cq + 1) / 2 +
+         static_cast<int64_t>(tq) * (cq + 1) * t + kv_tile;
+}
 
 // ---------------------------------------------------------------------------
 // tile configurations
@@ -970,7 +990,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, D = Cfg::D;
   using Iter = typename std::conditional<DQ, DqIter<BN>, KvIter<BN>>::type;
   // dQ role: one CTA per (item, q head); dK role: the items carry their kv head
-  const int item_idx = DQ ? blockIdx.x / p.hq : blockIdx.x;
+  const int item_idx = DQ ? blockIdx.x / p.nheads : blockIdx.x;
   if (item_idx >= (DQ ? p.hdr->n_dq : p.hdr->n_kv)) return;
   if (status_bad(p.status)) return;
 
@@ -989,7 +1009,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WorkItem it = p.items[item_idx];
-  const int head = DQ ? blockIdx.x % p.hq : it.step;   // q head (dQ role) or kv head (dK role)
+  const int head = DQ ? p.head0 + blockIdx.x % p.nheads : it.step;   // q head (dQ role) or kv head (dK role)
   const int G = p.hq / p.hkv;
   const int g = DQ ? head / G : head;          // kv head
   const SeqInfo si = seq_info(p, it.b);
@@ -1170,10 +1190,17 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     uint64_t col_l = 0, col_d = 0;
     for (int j = 0; !itr.done; ++j, itr.next()) {
       int c_lo = 0, c_hi = BN;                        // visible streamed columns of this row
+      uint4* ds_tile = nullptr;                      // dS backward: this unit's dS tile
       if constexpr (DQ) {
         const int k0 = itr.k0();
         const int kend = itr.diag ? min(itr.kv_hi, r_pos + 1) : itr.kv_hi;
         c_hi = r_valid ? kend - k0 : 0;
+        if (p.ds != nullptr) {
+          const int tpc = (si.L + 127) / 128;
+          const int kv_tile = (k0 / si.L) * tpc + (k0 % si.L) / 128;
+          ds_tile = reinterpret_cast<uint4*>(p.ds) +
+                    ds_tile_index(p, it.b, si.L, it.c, it.tile, kv_tile, head % G) * (128 * 128 / 8);
+        }
       } else {
         // -LSE (log2 units) and -Delta * scale of this contribution's query
         // columns: every lane holds two of its warpgroup's 64 columns (2*lane
@@ -1251,6 +1278,13 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           }
         }
         tmem_st16(t0 + Cfg::T_P + c_first * 32 + (c - c_first) * 16, pk);   // in place, own columns
+        if (DQ && ds_tile != nullptr) {
+          // 16-byte pieces 4c .. 4c+3 (8 columns each) of this row: a warp's
+          // store covers 32 consecutive rows of one piece (512 bytes)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            ds_tile[(4 * c + i) * 128 + row] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -1275,6 +1309,173 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                           const int pos = wrow0 + rr;
                           if (pos >= r_hi) return nullptr;
                           return reinterpret_cast<uint4*>(outp + thd_row(si.start + pos, rhead, rhpg, p.T) * D);
+                        });
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// D = 256 dK pass of the dS backward: dK = sum over the contributions of
+// dS^T Q, with the dS tiles the dQ pass wrote.  One CTA per 128-row KV tile of
+// kv head p.kv_head (the other heads' items leave at once); per contribution
+// (canonical order) a stage receives the dS tile (32 KB, one bulk copy) and
+// the contribution's Q tile (64 KB, four 64-column TMA boxes), and one M=128,
+// N=256, K=128 product accumulates dK in TMEM (the first one with
+// accumulation off).  dS^T is read from the unswizzled tile as an MN-major A
+// operand: its 8-column pieces hold the 128 query rows contiguously, so a core
+// matrix (8 query rows x 8 KV columns) is 128 contiguous bytes, core matrices
+// 128 bytes apart along K (query rows: the descriptor's leading offset) and
+// 2048 along M (KV columns: its stride offset).
+struct DkDsCfg {
+  static constexpr int THREADS = 384;           // 0 TMA, 1 MMA, 2 TMEM, 4..11 epilogue
+  static constexpr int D = 256;
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int DS_BYTES = 128 * 128 * 2;
+  static constexpr int Q_BYTES = BN * D * 2;
+  static constexpr int STAGE = DS_BYTES + Q_BYTES;
+  static constexpr int NST = 2;
+  static constexpr int SMEM_BAR = NST * STAGE;
+  static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
+  static constexpr int T_ACC = 0, TMEM_COLS = 256;
+  static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
+  static_assert(NST * STAGE >= 8 * 32 * 256, "epilogue staging fits the stages");
+};
+
+__global__ void __launch_bounds__(DkDsCfg::THREADS, 1)
+attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams p) {
+  using Cfg = DkDsCfg;
+  constexpr int BM = Cfg::BM, BN = Cfg::BN, D = Cfg::D, NST = Cfg::NST;
+  const int item_idx = blockIdx.x;
+  if (item_idx >= p.hdr->n_kv) return;
+  const WorkItem it = p.items[item_idx];
+  if (it.step != p.kv_head) return;                 // another kv head's tile
+  if (status_bad(p.status)) return;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::SMEM_BAR);
+  uint64_t* full = bars;                  // [NST]
+  uint64_t* empty = full + NST;           // [NST]
+  uint64_t* acc_done = empty + NST;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = it.step;
+  const int G = p.hq / p.hkv;
+  const SeqInfo si = seq_info(p, it.b);
+  const int r_lo = it.c * si.L + it.tile * BM;
+  const int r_hi = min(r_lo + BM, (it.c + 1) * si.L);
+  const int r_valid_hi = min(r_hi, si.S);
+  const int tpc = (si.L + 127) / 128;
+  const int kv_tile = it.c * tpc + it.tile;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(acc_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  KvIter<BN> itr0;
+  itr0.init(p.cp, it.c, si.L, si.S, r_lo, G, g);
+  const bool any = !itr0.done;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      KvIter<BN> itr = itr0;
+      int issued[NST] = {0, 0};
+      bool ok = true;
+      for (int j = 0; !itr.done && ok; ++j, itr.next()) {
+        const int st = j % NST;
+        if (j >= NST) ok = mbar_wait(empty + st, ((j / NST) - 1) & 1, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(full + st, Cfg::STAGE);
+        uint8_t* dst = smem + st * Cfg::STAGE;
+        const __nv_bfloat16* tile =
+            p.ds + ds_tile_index(p, it.b, si.L, itr.cq, itr.tq, kv_tile, itr.h) * (128 * 128);
+        bulk_load(dst, tile, Cfg::DS_BYTES, full + st);
+        const int hq = itr.head();
+        const int row = static_cast<int>((hq / p.hpg_q) * p.T) + si.start + itr.q0();
+        for (int kc = 0; kc < D / 64; ++kc)
+          tma_load_3d(dst + Cfg::DS_BYTES + kc * BN * 128, &tm_q, kc * 64, hq % p.hpg_q, row, full + st);
+        issued[st]++;
+      }
+      if (!ok) {
+        raise_status(p.status, CCG_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      volatile int never = 0;
+      for (int s = 0; s < NST; ++s)
+        if (issued[s] > 0) mbar_wait(full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      KvIter<BN> itr = itr0;
+      bool ok = true;
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, D, true, true);
+      for (int j = 0; !itr.done && ok; ++j, itr.next()) {
+        const int st = j % NST;
+        ok = mbar_wait(full + st, (j / NST) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t base = smem_u32(smem + st * Cfg::STAGE);
+        const uint64_t a_desc = smem_desc_noswz(base, 128, 2048);           // dS^T, MN-major
+        const uint64_t b_desc = smem_desc_sw128(base + Cfg::DS_BYTES, BN * 128, 1024);   // Q, MN-major
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          umma_ss(tmem + Cfg::T_ACC, a_desc + static_cast<uint64_t>(k * 16 * 16 >> 4), b_desc + mnmajor_step(k),
+                  idesc, (j > 0 || k > 0) ? 1u : 0u);
+        umma_commit(empty + st);
+      }
+      if (!ok) {
+        raise_status(p.status, CCG_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit(acc_done);
+      volatile int never = 0;
+      mbar_wait(acc_done, 0, &never, 200000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int wg = (warp - 4) >> 2;
+    const int row = ((warp & 3) << 5) + lane;
+    const uint32_t t0 = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const bool r_valid = r_lo + row < r_valid_hi;
+    bool ok = true;
+    if (any) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
+    if (!ok) {
+      raise_status(p.status, CCG_ERR_TIMEOUT);
+      *abort_flag = 1;
+    } else {
+      // each warpgroup writes 128 columns of the tile's rows (real rows the
+      // gradient, padding rows 0), staged in the idle stage area
+      tc_fence_after();
+      __nv_bfloat16* outp = p.out1 + wg * (D / 2);
+      uint4* stage = reinterpret_cast<uint4*>(smem) + (warp - 4) * 32 * 16;
+      const int wrow0 = r_lo + (warp & 3) * 32;
+      store_rows_staged(stage, t0 + Cfg::T_ACC + wg * (D / 2), any, !any || !r_valid, 1.f, lane,
+                        [&](int rr) -> uint4* {
+                          const int pos = wrow0 + rr;
+                          if (pos >= r_hi) return nullptr;
+                          return reinterpret_cast<uint4*>(outp + thd_row(si.start + pos, g, p.hpg_kv, p.T) * D);
                         });
     }
   }
@@ -1626,10 +1827,21 @@ cudaError_t launch_half(const CUtensorMap* m, const BwdParams& p, int grid_items
   cudaError_t e = once_per_device(
       attr_done, [&] { return set_smem(attn_bwd_half_kernel<ROLE, kHalfWarpgroups>, smem); });
   if (e != cudaSuccess) return e;
-  const int64_t grid = static_cast<int64_t>(grid_items) * (ROLE == HalfRole::kDq ? p.hq : p.hkv);
+  const int64_t grid = static_cast<int64_t>(grid_items) * (ROLE == HalfRole::kDq ? p.nheads : p.hkv);
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
   attn_bwd_half_kernel<ROLE, kHalfWarpgroups>
       <<<static_cast<unsigned>(grid), Cfg::THREADS, smem, s>>>(m[0], m[1], m[2], m[3], p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dk_ds(const CUtensorMap& tq, const BwdParams& p, int grid_items, cudaStream_t s) {
+  const int smem = DkDsCfg::SMEM_TOTAL + 1024;
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_dk_ds_kernel, smem); });
+  if (e != cudaSuccess) return e;
+  const int64_t grid = static_cast<int64_t>(grid_items) * p.hkv;
+  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+  attn_bwd_dk_ds_kernel<<<static_cast<unsigned>(grid), DkDsCfg::THREADS, smem, s>>>(tq, p);
   return cudaGetLastError();
 }
 
@@ -1663,7 +1875,7 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
                             const PlanHeader* hdr, const int32_t* cu, const int32_t* cu_pad, const float* lse,
                             const float* delta, void* dq, void* dk, void* dv, int32_t* status, int cp, int hq,
                             int hkv, int head_groups, int64_t T, int D, float scale, int grid_q, int grid_kv,
-                            int* launches, cudaStream_t stream) {
+                            int* launches, cudaStream_t stream, void* ds, const int64_t* ds_base, int64_t ds_cap) {
   BwdParams p;
   p.hdr = hdr;
   p.cu = cu;
@@ -1679,7 +1891,49 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
   p.T = T;
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
+  p.head0 = 0;
+  p.nheads = hq;
+  p.ds = nullptr;
+  p.ds_base = ds_base;
+  p.ds_cap = ds_cap;
+  p.kv_head = 0;
   cudaError_t e;
+  if (D == 256 && ds != nullptr) {
+    // dS backward: per kv head, the dQ pass over its q heads writes their dS
+    // tiles, then its dK pass reads them; then the dV pass over every head
+    const int G = hq / hkv;
+    for (int g = 0; g < hkv; ++g) {
+      p.items = dq_items;
+      p.out0 = static_cast<__nv_bfloat16*>(dq);
+      p.out1 = nullptr;
+      p.head0 = g * G;
+      p.nheads = G;
+      p.ds = static_cast<__nv_bfloat16*>(ds);
+      prof_begin("attn_bwd_dq", stream);
+      e = launch_half<HalfRole::kDq>(maps, p, grid_q, stream);
+      prof_end(stream);
+      if (e != cudaSuccess) return e;
+      ++*launches;
+      p.items = kv_items;
+      p.out0 = static_cast<__nv_bfloat16*>(dv);
+      p.out1 = static_cast<__nv_bfloat16*>(dk);
+      p.kv_head = g;
+      prof_begin("attn_bwd_dk", stream);
+      e = launch_dk_ds(maps[8], p, grid_kv, stream);
+      prof_end(stream);
+      if (e != cudaSuccess) return e;
+      ++*launches;
+    }
+    p.ds = nullptr;
+    p.head0 = 0;
+    p.nheads = hq;
+    prof_begin("attn_bwd_dv", stream);
+    e = launch_dv256(maps + 4, p, grid_kv, stream);
+    prof_end(stream);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    return cudaSuccess;
+  }
   // dQ pass
   p.items = dq_items;
   p.out0 = static_cast<__nv_bfloat16*>(dq);

@@ -65,7 +65,8 @@ __device__ int block_emit(int n, int base, CountF count, WriteF write) {
 __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, int B, int64_t T,
             int cp, int hkv, int bm, int bn, int cap_q, int cap_kv, int want, int step_only, PlanHeader* hdr,
-            WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items, int32_t* status) {
+            WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items, int64_t max_pad, int64_t* ds_base,
+            int32_t* status) {
   __shared__ int bad;
   const int C = 2 * cp;
   if (threadIdx.x == 0) {
@@ -77,6 +78,7 @@ plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, 
     const int S = __ldg(cu + b + 1) - __ldg(cu + b);
     const int P = __ldg(cu_pad + b + 1) - __ldg(cu_pad + b);
     if (S < 0 || P < S || P % C != 0) atomicExch(&bad, 1);
+    if (ds_base != nullptr && P > max_pad) atomicExch(&bad, 1);    // the padded-length bound of the dS backward
   }
   __syncthreads();
   if (bad) {
@@ -176,6 +178,18 @@ plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, 
     if (slot > cap_kv) overflow = 1;
     if (threadIdx.x == 0) hdr->n_kv = min(slot, cap_kv);
   }
+  // dS backward: each sequence's first tile in a q head's dS region (t^2 *
+  // 2CP(2CP+1)/2 tiles for t 128-row tiles a chunk; the host sized the region
+  // from the padded-length bound checked above)
+  if (ds_base != nullptr && threadIdx.x == 0) {
+    int64_t run = 0;
+    for (int b = 0; b < B; ++b) {
+      const int64_t t = (chunk_len(b) + 127) / 128;
+      ds_base[b] = run;
+      run += t * t * (C * (C + 1) / 2);
+    }
+    ds_base[B] = run;
+  }
   if (threadIdx.x == 0) {
     hdr->valid = 1;
     if (overflow) raise_status(status, CCG_ERR_SEQLENS);
@@ -223,9 +237,9 @@ cudaError_t launch_bounded_wait_selftest(int32_t* status, uint32_t limit_us, cud
 cudaError_t launch_plan(const int32_t* cu, const int32_t* cu_pad, int B, int64_t T, int cp, int hkv, int bm,
                         int bn, int cap_q, int cap_kv, int want, int step_only, PlanHeader* hdr,
                         WorkItem* fwd_items, WorkItem* dq_items, WorkItem* kv_items,
-                        int32_t* status, cudaStream_t stream) {
+                        int32_t* status, cudaStream_t stream, int64_t max_pad, int64_t* ds_base) {
   plan_kernel<<<1, kPlanThreads, 0, stream>>>(cu, cu_pad, B, T, cp, hkv, bm, bn, cap_q, cap_kv, want, step_only,
-                                               hdr, fwd_items, dq_items, kv_items, status);
+                                               hdr, fwd_items, dq_items, kv_items, max_pad, ds_base, status);
   return cudaGetLastError();
 }
 

@@ -84,6 +84,15 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Bulk copy of `bytes` contiguous bytes global -> this CTA's shared memory
+// (both 16-byte aligned, bytes a multiple of 16), completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes),
+                 "r"(smem_u32(bar))
+               : "memory");
+}
+
 // TMA tile store of one box from this CTA's shared memory (bulk async-group
 // completion): the source must have been written before a
 // fence.proxy.async by every writing thread and a barrier.
@@ -147,6 +156,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFF) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// The same descriptor for an unswizzled tile of 8 x 16-byte core matrices
+// (each 128 contiguous bytes): lbo / sbo are the byte distances between
+// neighbouring core matrices; for an MN-major operand (each core matrix 8
+// K rows of 8 contiguous MN elements) lbo is the distance along K and sbo
+// along MN (established by the dK pass of the dS backward against the oracle).
+__device__ __forceinline__ uint64_t smem_desc_noswz(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFF) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFF) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
   return d;
 }
 

@@ -70,14 +70,16 @@ class AttentionStep:
     no partials, no merge), unpack.  fused: forward with one online softmax
     over all ring steps (ccg_attn_fwd_fused) instead of partials + merge.
     head_parts: P > 1 runs the ring forward and merge over P head parts in
-    turn (a workspace sized for Hq/P heads).
+    turn (a workspace sized for Hq/P heads).  keep_ds: give the backward the
+    workload's longest padded sequence as its length bound, which at D = 256
+    selects the backward that keeps dS for the dK pass.
 
     The caller-facing buffers (inputs, o, lse, dq, dk, dv) form an IOSet; a
     second set is allocated on demand for the host pipeline, in which the
     copies of one step overlap the compute of its neighbours.
     """
 
-    def __init__(self, w, inputs, device="cuda", schedule="ring", fused=False, head_parts=0):
+    def __init__(self, w, inputs, device="cuda", schedule="ring", fused=False, head_parts=0, keep_ds=False):
         load()
         if schedule not in ("ring", "a2a"):
             raise ValueError(schedule)
@@ -87,6 +89,7 @@ class AttentionStep:
         self.schedule = schedule
         self.fused = fused or schedule == "a2a"
         self.head_parts = head_parts
+        self.max_seqlen = int(max(w.padded)) if keep_ds and w.padded else 0
         self.attn_cp = 1 if schedule == "a2a" else w.cp
         T, hq, hkv, D, cp = w.total_tokens, w.hq, w.hkv, w.head_dim, w.cp
         self.split = bool(w.pack_roundtrip) or schedule == "a2a"
@@ -144,7 +147,7 @@ class AttentionStep:
                  fused=self.fused, head_parts=self.head_parts, **kw)
         n += last_launch_count()
         attn_bwd(q, k, v, o, do, io.lse, cu, cpad, self.attn_cp, head_groups=hg, dq=dq, dk=dk, dv=dv,
-                 workspace=self.ws_b, **kw)
+                 workspace=self.ws_b, max_seqlen=self.max_seqlen, **kw)
         n += last_launch_count()
         if self.split:
             for src, dst in ((self.os, io.o), (self.dqs, io.dq), (self.dks, io.dk), (self.dvs, io.dv)):
