@@ -85,25 +85,58 @@ def merge_bytes(w):
 
 
 def kernel_work(w):
-    """name -> (bound, algorithmic amount per launch [FLOP or byte])."""
+    """name -> (bound, algorithmic amount [FLOP or byte], "step" or "launch"):
+    the amount of one whole step (split evenly over the kernel's launches in
+    the step: the dQ and dK passes of the backward that keeps dS run once
+    per kv head) or of one launch."""
     D, hq, hkv, T = w.head_dim, w.hq, w.hkv, w.total_tokens
     U = 2.0 * D * hq * causal_pairs(w)           # one D-wide GEMM over all causal pairs
     tq = T * hq * D * 2
     tkv = T * hkv * D * 2
     work = {
-        "attn_fwd": ("tensor", 2.0 * U),            # all ring-step partials (or fused), one launch
-        "pad_rows": ("hbm", 0.0),
-        "attn_bwd_dq": ("tensor", 3.0 * U),        # S, dP and dQ
-        "attn_bwd_dv": ("tensor", 1.0 * U),
-        "attn_bwd_dk": ("tensor", 1.0 * U),
-        "attn_bwd_dkdv": ("tensor", 2.0 * U),
-        "lse_merge": ("hbm", merge_bytes(w)),
-        "bwd_dot": ("hbm", 2.0 * tq + T * hq * 4),
-        "thd_pack": ("hbm", (2 * tq + 2 * tkv) / 2.0),      # mean over q, k, v, dO
-        "thd_unpack": ("hbm", (2 * tq + 2 * tkv) / 2.0),    # mean over o, dq, dk, dv
-        "plan": ("hbm", 0.0),
+        "attn_fwd": ("tensor", 2.0 * U, "step"),            # all ring-step partials (or fused)
+        "pad_rows": ("hbm", 0.0, "launch"),
+        "attn_bwd_dq": ("tensor", 3.0 * U, "step"),         # S, dP and dQ
+        "attn_bwd_dv": ("tensor", 1.0 * U, "step"),
+        "attn_bwd_dk": ("tensor", 1.0 * U, "step"),
+        "attn_bwd_dkdv": ("tensor", 2.0 * U, "step"),
+        "lse_merge": ("hbm", merge_bytes(w), "step"),
+        "bwd_dot": ("hbm", 2.0 * tq + T * hq * 4, "step"),
+        "thd_pack": ("hbm", (2 * tq + 2 * tkv) / 2.0, "launch"),      # mean over q, k, v, dO
+        "thd_unpack": ("hbm", (2 * tq + 2 * tkv) / 2.0, "launch"),    # mean over o, dq, dk, dv
+        "plan": ("hbm", 0.0, "launch"),
     }
     return work
+
+
+def attribute_kernels(prof, work, steps, pk):
+    """Per-kernel figures from (name, ms) launch records of `steps` steps:
+    launches a step, time a launch, share, and the achieved rate of the
+    kernel's algorithmic work a launch against the measured peak.  Returns
+    (kernels, {name: [launches, total ms]})."""
+    agg = {}
+    for name, t in prof:
+        a = agg.setdefault(name, [0, 0.0])
+        a[0] += 1
+        a[1] += t
+    tot = sum(a[1] for a in agg.values()) or 1.0
+    kernels = {}
+    for name, (n, t) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
+        bound, amount, per = work.get(name, ("hbm", 0.0, "launch"))
+        avg = t / n
+        if per == "step":
+            amount /= n / steps                             # the step's work over its launches
+        if bound == "tensor":
+            ach = amount / (avg / 1e3) / 1e12
+            peak = pk["bf16_sustained"]
+        else:
+            ach = amount / (avg / 1e3) / 1e9
+            peak = pk["hbm"]
+        kernels[name] = {"launches_per_step": n / steps, "ms_per_launch": round(avg, 4),
+                         "share": round(t / tot, 4), "bound": bound,
+                         "achieved": round(ach, 2), "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+                         "frac": round(ach / peak, 4) if peak else None}
+    return kernels, agg
 
 
 # ------------------------------------------------------------------ clocks
@@ -315,28 +348,8 @@ def measure(w, args, dev, pg, world, rank, clocks_uuid=None, head_parts=0):
     value = job_throughput(flops, world, ms_max)
 
     # per-kernel attribution inside the timed region
-    work = kernel_work(w)
-    agg = {}
-    for name, t in prof:
-        a = agg.setdefault(name, [0, 0.0])
-        a[0] += 1
-        a[1] += t
-    tot = sum(a[1] for a in agg.values()) or 1.0
     pk = peaks()
-    kernels = {}
-    for name, (n, t) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
-        bound, amount = work.get(name, ("hbm", 0.0))
-        avg = t / n
-        if bound == "tensor":
-            ach = amount / (avg / 1e3) / 1e12
-            peak = pk["bf16_sustained"]
-        else:
-            ach = amount / (avg / 1e3) / 1e9
-            peak = pk["hbm"]
-        kernels[name] = {"launches_per_step": n / args.steps, "ms_per_launch": round(avg, 4),
-                         "share": round(t / tot, 4), "bound": bound,
-                         "achieved": round(ach, 2), "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
-                         "frac": round(ach / peak, 4) if peak else None}
+    kernels, agg = attribute_kernels(prof, kernel_work(w), args.steps, pk)
     dom = max(agg.items(), key=lambda kv: kv[1][1])[0]
     dk = kernels[dom]
     traffic = None

@@ -62,3 +62,24 @@ def test_both_bench_arms_report_the_same_config():
         assert cfg["forward"] == ("fused online softmax" if (fwd == "fused" or schedule == "a2a")
                                   else "ring-step partials + LSE merge")
         assert cfg["parallelism"] == ("replicas x2" if world == 2 else "1 GPU, CP emulated")
+
+
+def test_kernel_attribution_splits_a_steps_work_over_its_launches():
+    """A kernel launched several times a step (the dQ and dK passes of the
+    backward that keeps dS: once per kv head) is credited the step's work
+    divided by its launches a step; a kernel whose work is given per launch
+    (the pack) keeps it."""
+    import bench
+    U = 3.0e12
+    work = {"attn_bwd_dq": ("tensor", 3.0 * U, "step"), "thd_pack": ("hbm", 8.0e9, "launch")}
+    pk = {"bf16_sustained": 1700.0, "hbm": 6800.0}
+    steps = 2
+    prof = [("attn_bwd_dq", 10.0)] * (8 * steps) + [("thd_pack", 2.0)] * (4 * steps)
+    kernels, agg = bench.attribute_kernels(prof, work, steps, pk)
+    dq = kernels["attn_bwd_dq"]
+    assert dq["launches_per_step"] == 8 and dq["ms_per_launch"] == 10.0
+    assert abs(dq["achieved"] - (3.0 * U / 8) / 10e-3 / 1e12) < 0.01
+    assert abs(dq["frac"] - dq["achieved"] / 1700.0) < 1e-4
+    pack = kernels["thd_pack"]
+    assert abs(pack["achieved"] - 8.0e9 / 2e-3 / 1e9) < 0.01
+    assert agg["attn_bwd_dq"] == [16, 160.0]
