@@ -198,7 +198,7 @@ Layout workspace_layout(const ccg_attn_desc* d, int kind) {
   L.ds_base = off;
   off = align_up(off + (L.ds_cap_tiles > 0 ? size_t(d->batch + 1) * sizeof(int64_t) : 0), 256);
   L.ds = off;
-  off = align_up(off + size_t(L.ds_cap_tiles) * (d->hq / d->hkv) * kDsTileBytes, 256);
+  off = align_up(off + 2 * size_t(L.ds_cap_tiles) * (d->hq / d->hkv) * kDsTileBytes, 256);   // dS, then P
   // the partial slabs hold one head part (all heads without partitioning)
   const size_t rows = size_t(d->total_tokens) * d->hq / head_parts_of(d);
   L.o_parts = off;

@@ -58,6 +58,8 @@ struct BwdParams {
   // tq (cq+1) t + j) * 128 * 128, t = 128-row tiles a chunk.  A tile holds,
   // for each 8-column (16-byte) piece of the KV columns, the piece of all 128
   // query rows: element (q row r, KV column c) at ((c / 8) * 128 + r) * 8 + c % 8.
+  // The unit's BF16 P tile follows in the same layout G * ds_cap tiles later,
+  // for the dV pass (dV += P^T dO).
   __nv_bfloat16* ds;
   const int64_t* ds_base;
   int64_t ds_cap;
@@ -1191,6 +1193,15 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     for (int j = 0; !itr.done; ++j, itr.next()) {
       int c_lo = 0, c_hi = BN;                        // visible streamed columns of this row
       uint4* ds_tile = nullptr;                      // dS backward: this unit's dS tile
+      uint32_t pk_last[16], pp_last[16];             // ... and its last chunk's dS and P
+      auto store_ds_p = [&](uint4* tile, int c, const uint32_t (&dsv)[16], const uint32_t (&pv)[16]) {
+        uint4* p_tile = tile + static_cast<int64_t>(G) * p.ds_cap * (128 * 128 / 8);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          tile[(4 * c + i) * 128 + row] = make_uint4(dsv[4 * i], dsv[4 * i + 1], dsv[4 * i + 2], dsv[4 * i + 3]);
+          p_tile[(4 * c + i) * 128 + row] = make_uint4(pv[4 * i], pv[4 * i + 1], pv[4 * i + 2], pv[4 * i + 3]);
+        }
+      };
       if constexpr (DQ) {
         const int k0 = itr.k0();
         const int kend = itr.diag ? min(itr.kv_hi, r_pos + 1) : itr.kv_hi;
@@ -1248,6 +1259,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         // dK role: the columns' -LSE2 and -Delta*scale, from the lanes that hold them
         uint32_t pk[16];
+        uint32_t pp[16];                             // dQ role, dS backward: BF16 P
 #pragma unroll
         for (int x2 = 0; x2 < 8; ++x2) {
           ulonglong2 lv, dv;
@@ -1275,15 +1287,22 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             float d0, d1;
             f32x2_split(mul_f32x2(pv, t), d0, d1);
             pk[x] = pack_bf16x2(d0, d1);
+            if constexpr (DQ) {
+              float q0, q1;
+              f32x2_split(pv, q0, q1);
+              pp[x] = pack_bf16x2(q0, q1);
+            }
           }
         }
         tmem_st16(t0 + Cfg::T_P + c_first * 32 + (c - c_first) * 16, pk);   // in place, own columns
-        if (DQ && ds_tile != nullptr) {
-          // 16-byte pieces 4c .. 4c+3 (8 columns each) of this row: a warp's
-          // store covers 32 consecutive rows of one piece (512 bytes)
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            ds_tile[(4 * c + i) * 128 + row] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        if constexpr (DQ) {
+          // 16-byte pieces 4c .. 4c+3 (8 columns each) of this row, of dS and
+          // of P: a warp's store covers 32 consecutive rows of one piece (512
+          // bytes).  The last chunk's go out after the hand-over below, while
+          // the gradient product runs.
+          if (ds_tile != nullptr) {
+            store_ds_p(ds_tile, c, pk, pp);
+          }
         }
       }
       tmem_wait_st();
@@ -1345,6 +1364,9 @@ struct DkDsCfg {
   static_assert(NST * STAGE >= 8 * 32 * 256, "epilogue staging fits the stages");
 };
 
+// DV: the dV pass the same way, from the stored P tiles and the
+// contributions' dO tiles (dV += P^T dO); tm_b is then the dO map.
+template <bool DV>
 __global__ void __launch_bounds__(DkDsCfg::THREADS, 1)
 attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams p) {
   using Cfg = DkDsCfg;
@@ -1409,7 +1431,8 @@ attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams 
         mbar_arrive_expect_tx(full + st, Cfg::STAGE);
         uint8_t* dst = smem + st * Cfg::STAGE;
         const __nv_bfloat16* tile =
-            p.ds + ds_tile_index(p, it.b, si.L, itr.cq, itr.tq, kv_tile, itr.h) * (128 * 128);
+            p.ds + (ds_tile_index(p, it.b, si.L, itr.cq, itr.tq, kv_tile, itr.h) + (DV ? G * p.ds_cap : 0)) *
+                       (128 * 128);
         bulk_load(dst, tile, Cfg::DS_BYTES, full + st);
         const int hq = itr.head();
         const int row = static_cast<int>((hq / p.hpg_q) * p.T) + si.start + itr.q0();
@@ -1468,7 +1491,7 @@ attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams 
       // each warpgroup writes 128 columns of the tile's rows (real rows the
       // gradient, padding rows 0), staged in the idle stage area
       tc_fence_after();
-      __nv_bfloat16* outp = p.out1 + wg * (D / 2);
+      __nv_bfloat16* outp = (DV ? p.out0 : p.out1) + wg * (D / 2);
       uint4* stage = reinterpret_cast<uint4*>(smem) + (warp - 4) * 32 * 16;
       const int wrow0 = r_lo + (warp & 3) * 32;
       store_rows_staged(stage, t0 + Cfg::T_ACC + wg * (D / 2), any, !any || !r_valid, 1.f, lane,
@@ -1834,14 +1857,15 @@ cudaError_t launch_half(const CUtensorMap* m, const BwdParams& p, int grid_items
   return cudaGetLastError();
 }
 
-cudaError_t launch_dk_ds(const CUtensorMap& tq, const BwdParams& p, int grid_items, cudaStream_t s) {
+template <bool DV>
+cudaError_t launch_dk_ds(const CUtensorMap& tb, const BwdParams& p, int grid_items, cudaStream_t s) {
   const int smem = DkDsCfg::SMEM_TOTAL + 1024;
   static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_dk_ds_kernel, smem); });
+  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_dk_ds_kernel<DV>, smem); });
   if (e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(grid_items) * p.hkv;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  attn_bwd_dk_ds_kernel<<<static_cast<unsigned>(grid), DkDsCfg::THREADS, smem, s>>>(tq, p);
+  attn_bwd_dk_ds_kernel<DV><<<static_cast<unsigned>(grid), DkDsCfg::THREADS, smem, s>>>(tb, p);
   return cudaGetLastError();
 }
 
@@ -1900,7 +1924,7 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
   cudaError_t e;
   if (D == 256 && ds != nullptr) {
     // dS backward: per kv head, the dQ pass over its q heads writes their dS
-    // tiles, then its dK pass reads them; then the dV pass over every head
+    // and P tiles, then its dK pass and its dV pass read them
     const int G = hq / hkv;
     for (int g = 0; g < hkv; ++g) {
       p.items = dq_items;
@@ -1919,19 +1943,16 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
       p.out1 = static_cast<__nv_bfloat16*>(dk);
       p.kv_head = g;
       prof_begin("attn_bwd_dk", stream);
-      e = launch_dk_ds(maps[8], p, grid_kv, stream);
+      e = launch_dk_ds<false>(maps[8], p, grid_kv, stream);
+      prof_end(stream);
+      if (e != cudaSuccess) return e;
+      ++*launches;
+      prof_begin("attn_bwd_dv", stream);
+      e = launch_dk_ds<true>(maps[11], p, grid_kv, stream);
       prof_end(stream);
       if (e != cudaSuccess) return e;
       ++*launches;
     }
-    p.ds = nullptr;
-    p.head0 = 0;
-    p.nheads = hq;
-    prof_begin("attn_bwd_dv", stream);
-    e = launch_dv256(maps + 4, p, grid_kv, stream);
-    prof_end(stream);
-    if (e != cudaSuccess) return e;
-    ++*launches;
     return cudaSuccess;
   }
   // dQ pass

@@ -120,9 +120,9 @@ def test_head_parts_shrink_the_forward_workspace_and_are_validated(L):
 
 def test_padded_length_bound_sizes_the_ds_backward_workspace(L):
     """max_seqlen > 0 at D = 256: the backward workspace adds one GQA group's
-    dS tiles (t_max * (T / (128 * 2CP) + B) * CP(2CP+1) tiles of 32 KiB per q
-    head, t_max = 128-row tiles of the longest chunk); at D = 128, or with no
-    bound, it does not change; a negative bound is invalid."""
+    dS and P tiles (t_max * (T / (128 * 2CP) + B) * CP(2CP+1) tiles of 32 KiB
+    each per q head, t_max = 128-row tiles of the longest chunk); at D = 128,
+    or with no bound, it does not change; a negative bound is invalid."""
     import context_causal_gqa_gb300 as ccg
     B, T, hq, hkv, cp = 4, 4 * 8192, 32, 8, 8
     C = 2 * cp
@@ -130,7 +130,7 @@ def test_padded_length_bound_sizes_the_ds_backward_workspace(L):
     ds = ccg.workspace_size(ccg.make_desc(B, hq, hkv, 256, cp, T, max_seqlen=8192), 1)
     t_max = -(-8192 // C // 128)
     tiles = t_max * (T // (128 * C) + B) * (C * (C + 1) // 2)
-    extra = tiles * (hq // hkv) * 128 * 128 * 2 + (B + 1) * 8
+    extra = 2 * tiles * (hq // hkv) * 128 * 128 * 2 + (B + 1) * 8       # dS and P tiles
     assert 0 <= (ds - base) - extra <= 3 * 256
     assert ccg.workspace_size(ccg.make_desc(B, hq, hkv, 128, cp, T, max_seqlen=8192), 1) == \
         ccg.workspace_size(ccg.make_desc(B, hq, hkv, 128, cp, T), 1)

@@ -1,8 +1,8 @@
-"""The D = 256 backward that keeps dS (a padded-length bound in the
-descriptor): the dQ pass writes every unit's dS tile, the dK pass reads them
-back.  Checked against the FP64 oracle, against the backward that recomputes
-S^T and dP^T, for bitwise repeatability under NaN-poisoned outputs, and for
-the device check of the bound.
+"""The D = 256 backward that keeps dS and P (a padded-length bound in the
+descriptor): the dQ pass writes every unit's dS and P tiles, the dK and dV
+passes read them back.  Checked against the FP64 oracle, against the
+backward that recomputes them, for bitwise repeatability under NaN-poisoned
+outputs, and for the device check of the bound.
 """
 
 import numpy as np
@@ -56,18 +56,18 @@ def test_ds_backward_matches_oracle(lib, w):
 
 @pytest.mark.parametrize("w", SHAPES[:3], ids=lambda w: w.name)
 def test_ds_backward_agrees_with_the_recomputing_backward(lib, w):
-    """Same dS values (the same arithmetic on the same S and dP, up to the
-    tensor core's summation order in S versus S^T): dQ and dV are those of
-    the recomputing backward bit for bit (the same kernels), dK agrees to
+    """Same dS and P values (the same arithmetic on the same S and dP, up to
+    the tensor core's summation order in S versus S^T): dQ is that of the
+    recomputing backward bit for bit (the same kernel), dK and dV agree to
     BF16 rounding."""
     x = W.make_inputs(w, device="cuda")
     o, lse = _fwd(lib, x, w)
     g0 = _bwd(lib, x, w, o, lse, 0)
     g1 = _bwd(lib, x, w, o, lse, _bound(w))
     assert torch.equal(g0[0], g1[0])
-    assert torch.equal(g0[2], g1[2])
-    a, b = f64(g1[1]), f64(g0[1])
-    assert np.linalg.norm(a - b) <= 1e-2 * np.linalg.norm(b) + 1e-6
+    for i in (1, 2):
+        a, b = f64(g1[i]), f64(g0[i])
+        assert np.linalg.norm(a - b) <= 1e-2 * np.linalg.norm(b) + 1e-6
 
 
 def test_ds_backward_bitwise_repeatable_under_poison(lib):
