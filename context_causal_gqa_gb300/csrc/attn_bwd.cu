@@ -153,10 +153,7 @@ struct DqIter {
   bool diag, done;
 
   __device__ void load_vis() {
-    int v[2];
-    nv = visible_kv_chunks(cq, ring_source(r, s, cp), cp, v);
-    vis0 = v[0];
-    vis1 = v[1];
+    nv = visible_kv_chunks2(cq, ring_source(r, s, cp), cp, vis0, vis1);
   }
   __device__ void load_segment() {
     const int j = vi == 0 ? vis0 : vis1;
@@ -431,8 +428,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (lane == 0) {
       DqIter<BN> itr;
       itr.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
-      int issued[NSLOT];
-      for (int s = 0; s < NSLOT; ++s) issued[s] = 0;
+      int64_t n_loads = 0;                       // copies issued (slot = position % NSLOT)
       bool ok = true;
       if (!itr.done) {
         const int row = static_cast<int>((h / p.hpg_q) * p.T) + si.start + q_lo;
@@ -454,7 +450,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           for (int kc = 0; kc < KCH; ++kc)
             tma_load_3d(dst + kc * BN * 128, is_v ? &tm_v : &tm_k, kc * 64, g % p.hpg_kv, kv_group_row + k0,
                         full + slot);
-          issued[slot]++;
+          ++n_loads;
           if (!is_v) itr.next();
         }
         if (!ok) {
@@ -463,8 +459,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         volatile int never = 0;
         mbar_wait(res_full, 0, &never, 200000000ull);
-        for (int s = 0; s < NSLOT; ++s)
-          if (issued[s] > 0) mbar_wait(full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+        wait_last_copies(full, NSLOT, n_loads);
       }
     }
   } else if (warp == 1) {
@@ -689,8 +684,7 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (lane == 0) {
       KvIter<BN> itr;
       itr.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
-      int issued[NSLOT];
-      for (int s = 0; s < NSLOT; ++s) issued[s] = 0;
+      int64_t n_loads = 0;                       // copies issued (slot = position % NSLOT)
       bool ok = true;
       if (!itr.done) {
         const int krow = static_cast<int>((g / p.hpg_kv) * p.T) + si.start + k_lo;
@@ -712,7 +706,7 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           uint8_t* dst = smem + Cfg::SMEM_SLOT + slot * Cfg::SLOT_BYTES;
           for (int kc = 0; kc < KCH; ++kc)
             tma_load_3d(dst + kc * BN * 128, is_q ? &tm_q : &tm_do, kc * 64, hq % p.hpg_q, qrow, full + slot);
-          issued[slot]++;
+          ++n_loads;
           if (!first) itr.next();
         }
         if (!ok) {
@@ -721,8 +715,7 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         volatile int never = 0;
         mbar_wait(res_full, 0, &never, 200000000ull);
-        for (int s = 0; s < NSLOT; ++s)
-          if (issued[s] > 0) mbar_wait(full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+        wait_last_copies(full, NSLOT, n_loads);
       }
     }
   } else if (warp == 1) {
@@ -1051,8 +1044,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if (lane == 0) {
       Iter itr;
       iter_init(itr);
-      int issued[NSLOT];
-      for (int s = 0; s < NSLOT; ++s) issued[s] = 0;
+      int64_t n_loads = 0;                       // copies issued (slot = position % NSLOT)
       bool ok = true;
       if (!itr.done) {
         // resident tiles: Q and dO of (tile, q head), or K and V of (tile, kv head)
@@ -1088,7 +1080,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           uint8_t* dst = smem + Cfg::SMEM_SLOT + slot * Cfg::HALF_BYTES;
           for (int kc = 0; kc < 2; ++kc)
             tma_load_3d(dst + kc * BN * 128, map, (2 * half + kc) * 64, hc, row, full + slot);
-          issued[slot]++;
+          ++n_loads;
           if (part == 3) itr.next();
         }
         if (!ok) {
@@ -1097,8 +1089,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         volatile int never = 0;
         mbar_wait(res_full, 0, &never, 200000000ull);
-        for (int s = 0; s < NSLOT; ++s)
-          if (issued[s] > 0) mbar_wait(full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+        wait_last_copies(full, NSLOT, n_loads);
       }
     }
   } else if (warp == 1) {
@@ -1193,7 +1184,6 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     for (int j = 0; !itr.done; ++j, itr.next()) {
       int c_lo = 0, c_hi = BN;                        // visible streamed columns of this row
       uint4* ds_tile = nullptr;                      // dS backward: this unit's dS tile
-      uint32_t pk_last[16], pp_last[16];             // ... and its last chunk's dS and P
       auto store_ds_p = [&](uint4* tile, int c, const uint32_t (&dsv)[16], const uint32_t (&pv)[16]) {
         uint4* p_tile = tile + static_cast<int64_t>(G) * p.ds_cap * (128 * 128 / 8);
 #pragma unroll
@@ -1422,7 +1412,7 @@ attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams 
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       KvIter<BN> itr = itr0;
-      int issued[NST] = {0, 0};
+      int64_t n_loads = 0;
       bool ok = true;
       for (int j = 0; !itr.done && ok; ++j, itr.next()) {
         const int st = j % NST;
@@ -1438,15 +1428,13 @@ attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams 
         const int row = static_cast<int>((hq / p.hpg_q) * p.T) + si.start + itr.q0();
         for (int kc = 0; kc < D / 64; ++kc)
           tma_load_3d(dst + Cfg::DS_BYTES + kc * BN * 128, &tm_q, kc * 64, hq % p.hpg_q, row, full + st);
-        issued[st]++;
+        ++n_loads;
       }
       if (!ok) {
         raise_status(p.status, CCG_ERR_TIMEOUT);
         *abort_flag = 1;
       }
-      volatile int never = 0;
-      for (int s = 0; s < NST; ++s)
-        if (issued[s] > 0) mbar_wait(full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+      wait_last_copies(full, NST, n_loads);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -1607,8 +1595,7 @@ attn_bwd_dv256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       KvIter<BN> qi, di;                         // Q runs one contribution ahead of dO
       qi.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
       di.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
-      int issued[NSLOT];
-      for (int s = 0; s < NSLOT; ++s) issued[s] = 0;
+      int64_t n_loads = 0;                       // copies issued (slot = position % NSLOT)
       bool ok = true;
       int t = 0;                                 // stream position
       auto load = [&](const KvIter<BN>& itr, const CUtensorMap* map) -> bool {
@@ -1621,7 +1608,7 @@ attn_bwd_dv256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           uint8_t* dst = smem + Cfg::SMEM_SLOT + slot * Cfg::HALF_BYTES;
           for (int kc = 0; kc < 2; ++kc)
             tma_load_3d(dst + kc * BN * 128, map, (2 * hf + kc) * 64, hq % p.hpg_q, row, full + slot);
-          issued[slot]++;
+          ++n_loads;
         }
         return true;
       };
@@ -1646,8 +1633,7 @@ attn_bwd_dv256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         }
         volatile int never = 0;
         mbar_wait(res_full, 0, &never, 200000000ull);
-        for (int s = 0; s < NSLOT; ++s)
-          if (issued[s] > 0) mbar_wait(full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+        wait_last_copies(full, NSLOT, n_loads);
       }
     }
   } else if (warp == 1) {

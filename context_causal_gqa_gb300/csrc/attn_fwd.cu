@@ -140,10 +140,7 @@ struct KvTileIter {
   bool diag, done;
 
   __device__ void load_vis() {
-    int v[2];
-    nv = visible_kv_chunks(cq, ring_source(r, s, cp), cp, v);
-    vis0 = v[0];
-    vis1 = v[1];
+    nv = visible_kv_chunks2(cq, ring_source(r, s, cp), cp, vis0, vis1);
   }
   __device__ void load_segment() {
     const int j = vi == 0 ? vis0 : vis1;
@@ -307,8 +304,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(PAIR ? &tm_k2 : &tm_k);
       tma_prefetch_desc(&tm_v);
-      int issued[NSLOT];
-      for (int s = 0; s < NSLOT; ++s) issued[s] = 0;
+      int64_t n_loads = 0;                       // copies issued (slot = position % NSLOT)
       int q_loads = 0;
       bool ok = true;
       int64_t u = 0;                                   // K/V tile positions streamed by this CTA
@@ -362,7 +358,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               tma_load_3d(dst + kc * BN * 128, which == 0 ? &tm_k : &tm_v, kc * 64, g % p.hpg_kv,
                           kv_group_row + k0, kv_full + sl);
           }
-          issued[sl]++;
+          ++n_loads;
           ++u;
           return true;
         };
@@ -389,8 +385,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       volatile int never = 0;
       if (arm) {
         if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, &never, 200000000ull);
-        for (int s = 0; s < NSLOT; ++s)
-          if (issued[s] > 0) mbar_wait(kv_full + s, (issued[s] - 1) & 1, &never, 200000000ull);
+        wait_last_copies(kv_full, NSLOT, n_loads);
       }
     }
   } else if (warp == 1) {

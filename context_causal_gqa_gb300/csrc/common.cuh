@@ -81,6 +81,15 @@ __host__ __device__ __forceinline__ int visible_kv_chunks(int cq, int src, int c
   return n;
 }
 
+// The same into two scalars (v1 only meaningful when two are visible): the
+// kernels' tile iterators keep no indexed arrays.
+__host__ __device__ __forceinline__ int visible_kv_chunks2(int cq, int src, int cp, int& v0, int& v1) {
+  const int a = src, b = 2 * cp - 1 - src;
+  v0 = a <= cq ? a : b;
+  v1 = b;
+  return (a <= cq ? 1 : 0) + (b <= cq ? 1 : 0);
+}
+
 // Row offset in a head-grouped THD tensor: element (t, h, d) lives at
 // ((h / hpg) * T + t) * hpg * D + (h % hpg) * D + d.
 __host__ __device__ __forceinline__ int64_t thd_row(int64_t t, int h, int hpg, int64_t T) {

@@ -68,6 +68,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Bounded, silent wait until the last of the n copies a producer issued
+// round-robin into nslot slots (copy t into slot t % nslot, each completing
+// one phase of full[slot]) have landed, so that a CTA never leaves with a
+// copy in flight into its shared memory.  The per-slot counts follow from n
+// alone, so the producer keeps no per-slot state.
+__device__ __forceinline__ void wait_last_copies(uint64_t* full, int nslot, int64_t n) {
+  volatile int never = 0;
+  for (int s = 0; s < nslot && s < n; ++s) {
+    const int64_t copies = (n - 1 - s) / nslot + 1;
+    mbar_wait(full + s, static_cast<uint32_t>((copies - 1) & 1), &never, 200000000ull);
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
