@@ -39,7 +39,8 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items,
                             void* dk, void* dv, int32_t* status, int cp, int hq, int hkv,
                             int head_groups, int64_t T, int D, float scale, int grid_q,
                             int grid_kv, int* launches, cudaStream_t stream, void* ds = nullptr,
-                            const int64_t* ds_base = nullptr, int64_t ds_cap = 0);
+                            const int64_t* ds_base = nullptr, int64_t ds_cap = 0,
+                            const CUtensorMap* ds_map = nullptr, int kv_pairs = 0);
 int bwd_kv_tile_rows(int D);
 int bwd_q_tile_rows(int D);
 int bwd_map_rows(int which, int D);
@@ -100,6 +101,7 @@ int num_sms_cached() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t ds_cap_tiles(const ccg_attn_desc* d);
 
 ccg_status check_desc(const ccg_attn_desc* d) {
   if (d == nullptr) return CCG_ERR_INVALID_ARG;
@@ -134,6 +136,8 @@ ccg_status check_desc(const ccg_attn_desc* d) {
     if (d->head_groups != 1) return CCG_ERR_UNSUPPORTED;
     if (pitches[i] >= (int64_t(1) << 36)) return CCG_ERR_UNSUPPORTED;
   }
+  // the dS backward addresses its dS and P tiles with 32-bit TMA coordinates
+  if (2 * ds_cap_tiles(d) * (d->hq / d->hkv) >= (int64_t(1) << 31)) return CCG_ERR_UNSUPPORTED;
   return CCG_OK;
 }
 
@@ -264,6 +268,21 @@ bool make_out_map(CUtensorMap* m, void* base, int D, int hpg, int64_t rows, int 
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over the dS and P tiles of the dS backward: dims (128 columns,
+// 128 rows, ntiles), unswizzled boxes of one whole 32 KB tile (its bytes in
+// order).  A load at tile -1 lies wholly outside and reads zeros.
+bool make_tile_map(CUtensorMap* m, void* base, int64_t ntiles) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {128, 128, static_cast<cuuint64_t>(ntiles)};
+  cuuint64_t strides[2] = {128 * 2, 128 * 128 * 2};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -696,11 +715,20 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
   for (int i = 0; i < 12; ++i)
     if (!make_thd_map(&maps[i], bases[i % 4], D, hpgs[i % 4], rows, bwd_map_rows(i, D), input_pitch(desc, i % 4)))
       return CCG_ERR_CUDA;
+  // dS backward: the tile map of its dS and P tiles, and a bound on the KV
+  // tile pairs of one kv head (sum over sequences and chunks of ceil(t / 2))
+  CUtensorMap ds_map;
+  int kv_pairs = 0;
+  if (L.ds_cap_tiles > 0) {
+    if (!make_tile_map(&ds_map, base + L.ds, 2 * L.ds_cap_tiles * (desc->hq / desc->hkv))) return CCG_ERR_CUDA;
+    kv_pairs = static_cast<int>(desc->total_tokens / 256 + int64_t(desc->batch) * 2 * desc->cp + 1);
+  }
   int kl = 0;
   if (launch_attn_bwd(maps, dq_items, kv_items, hdr, cu_seqlens, cu_seqlens_padded, lse, delta, dq, dk, dv,
                       d_status, desc->cp, desc->hq, desc->hkv, hg, desc->total_tokens, D,
                       softmax_scale(desc), L.cap_q, L.cap_kv, &kl, s, L.ds_cap_tiles > 0 ? base + L.ds : nullptr,
-                      reinterpret_cast<const int64_t*>(base + L.ds_base), L.ds_cap_tiles) != cudaSuccess)
+                      reinterpret_cast<const int64_t*>(base + L.ds_base), L.ds_cap_tiles,
+                      L.ds_cap_tiles > 0 ? &ds_map : nullptr, kv_pairs) != cudaSuccess)
     return CCG_ERR_CUDA;
   launches += kl;
   g_last_launches = launches;

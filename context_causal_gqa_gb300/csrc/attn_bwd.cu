@@ -1329,24 +1329,36 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
 // ---------------------------------------------------------------------------
 // D = 256 dK pass of the dS backward: dK = sum over the contributions of
-// dS^T Q, with the dS tiles the dQ pass wrote.  One CTA per 128-row KV tile of
-// kv head p.kv_head (the other heads' items leave at once); per contribution
-// (canonical order) a stage receives the dS tile (32 KB, one bulk copy) and
-// the contribution's Q tile (64 KB, four 64-column TMA boxes), and one M=128,
-// N=256, K=128 product accumulates dK in TMEM (the first one with
-// accumulation off).  dS^T is read from the unswizzled tile as an MN-major A
-// operand: its 8-column pieces hold the 128 query rows contiguously, so a core
-// matrix (8 query rows x 8 KV columns) is 128 contiguous bytes, core matrices
-// 128 bytes apart along K (query rows: the descriptor's leading offset) and
-// 2048 along M (KV columns: its stride offset).
-struct DkDsCfg {
-  static constexpr int THREADS = 384;           // 0 TMA, 1 MMA, 2 TMEM, 4..11 epilogue
+// dS^T Q, with the dS tiles the dQ pass wrote (the dV pass: dV = sum of
+// P^T dO, with the P tiles).  Per contribution (canonical order) a stage
+// receives the KV tile's dS tile and the contribution's Q tile, and one
+// product accumulates dK in TMEM (the first one with accumulation off).
+// dS^T is read from the unswizzled tile as an MN-major A operand: its
+// 8-column pieces hold the 128 query rows contiguously, so a core matrix (8
+// query rows x 8 KV columns) is 128 contiguous bytes, core matrices 128
+// bytes apart along K (query rows: the descriptor's leading offset) and 2048
+// along M (KV columns: its stride offset).
+//
+// CTA pairs: a (2,1,1) cluster takes KV tiles 2i and 2i+1 of a chunk and
+// computes both with one M = 256, N = 256, K = 128 tcgen05 product per
+// contribution, issued by rank 0.  Each CTA loads its
+// own tile's dS^T (P^T) rows (A, 32 KB) and half of the contribution's Q
+// (dO) tile, its 128 of the 256 columns (B, 32 KB): 64 KB a CTA a
+// contribution instead of 96 KB.  Both CTAs follow tile 2i's contributions;
+// tile 2i+1 sees all of them but the diagonal query tile 2i (a tile-level
+// causal rule), where its CTA loads a zero tile instead (a load past the
+// tile map's start, which TMA fills with zeros), so that it adds exactly 0
+// in the canonical order.  Without a tile 2i+1 (odd tiles in the chunk)
+// rank 1 computes zeros and writes nothing.  The items are pairs, kv head
+// p.kv_head's at [kv_head * n, (kv_head + 1) * n), n = n_kv / hkv.
+struct DkvPairCfg {
+  static constexpr int THREADS = 384;           // 0 TMA, 1 MMA (rank 0), 2 TMEM, 4..11 epilogue
   static constexpr int D = 256;
   static constexpr int BM = 128, BN = 128;
-  static constexpr int DS_BYTES = 128 * 128 * 2;
-  static constexpr int Q_BYTES = BN * D * 2;
-  static constexpr int STAGE = DS_BYTES + Q_BYTES;
-  static constexpr int NST = 2;
+  static constexpr int A_BYTES = 128 * 128 * 2;
+  static constexpr int B_BYTES = BN * (D / 2) * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int NST = 3;
   static constexpr int SMEM_BAR = NST * STAGE;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
   static constexpr int T_ACC = 0, TMEM_COLS = 256;
@@ -1354,26 +1366,26 @@ struct DkDsCfg {
   static_assert(NST * STAGE >= 8 * 32 * 256, "epilogue staging fits the stages");
 };
 
-// DV: the dV pass the same way, from the stored P tiles and the
-// contributions' dO tiles (dV += P^T dO); tm_b is then the dO map.
 template <bool DV>
-__global__ void __launch_bounds__(DkDsCfg::THREADS, 1)
-attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams p) {
-  using Cfg = DkDsCfg;
+__global__ void __launch_bounds__(DkvPairCfg::THREADS, 1)
+attn_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_t,
+                         const BwdParams p) {
+  using Cfg = DkvPairCfg;
   constexpr int BM = Cfg::BM, BN = Cfg::BN, D = Cfg::D, NST = Cfg::NST;
-  const int item_idx = blockIdx.x;
-  if (item_idx >= p.hdr->n_kv) return;
-  const WorkItem it = p.items[item_idx];
-  if (it.step != p.kv_head) return;                 // another kv head's tile
-  if (status_bad(p.status)) return;
+  const int n_head = p.hdr->n_kv / p.hkv;
+  const int pair = blockIdx.x >> 1;
+  if (pair >= n_head) return;                       // both CTAs of the cluster, or neither
+  // (a pair never returns on the status word: its two reads could differ)
+  const uint32_t rank = cluster_ctarank();
+  const WorkItem it = p.items[static_cast<int64_t>(p.kv_head) * n_head + pair];
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::SMEM_BAR);
-  uint64_t* full = bars;                  // [NST]
-  uint64_t* empty = full + NST;           // [NST]
-  uint64_t* acc_done = empty + NST;
+  uint64_t* full = bars;                  // [NST] rank 0's count both CTAs' copies
+  uint64_t* empty = full + NST;           // [NST] both CTAs (multicast commits)
+  uint64_t* acc_done = empty + NST;       // both CTAs
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -1381,11 +1393,13 @@ attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams 
   const int g = it.step;
   const int G = p.hq / p.hkv;
   const SeqInfo si = seq_info(p, it.b);
-  const int r_lo = it.c * si.L + it.tile * BM;
+  const int tpc = (si.L + 127) / 128;
+  const int tile = 2 * it.tile + static_cast<int>(rank);   // this CTA's KV tile of the chunk
+  const bool has_tile = tile < tpc;
+  const int r_lo = it.c * si.L + tile * BM;
   const int r_hi = min(r_lo + BM, (it.c + 1) * si.L);
   const int r_valid_hi = min(r_hi, si.S);
-  const int tpc = (si.L + 127) / 128;
-  const int kv_tile = it.c * tpc + it.tile;
+  const int kv_tile = it.c * tpc + tile;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -1397,15 +1411,17 @@ attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams 
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync_all();                     // both CTAs' barriers initialised
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the contributions of tile 2i (those of tile 2i+1 are among them)
   KvIter<BN> itr0;
-  itr0.init(p.cp, it.c, si.L, si.S, r_lo, G, g);
+  itr0.init(p.cp, it.c, si.L, si.S, it.c * si.L + 2 * it.tile * BM, G, g);
   const bool any = !itr0.done;
 
   if (warp == 0) {
@@ -1414,53 +1430,60 @@ attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams 
       KvIter<BN> itr = itr0;
       int64_t n_loads = 0;
       bool ok = true;
+      const int64_t plane = DV ? static_cast<int64_t>(G) * p.ds_cap : 0;
       for (int j = 0; !itr.done && ok; ++j, itr.next()) {
         const int st = j % NST;
         if (j >= NST) ok = mbar_wait(empty + st, ((j / NST) - 1) & 1, abort_flag);
         if (!ok) break;
-        mbar_arrive_expect_tx(full + st, Cfg::STAGE);
+        const uint32_t bar = mapa_u32(full + st, 0);
+        if (rank == 0) mbar_arrive_expect_tx(full + st, 2 * Cfg::STAGE);
         uint8_t* dst = smem + st * Cfg::STAGE;
-        const __nv_bfloat16* tile =
-            p.ds + (ds_tile_index(p, it.b, si.L, itr.cq, itr.tq, kv_tile, itr.h) + (DV ? G * p.ds_cap : 0)) *
-                       (128 * 128);
-        bulk_load(dst, tile, Cfg::DS_BYTES, full + st);
+        // this CTA's unit of the contribution exists unless its tile lies
+        // past the sequence or above the diagonal query tile
+        const int q0 = itr.q0();
+        const bool unit = has_tile && r_lo < si.S && (itr.cq != it.c || r_lo < min(q0 + BN, itr.q_valid_hi));
+        const int32_t t_idx =
+            unit ? static_cast<int32_t>(plane + ds_tile_index(p, it.b, si.L, itr.cq, itr.tq, kv_tile, itr.h)) : -1;
+        tma_load_3d_pair(dst, &tm_t, 0, 0, t_idx, bar);
         const int hq = itr.head();
-        const int row = static_cast<int>((hq / p.hpg_q) * p.T) + si.start + itr.q0();
-        for (int kc = 0; kc < D / 64; ++kc)
-          tma_load_3d(dst + Cfg::DS_BYTES + kc * BN * 128, &tm_q, kc * 64, hq % p.hpg_q, row, full + st);
+        const int row = static_cast<int>((hq / p.hpg_q) * p.T) + si.start + q0;
+        for (int kc = 0; kc < 2; ++kc)
+          tma_load_3d_pair(dst + Cfg::A_BYTES + kc * BN * 128, &tm_b, (2 * static_cast<int>(rank) + kc) * 64,
+                           hq % p.hpg_q, row, bar);
         ++n_loads;
       }
       if (!ok) {
         raise_status(p.status, CCG_ERR_TIMEOUT);
         *abort_flag = 1;
       }
-      wait_last_copies(full, NST, n_loads);
+      // rank 0's barriers count both CTAs' copies; the CTAs leave together
+      if (rank == 0) wait_last_copies(full, NST, n_loads);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    if (lane == 0 && rank == 0) {
       KvIter<BN> itr = itr0;
       bool ok = true;
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, D, true, true);
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, D, true, true);
       for (int j = 0; !itr.done && ok; ++j, itr.next()) {
         const int st = j % NST;
         ok = mbar_wait(full + st, (j / NST) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t base = smem_u32(smem + st * Cfg::STAGE);
-        const uint64_t a_desc = smem_desc_noswz(base, 128, 2048);           // dS^T, MN-major
-        const uint64_t b_desc = smem_desc_sw128(base + Cfg::DS_BYTES, BN * 128, 1024);   // Q, MN-major
+        const uint64_t a_desc = smem_desc_noswz(base, 128, 2048);           // dS^T (P^T), MN-major
+        const uint64_t b_desc = smem_desc_sw128(base + Cfg::A_BYTES, BN * 128, 1024);   // Q (dO) half, MN-major
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          umma_ss(tmem + Cfg::T_ACC, a_desc + static_cast<uint64_t>(k * 16 * 16 >> 4), b_desc + mnmajor_step(k),
-                  idesc, (j > 0 || k > 0) ? 1u : 0u);
-        umma_commit(empty + st);
+          umma_ss_pair(tmem + Cfg::T_ACC, a_desc + static_cast<uint64_t>(k * 16 * 16 >> 4),
+                       b_desc + mnmajor_step(k), idesc, (j > 0 || k > 0) ? 1u : 0u);
+        umma_commit_pair_both(empty + st);
       }
       if (!ok) {
         raise_status(p.status, CCG_ERR_TIMEOUT);
         *abort_flag = 1;
       }
-      umma_commit(acc_done);
+      umma_commit_pair_both(acc_done);
       volatile int never = 0;
       mbar_wait(acc_done, 0, &never, 200000000ull);
     }
@@ -1475,7 +1498,7 @@ attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams 
     if (!ok) {
       raise_status(p.status, CCG_ERR_TIMEOUT);
       *abort_flag = 1;
-    } else {
+    } else if (has_tile) {
       // each warpgroup writes 128 columns of the tile's rows (real rows the
       // gradient, padding rows 0), staged in the idle stage area
       tc_fence_after();
@@ -1490,10 +1513,14 @@ attn_bwd_dk_ds_kernel(const __grid_constant__ CUtensorMap tm_q, const BwdParams 
                         });
     }
   }
+  // neither CTA leaves (nor frees TMEM) while the other may still use its
+  // shared memory or TMEM: rank 0's MMA thread has seen every product
+  // complete, its producer every copy land
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync_all();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  if (warp == 2) tmem_dealloc_pair(tmem, Cfg::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -1844,14 +1871,28 @@ cudaError_t launch_half(const CUtensorMap* m, const BwdParams& p, int grid_items
 }
 
 template <bool DV>
-cudaError_t launch_dk_ds(const CUtensorMap& tb, const BwdParams& p, int grid_items, cudaStream_t s) {
-  const int smem = DkDsCfg::SMEM_TOTAL + 1024;
+cudaError_t launch_dkv_pair(const CUtensorMap& tb, const CUtensorMap& tt, const BwdParams& p, int pairs,
+                            cudaStream_t s) {
+  auto kern = attn_bwd_dkv_pair_kernel<DV>;
+  const int smem = DkvPairCfg::SMEM_TOTAL + 1024;
   static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_dk_ds_kernel<DV>, smem); });
+  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(kern, smem); });
   if (e != cudaSuccess) return e;
-  const int64_t grid = static_cast<int64_t>(grid_items) * p.hkv;
-  if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  attn_bwd_dk_ds_kernel<DV><<<static_cast<unsigned>(grid), DkDsCfg::THREADS, smem, s>>>(tb, p);
+  if (pairs < 1 || pairs > 0x3fffffff) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.blockDim = dim3(DkvPairCfg::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, tb, tt, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1885,7 +1926,8 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
                             const PlanHeader* hdr, const int32_t* cu, const int32_t* cu_pad, const float* lse,
                             const float* delta, void* dq, void* dk, void* dv, int32_t* status, int cp, int hq,
                             int hkv, int head_groups, int64_t T, int D, float scale, int grid_q, int grid_kv,
-                            int* launches, cudaStream_t stream, void* ds, const int64_t* ds_base, int64_t ds_cap) {
+                            int* launches, cudaStream_t stream, void* ds, const int64_t* ds_base, int64_t ds_cap,
+                            const CUtensorMap* ds_map, int kv_pairs) {
   BwdParams p;
   p.hdr = hdr;
   p.cu = cu;
@@ -1929,12 +1971,12 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
       p.out1 = static_cast<__nv_bfloat16*>(dk);
       p.kv_head = g;
       prof_begin("attn_bwd_dk", stream);
-      e = launch_dk_ds<false>(maps[8], p, grid_kv, stream);
+      e = launch_dkv_pair<false>(maps[8], *ds_map, p, kv_pairs, stream);
       prof_end(stream);
       if (e != cudaSuccess) return e;
       ++*launches;
       prof_begin("attn_bwd_dv", stream);
-      e = launch_dk_ds<true>(maps[11], p, grid_kv, stream);
+      e = launch_dkv_pair<true>(maps[11], *ds_map, p, kv_pairs, stream);
       prof_end(stream);
       if (e != cudaSuccess) return e;
       ++*launches;

@@ -166,8 +166,18 @@ plan_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ cu_pad, 
     if (threadIdx.x == 0) hdr->n_dq = min(slot, cap_q);
     // dK/dV pass: one item per (KV tile, kv head), (sequence, kv head)-major,
     // so that the CTAs in flight stream the Q/dO of few kv heads' groups;
-    // earlier KV chunks are seen by more queries, so they go first
-    {
+    // earlier KV chunks are seen by more queries, so they go first.  The dS
+    // backward (CTA pairs, one launch per kv head) instead takes one item per
+    // pair of KV tiles (2i, 2i+1) of a chunk, kv-head-major, so that a kv
+    // head's items are one contiguous n_kv / hkv range.
+    if (ds_base != nullptr) {
+      auto count = [&](int i) { return (all_tiles((i / C) % B, bn) + 1) / 2; };
+      auto write = [&](int i, int first, int n) {
+        const int g = i / (B * C), b = (i / C) % B, j = i % C;
+        for (int t = 0; t < n && first + t < cap_kv; ++t) kv_items[first + t] = WorkItem{b, j, t, g};
+      };
+      slot = block_emit(hkv * B * C, 0, count, write);
+    } else {
       auto count = [&](int i) { return all_tiles(i / (hkv * C), bn); };
       auto write = [&](int i, int first, int n) {
         const int b = i / (hkv * C), g = (i / C) % hkv, j = i % C;

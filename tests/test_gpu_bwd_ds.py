@@ -24,7 +24,12 @@ SHAPES = [
     W.custom_workload("ds_gqa8_d256_cp4_ragged", [1100, 36], 8, 1, 256, 4, pad_to=8),
     W.custom_workload("ds_empty_seqs_d256_cp2", [0, 300, 0, 77], 4, 2, 256, 2, pad_to=8),
     W.custom_workload("ds_cp16_d256_pad", [1000, 2100], 4, 1, 256, 16, pad_to=32),
+    # several KV tiles a chunk: the dK/dV passes' CTA pairs (tiles 2i, 2i+1),
+    # an odd last tile without a partner, ragged and padding tiles
+    W.custom_workload("ds_gqa4_d256_cp2_t3", [1536, 1200], 4, 1, 256, 2, pad_to=128),
+    W.custom_workload("ds_gqa2_d256_cp1_t4", [1024, 700, 260], 4, 2, 256, 1, pad_to=2),
 ]
+MULTI_TILE = SHAPES[-2:]
 
 
 def _bound(w):
@@ -54,7 +59,7 @@ def test_ds_backward_matches_oracle(lib, w):
         assert np.all(f64(a)[pad] == 0)
 
 
-@pytest.mark.parametrize("w", SHAPES[:3], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", SHAPES[:3] + MULTI_TILE, ids=lambda w: w.name)
 def test_ds_backward_agrees_with_the_recomputing_backward(lib, w):
     """Same dS and P values (the same arithmetic on the same S and dP, up to
     the tensor core's summation order in S versus S^T): dQ is that of the
