@@ -1,5 +1,6 @@
 """Full-size parity at the workloads' own sizes, in the launch configuration
-bench.py times (the AttentionStep pipeline), on seeded sampled
+bench.py times (the AttentionStep pipeline with the backward that keeps dS
+and P), on seeded sampled
 (sequence, q head) pairs the oracle computes one by one: O, LSE and dQ of
 the sampled head, dK and dV of its kv head (the oracle sums its whole GQA
 group).  Also checks that outputs are bitwise identical across three steps
@@ -72,7 +73,8 @@ def test_full_size_sampled_pairs_and_repeatability(lib, name):
     from context_causal_gqa_gb300.pipeline import AttentionStep
     w = W.WORKLOADS[name]
     x = W.make_inputs(w, device="cuda")
-    step = AttentionStep(w, x)
+    step = AttentionStep(w, x, keep_ds=True)      # the bench's backward (keeps dS and P at D=256)
+    assert step.max_seqlen > 0
     step.run()
     torch.cuda.synchronize()
     step.check()
