@@ -161,12 +161,14 @@ struct Layout {
   int64_t ds_cap_tiles;     // dS tiles of one q head the dS region holds (0: no dS backward)
 };
 
-// The D = 256 backward that keeps dS (a padded-length bound in the
-// descriptor): one 128 x 128 BF16 dS tile per (query tile, visible KV tile)
-// of each q head of one GQA group.  Per sequence and head the tiles number
+// The backward that keeps dS (a padded-length bound in the descriptor): one
+// 128 x 128 BF16 dS tile per (query tile, visible KV tile) of each q head of
+// one GQA group (and at D = 256 a P tile each as well).  Per sequence and head the tiles number
 // t^2 * 2CP(2CP+1)/2 (t = 128-row tiles of a chunk), and
 // sum_b t_b^2 <= t_max * sum_b t_b <= t_max * (T / (128 * 2CP) + B).
-bool bwd_keeps_ds(const ccg_attn_desc* d) { return d->head_dim == 256 && d->max_seqlen > 0; }
+bool bwd_keeps_ds(const ccg_attn_desc* d) { return d->max_seqlen > 0; }
+// dS tiles, then (D = 256) P tiles
+int64_t ds_planes(const ccg_attn_desc* d) { return d->head_dim == 256 ? 2 : 1; }
 int64_t ds_cap_tiles(const ccg_attn_desc* d) {
   if (!bwd_keeps_ds(d)) return 0;
   const int64_t C = 2 * d->cp;
@@ -202,7 +204,7 @@ Layout workspace_layout(const ccg_attn_desc* d, int kind) {
   L.ds_base = off;
   off = align_up(off + (L.ds_cap_tiles > 0 ? size_t(d->batch + 1) * sizeof(int64_t) : 0), 256);
   L.ds = off;
-  off = align_up(off + 2 * size_t(L.ds_cap_tiles) * (d->hq / d->hkv) * kDsTileBytes, 256);   // dS, then P
+  off = align_up(off + ds_planes(d) * size_t(L.ds_cap_tiles) * (d->hq / d->hkv) * kDsTileBytes, 256);
   // the partial slabs hold one head part (all heads without partitioning)
   const size_t rows = size_t(d->total_tokens) * d->hq / head_parts_of(d);
   L.o_parts = off;
@@ -720,7 +722,8 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
   CUtensorMap ds_map;
   int kv_pairs = 0;
   if (L.ds_cap_tiles > 0) {
-    if (!make_tile_map(&ds_map, base + L.ds, 2 * L.ds_cap_tiles * (desc->hq / desc->hkv))) return CCG_ERR_CUDA;
+    if (D == 256 && !make_tile_map(&ds_map, base + L.ds, 2 * L.ds_cap_tiles * (desc->hq / desc->hkv)))
+      return CCG_ERR_CUDA;
     kv_pairs = static_cast<int>(desc->total_tokens / 256 + int64_t(desc->batch) * 2 * desc->cp + 1);
   }
   int kl = 0;

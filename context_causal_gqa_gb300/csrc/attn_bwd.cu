@@ -374,7 +374,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const BwdParams p) {
   constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, KCH = D / 64;
-  const int item_idx = blockIdx.x / p.hq;
+  const int item_idx = blockIdx.x / p.nheads;
   if (item_idx >= p.hdr->n_dq) return;
   if (status_bad(p.status)) return;
 
@@ -393,8 +393,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WorkItem it = p.items[item_idx];
-  const int h = blockIdx.x % p.hq;
-  const int g = h / (p.hq / p.hkv);
+  const int h = p.head0 + blockIdx.x % p.nheads;   // q head
+  const int G = p.hq / p.hkv;
+  const int g = h / G;
   const SeqInfo si = seq_info(p, it.b);
   const int q_lo = it.c * si.L + it.tile * BM;                    // first row (sequence position)
   const int q_hi = min(q_lo + BM, (it.c + 1) * si.L);              // rows owned by this tile
@@ -554,6 +555,13 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const int k0 = itr.k0();
       const int kend = itr.diag ? min(itr.kv_hi, q_pos + 1) : itr.kv_hi;
       const int nvalid = row_valid ? kend - k0 : 0;
+      // dS backward: this unit's dS tile (the dK/dV pass reads it back)
+      uint4* ds_tile = nullptr;
+      if (p.ds != nullptr) {
+        const int tpc = (si.L + 127) / 128;
+        const int kv_tile = (k0 / si.L) * tpc + (k0 % si.L) / 128;
+        ds_tile = reinterpret_cast<uint4*>(p.ds) + ds_tile_index(p, it.b, si.L, it.c, it.tile, kv_tile, h % G) * (128 * 128 / 8);
+      }
       // hidden keys only on tiles that cross a row's last visible key: their
       // scores become -inf in registers, so P (and dS) come out exactly 0
       const bool masked = __any_sync(0xffffffffu, nvalid < BN);
@@ -582,6 +590,13 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           pk[x] = pack_bf16x2(d0, d1);
         }
         tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_A : tb) + c * 16, pk);
+        if (ds_tile != nullptr) {
+          // 16-byte pieces 4c .. 4c+3 of this row: a warp's store covers 32
+          // consecutive rows of one piece (512 bytes)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            ds_tile[(4 * c + i) * 128 + row] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -1528,6 +1543,303 @@ attn_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_
 }
 
 // ---------------------------------------------------------------------------
+// D = 128 dK/dV pass of the dS backward: dV = sum of P^T dO with P^T
+// recomputed from S^T = K Q^T, and dK = sum of dS^T Q with the dS tiles the
+// dQ pass stored, so dP^T is never formed.  One CTA per 128-row KV tile of
+// kv head p.kv_head (the items are the dS backward's KV tile pairs; CTA 2i+s
+// takes tile s of pair i).  K is resident (32 KB); per contribution (the
+// canonical order) the Q tile and the dS tile arrive together in one of two
+// 64 KB stages, the dO tile in one of two 32 KB stages.  TMEM: two S^T
+// buffers (128 columns each) next to the dV and dK accumulators, so the
+// softmax warpgroup of contribution j (j % 2) forms P^T while the tensor
+// core runs dV(j-1), dK(j) and S^T(j+1).  Product order: S^T(0), dK(0),
+// S^T(1), then per j: dV(j), dK(j+1), S^T(j+2) -- a Q/dS stage is released
+// by its dK product three products before the S^T that reuses it, a dO stage
+// by its dV five before.  The Q tile is read as the K-major B operand of
+// S^T and as the MN-major B operand of dK; dS^T is read MN-major from the
+// unswizzled stored tile (core matrices 128 B apart along K, 2048 B along M).
+struct DkvDs128Cfg {
+  static constexpr int THREADS = 384;           // 0 TMA, 1 MMA, 2 TMEM, 4..11 two softmax warpgroups
+  static constexpr int D = 128;
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int K_BYTES = BM * D * 2;    // resident K
+  static constexpr int Q_BYTES = BN * D * 2;
+  static constexpr int DS_BYTES = 128 * 128 * 2;
+  static constexpr int QS_BYTES = Q_BYTES + DS_BYTES;
+  static constexpr int DO_BYTES = BN * D * 2;
+  static constexpr int SMEM_QS = K_BYTES;
+  static constexpr int SMEM_DO = SMEM_QS + 2 * QS_BYTES;
+  static constexpr int SMEM_BAR = SMEM_DO + 2 * DO_BYTES;
+  static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
+  static constexpr int T_DV = 2 * BN, T_DK = 2 * BN + D, TMEM_COLS = 512;
+  static_assert(T_DK + D <= TMEM_COLS, "TMEM");
+  static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
+  static_assert(2 * QS_BYTES >= 8 * 32 * 256, "epilogue staging fits the Q/dS stages");
+};
+
+__global__ void __launch_bounds__(DkvDs128Cfg::THREADS, 1)
+attn_bwd_dkdv_ds128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using Cfg = DkvDs128Cfg;
+  constexpr int BM = Cfg::BM, BN = Cfg::BN, D = Cfg::D, KCH = D / 64;
+  const int n_head = p.hdr->n_kv / p.hkv;
+  const int pair = blockIdx.x >> 1;
+  if (pair >= n_head) return;
+  if (status_bad(p.status)) return;
+  const WorkItem it = p.items[static_cast<int64_t>(p.kv_head) * n_head + pair];
+  const SeqInfo si = seq_info(p, it.b);
+  const int tpc = (si.L + 127) / 128;
+  const int tile = 2 * it.tile + static_cast<int>(blockIdx.x & 1);
+  if (tile >= tpc) return;                          // a chunk with an odd number of tiles
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::SMEM_BAR);
+  uint64_t* res_full = bars;
+  uint64_t* qs_full = res_full + 1;       // [2] Q and dS of a contribution
+  uint64_t* qs_empty = qs_full + 2;       // [2]
+  uint64_t* do_full = qs_empty + 2;       // [2] dO of a contribution
+  uint64_t* do_empty = do_full + 2;       // [2]
+  uint64_t* s_full = do_empty + 2;        // [2] S^T in buffer b
+  uint64_t* p_full = s_full + 2;          // [2] P^T packed over buffer b
+  uint64_t* acc_done = p_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = it.step;
+  const int G = p.hq / p.hkv;
+  const int k_lo = it.c * si.L + tile * BM;
+  const int k_hi = min(k_lo + BM, (it.c + 1) * si.L);
+  const int k_valid_hi = min(k_hi, si.S);
+  const int kv_tile = it.c * tpc + tile;
+
+  if (threadIdx.x == 0) {
+    mbar_init(res_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(qs_full + b, 1);
+      mbar_init(qs_empty + b, 1);
+      mbar_init(do_full + b, 1);
+      mbar_init(do_empty + b, 1);
+      mbar_init(s_full + b, 1);
+      mbar_init(p_full + b, 128);
+    }
+    mbar_init(acc_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  KvIter<BN> itr0;
+  itr0.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
+  const bool any = !itr0.done;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      KvIter<BN> itr = itr0;
+      int64_t n = 0;                                 // contributions
+      int64_t n_qs = 0, n_do = 0;                    // Q/dS and dO copies issued
+      bool ok = true;
+      // L2: a dS tile is read once; a Q (dO) tile again by every KV tile that sees it
+      const uint64_t pol_once = l2_evict_first(), pol_reuse = l2_evict_last();
+      if (!itr.done) {
+        const int krow = static_cast<int>((g / p.hpg_kv) * p.T) + si.start + k_lo;
+        mbar_arrive_expect_tx(res_full, Cfg::K_BYTES);
+        for (int kc = 0; kc < KCH; ++kc)
+          tma_load_3d(smem + kc * BM * 128, &tm_k, kc * 64, g % p.hpg_kv, krow, res_full);
+        for (; !itr.done && ok; ++n, itr.next()) {
+          const int st = static_cast<int>(n & 1);
+          const uint32_t ph = static_cast<uint32_t>(((n >> 1) - 1) & 1);
+          const int hq = itr.head();
+          const int qrow = static_cast<int>((hq / p.hpg_q) * p.T) + si.start + itr.q0();
+          // Q and dS
+          if (n >= 2) ok = mbar_wait(qs_empty + st, ph, abort_flag);
+          if (!ok) break;
+          uint8_t* qs = smem + Cfg::SMEM_QS + st * Cfg::QS_BYTES;
+          mbar_arrive_expect_tx(qs_full + st, Cfg::QS_BYTES);
+          for (int kc = 0; kc < KCH; ++kc)
+            tma_load_3d_hint(qs + kc * BN * 128, &tm_q, kc * 64, hq % p.hpg_q, qrow, qs_full + st, pol_reuse);
+          const __nv_bfloat16* ds = p.ds + ds_tile_index(p, it.b, si.L, itr.cq, itr.tq, kv_tile, itr.h) * (128 * 128);
+          bulk_load_hint(qs + Cfg::Q_BYTES, ds, Cfg::DS_BYTES, qs_full + st, pol_once);
+          ++n_qs;
+          // dO
+          if (n >= 2) ok = mbar_wait(do_empty + st, ph, abort_flag);
+          if (!ok) break;
+          uint8_t* dst = smem + Cfg::SMEM_DO + st * Cfg::DO_BYTES;
+          mbar_arrive_expect_tx(do_full + st, Cfg::DO_BYTES);
+          for (int kc = 0; kc < KCH; ++kc)
+            tma_load_3d_hint(dst + kc * BN * 128, &tm_do, kc * 64, hq % p.hpg_q, qrow, do_full + st, pol_reuse);
+          ++n_do;
+        }
+        if (!ok) {
+          raise_status(p.status, CCG_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        volatile int never = 0;
+        mbar_wait(res_full, 0, &never, 200000000ull);
+        wait_last_copies(qs_full, 2, n_qs);
+        wait_last_copies(do_full, 2, n_do);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      KvIter<BN> cnt = itr0;
+      int n = 0;
+      for (; !cnt.done; cnt.next()) ++n;
+      bool ok = true;
+      if (n > 0) {
+        const uint64_t k_desc = smem_desc_sw128(smem_u32(smem), 16, 1024);
+        const uint32_t qs0 = smem_u32(smem + Cfg::SMEM_QS), do0 = smem_u32(smem + Cfg::SMEM_DO);
+        constexpr uint32_t idesc_dk = idesc_bf16_f32(BM, D, true, true);
+        ok = mbar_wait(res_full, 0, abort_flag);
+        tc_fence_after();
+        // S^T(j) = K Q_j^T into buffer j % 2 (the Q/dS stage is waited for here)
+        auto issue_s = [&](int j) -> bool {
+          const int st = j & 1;
+          if (!mbar_wait(qs_full + st, (j >> 1) & 1, abort_flag)) return false;
+          tc_fence_after();
+          mma_kk<BM, BN, D>(tmem + st * BN, k_desc, smem_desc_sw128(qs0 + st * Cfg::QS_BYTES, 16, 1024));
+          umma_commit(s_full + st);
+          return true;
+        };
+        // dK += dS_j^T Q_j (after S^T(j): the stage is already waited for)
+        auto issue_dk = [&](int j) {
+          const int st = j & 1;
+          const uint32_t base = qs0 + st * Cfg::QS_BYTES;
+          const uint64_t a_desc = smem_desc_noswz(base + Cfg::Q_BYTES, 128, 2048);
+          const uint64_t b_desc = smem_desc_sw128(base, BN * 128, 1024);
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k)
+            umma_ss(tmem + Cfg::T_DK, a_desc + static_cast<uint64_t>(k * 16 * 16 >> 4), b_desc + mnmajor_step(k),
+                    idesc_dk, (j > 0 || k > 0) ? 1u : 0u);
+          umma_commit(qs_empty + st);
+        };
+        if (ok) ok = issue_s(0);
+        if (ok) issue_dk(0);
+        if (ok && n > 1) ok = issue_s(1);
+        for (int j = 0; ok && j < n; ++j) {
+          const int b = j & 1;
+          // dV += P_j^T dO_j
+          ok = mbar_wait(p_full + b, (j >> 1) & 1, abort_flag);
+          if (!ok) break;
+          ok = mbar_wait(do_full + b, (j >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          mma_tn<BN, D>(tmem + Cfg::T_DV, tmem + b * BN, smem_desc_sw128(do0 + b * Cfg::DO_BYTES, BN * 128, 1024),
+                        j > 0);
+          umma_commit(do_empty + b);
+          if (j + 1 < n) issue_dk(j + 1);
+          if (j + 2 < n) ok = issue_s(j + 2);       // into buffer b, after dV(j) has read P^T there
+        }
+      }
+      if (!ok) {
+        raise_status(p.status, CCG_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      umma_commit(acc_done);
+      volatile int never = 0;
+      mbar_wait(acc_done, 0, &never, 200000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax: P^T of contributions j % 2 == wg
+    const int wg = (warp - 4) >> 2;
+    const int row = ((warp & 3) << 5) + lane;        // key row of the tile
+    const uint32_t t0 = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const int k_pos = k_lo + row;
+    const bool k_valid = k_pos < k_valid_hi;
+    const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2);
+    KvIter<BN> itr = itr0;
+    bool ok = true;
+    for (int j = 0; !itr.done; ++j, itr.next()) {
+      if ((j & 1) != wg) continue;
+      const uint32_t tb = t0 + wg * BN;
+      // -LSE (log2 units) of the contribution's query columns: lane l holds
+      // columns 2l, 2l+1 (lo) and 64+2l, 64+2l+1 (hi), handed out by shuffles
+      uint64_t lse_lo, lse_hi;
+      {
+        const int q0 = itr.q0();
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int col = (e >> 1) * 64 + 2 * lane + (e & 1);
+          v[e] = 0.f;
+          if (q0 + col < itr.q_valid_hi)
+            v[e] = -__ldg(p.lse + thd_row(si.start + q0 + col, itr.head(), p.hpg_q, p.T)) * kLog2e;
+        }
+        lse_lo = f32x2(v[0], v[1]);
+        lse_hi = f32x2(v[2], v[3]);
+      }
+      const int q0 = itr.q0();
+      // query column c is visible to this key row iff q0+c >= k_pos and q0+c < q_valid_hi
+      const int c_lo = k_valid ? max(0, k_pos - q0) : BN;
+      const int c_hi = k_valid ? itr.q_valid_hi - q0 : 0;
+      const bool masked = __any_sync(0xffffffffu, c_lo > 0 || c_hi < BN);
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full + wg, (j >> 1) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t rs[32];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        tmem_ld32(tb + c * 32, rs);
+        tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int col = c * 32 + x;
+            rs[x] = (col >= c_lo && col < c_hi) ? rs[x] : 0xff800000u;
+          }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          // columns c*32 + 2x, +1: held by lane (16c + x) % 32, in lo (c < 2) or hi
+          const uint64_t nl = __shfl_sync(0xffffffffu, c < 2 ? lse_lo : lse_hi, (16 * c + x) & 31);
+          float a0, a1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2, nl),
+                      a0, a1);
+          pk[x] = pack_bf16x2(ex2_approx(a0), ex2_approx(a1));
+        }
+        tmem_st16(tb + c * 16, pk);                 // P^T packed over the buffer's first 64 columns
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full + wg);
+    }
+    if (ok && any) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
+    if (!ok) {
+      raise_status(p.status, CCG_ERR_TIMEOUT);
+      *abort_flag = 1;
+    } else {
+      // warpgroup 0 writes dV, warpgroup 1 dK (real rows the gradient,
+      // padding rows 0), staged in the idle Q/dS stages
+      tc_fence_after();
+      __nv_bfloat16* outp = wg == 0 ? p.out0 : p.out1;
+      uint4* stage = reinterpret_cast<uint4*>(smem + Cfg::SMEM_QS) + (warp - 4) * 32 * 16;
+      const int wrow0 = k_lo + (warp & 3) * 32;
+      store_rows_staged(stage, t0 + (wg == 0 ? Cfg::T_DV : Cfg::T_DK), any, !any || !k_valid, 1.f, lane,
+                        [&](int rr) -> uint4* {
+                          const int pos = wrow0 + rr;
+                          if (pos >= k_hi) return nullptr;
+                          return reinterpret_cast<uint4*>(outp + thd_row(si.start + pos, g, p.hpg_kv, p.T) * D);
+                        });
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
 // D = 256 dV pass: one CTA per (128-row KV tile, kv head) with only K
 // resident (64 KB), so five half-tile slots stream the 128-column halves of
 // Q_i (for S^T = sum_h K[:, h] Q_i,h^T) and dO_i (for dV[:, h] += P^T dO_i,h)
@@ -1836,7 +2148,7 @@ cudaError_t launch_dq(const CUtensorMap* m, const BwdParams& p, int grid_items, 
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_dq_kernel<Cfg, D>, smem); });
   if (e != cudaSuccess) return e;
-  const int64_t grid = static_cast<int64_t>(grid_items) * p.hq;
+  const int64_t grid = static_cast<int64_t>(grid_items) * p.nheads;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
   attn_bwd_dq_kernel<Cfg, D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(m[0], m[1], m[2], m[3], p);
   return cudaGetLastError();
@@ -1900,6 +2212,17 @@ cudaError_t launch_dkv_pair(const CUtensorMap& tb, const CUtensorMap& tt, const 
   return cudaGetLastError();
 }
 
+cudaError_t launch_dkdv_ds128(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tdo,
+                              const BwdParams& p, int pairs, cudaStream_t s) {
+  const int smem = DkvDs128Cfg::SMEM_TOTAL + 1024;
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = once_per_device(attr_done, [&] { return set_smem(attn_bwd_dkdv_ds128_kernel, smem); });
+  if (e != cudaSuccess) return e;
+  if (pairs < 1 || pairs > 0x3fffffff) return cudaErrorInvalidValue;
+  attn_bwd_dkdv_ds128_kernel<<<static_cast<unsigned>(2 * pairs), DkvDs128Cfg::THREADS, smem, s>>>(tq, tk, tdo, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dv256(const CUtensorMap* m, const BwdParams& p, int grid_items, cudaStream_t s) {
   const int smem = DvCfg::SMEM_TOTAL + 1024;
   static std::atomic<uint64_t> attr_done{0};
@@ -1954,6 +2277,34 @@ cudaError_t launch_attn_bwd(const CUtensorMap* maps, const WorkItem* dq_items, c
   p.ds_cap = ds_cap;
   p.kv_head = 0;
   cudaError_t e;
+  if (D == 128 && ds != nullptr) {
+    // dS backward at D = 128: per kv head, the dQ pass over its q heads
+    // writes their dS tiles, then one dK/dV pass recomputes P^T and reads them
+    const int G = hq / hkv;
+    for (int g = 0; g < hkv; ++g) {
+      p.items = dq_items;
+      p.out0 = static_cast<__nv_bfloat16*>(dq);
+      p.out1 = nullptr;
+      p.head0 = g * G;
+      p.nheads = G;
+      p.ds = static_cast<__nv_bfloat16*>(ds);
+      prof_begin("attn_bwd_dq", stream);
+      e = launch_dq<Dq128, 128>(maps, p, grid_q, stream);
+      prof_end(stream);
+      if (e != cudaSuccess) return e;
+      ++*launches;
+      p.items = kv_items;
+      p.out0 = static_cast<__nv_bfloat16*>(dv);
+      p.out1 = static_cast<__nv_bfloat16*>(dk);
+      p.kv_head = g;
+      prof_begin("attn_bwd_dkdv", stream);
+      e = launch_dkdv_ds128(maps[4], maps[5], maps[7], p, kv_pairs, stream);
+      prof_end(stream);
+      if (e != cudaSuccess) return e;
+      ++*launches;
+    }
+    return cudaSuccess;
+  }
   if (D == 256 && ds != nullptr) {
     // dS backward: per kv head, the dQ pass over its q heads writes their dS
     // and P tiles, then its dK pass and its dV pass read them

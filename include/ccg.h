@@ -101,15 +101,17 @@ typedef struct {
   int64_t q_pitch, k_pitch, v_pitch, do_pitch;
   /* 0, or an upper bound on every sequence's padded length
    * (cu_seqlens_padded[b+1] - cu_seqlens_padded[b] <= max_seqlen, checked on
-   * the device: CCG_ERR_SEQLENS).  With D = 256 a bound selects the backward
-   * that keeps dS and P: the dQ pass also writes each unit's BF16 dS and P
-   * tiles to the workspace, and the dK and dV passes read them back
-   * (dK += dS^T Q, dV += P^T dO: one product per unit instead of
-   * recomputing S^T, and dP^T for dK).  The kv heads are then taken one at a
-   * time (the dQ pass over the kv head's q heads, then its dK and dV
-   * passes), so the tiles the workspace holds are those of one GQA group:
+   * the device: CCG_ERR_SEQLENS).  A bound selects the backward that keeps
+   * dS: the dQ pass also writes each unit's BF16 dS tile to the workspace
+   * and the dK pass reads it back (dK += dS^T Q, instead of recomputing dP^T
+   * and dS^T).  With D = 256 it keeps P as well (dV += P^T dO from the stored
+   * P: one product per unit each for dK and dV); with D = 128 one dK/dV pass
+   * recomputes only P^T.  The kv heads are then taken one at a time (the dQ
+   * pass over the kv head's q heads, then its dK/dV passes), so the tiles
+   * the workspace holds are those of one GQA group:
    * ccg_workspace_size(desc, 1) grows by about
-   * 2 (hq/hkv) * ceil(max_seqlen / (256 cp)) * (T / (256 cp) + B) * cp (2 cp + 1) * 32 KiB.
+   * K (hq/hkv) * ceil(max_seqlen / (256 cp)) * (T / (256 cp) + B) * cp (2 cp + 1) * 32 KiB,
+   * K = 2 at D = 256 (dS and P), 1 at D = 128 (dS).
    * 0 keeps the backward that recomputes them. */
   int64_t max_seqlen;
 } ccg_attn_desc;

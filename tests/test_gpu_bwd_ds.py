@@ -1,6 +1,6 @@
-"""The D = 256 backward that keeps dS and P (a padded-length bound in the
-descriptor): the dQ pass writes every unit's dS and P tiles, the dK and dV
-passes read them back.  Checked against the FP64 oracle, against the
+"""The backward that keeps dS (a padded-length bound in the descriptor): the
+dQ pass writes every unit's dS tile (at D = 256 its P tile too), the dK/dV
+passes read them back (at D = 128 one dK/dV pass recomputing only P^T).  Checked against the FP64 oracle, against the
 backward that recomputes them, for bitwise repeatability under NaN-poisoned
 outputs, and for the device check of the bound.
 """
@@ -30,6 +30,14 @@ SHAPES = [
     W.custom_workload("ds_gqa2_d256_cp1_t4", [1024, 700, 260], 4, 2, 256, 1, pad_to=2),
 ]
 MULTI_TILE = SHAPES[-2:]
+SHAPES_D128 = [
+    W.custom_workload("ds_gqa4_d128_cp2", [512], 4, 1, 128, 2),
+    W.custom_workload("ds_gqa2_d128_cp4_pad", [300, 77], 4, 2, 128, 4, pad_to=64),
+    W.custom_workload("ds_gqa8_d128_cp8_pad", [700, 1500], 8, 1, 128, 8, pad_to=128),
+    W.custom_workload("ds_empty_seqs_d128_cp2", [0, 300, 0, 77], 4, 2, 128, 2, pad_to=8),
+    W.custom_workload("ds_gqa4_d128_cp2_t3", [1536, 1200], 4, 1, 128, 2, pad_to=128),
+    W.custom_workload("ds_gqa2_d128_cp1_t4", [1024, 700, 260], 4, 2, 128, 1, pad_to=2),
+]
 
 
 def _bound(w):
@@ -45,7 +53,7 @@ def _bwd(lib, x, w, o, lse, max_seqlen, **kw):
                         max_seqlen=max_seqlen, **kw)
 
 
-@pytest.mark.parametrize("w", SHAPES, ids=lambda w: w.name)
+@pytest.mark.parametrize("w", SHAPES + SHAPES_D128, ids=lambda w: w.name)
 def test_ds_backward_matches_oracle(lib, w):
     x = W.make_inputs(w, device="cuda")
     o, lse = _fwd(lib, x, w)
@@ -59,7 +67,7 @@ def test_ds_backward_matches_oracle(lib, w):
         assert np.all(f64(a)[pad] == 0)
 
 
-@pytest.mark.parametrize("w", SHAPES[:3] + MULTI_TILE, ids=lambda w: w.name)
+@pytest.mark.parametrize("w", SHAPES[:3] + MULTI_TILE + SHAPES_D128[:1] + SHAPES_D128[-2:], ids=lambda w: w.name)
 def test_ds_backward_agrees_with_the_recomputing_backward(lib, w):
     """Same dS and P values (the same arithmetic on the same S and dP, up to
     the tensor core's summation order in S versus S^T): dQ is that of the
@@ -75,8 +83,8 @@ def test_ds_backward_agrees_with_the_recomputing_backward(lib, w):
         assert np.linalg.norm(a - b) <= 1e-2 * np.linalg.norm(b) + 1e-6
 
 
-def test_ds_backward_bitwise_repeatable_under_poison(lib):
-    w = SHAPES[2]
+@pytest.mark.parametrize("w", [SHAPES[2], SHAPES_D128[2]], ids=lambda w: w.name)
+def test_ds_backward_bitwise_repeatable_under_poison(lib, w):
     x = W.make_inputs(w, device="cuda")
     o, lse = _fwd(lib, x, w)
     g1 = _bwd(lib, x, w, o, lse, _bound(w))
