@@ -82,7 +82,7 @@ __device__ __forceinline__ int64_t ds_tile_index(const BwdParams& p, int b, int 
 // with the final LSE every tile's P is independent of the others.
 constexpr int kThreads = 384;    // warp 0 TMA, 1 MMA, 2 TMEM alloc, 3 idle, 4-11 two softmax warpgroups
 
-template <int D, int BN_, int NSLOT_, int NBUF_>
+template <int D, int BN_, int NSLOT_, int NBUF_, bool SDB_ = false>
 struct DqCfg {
   static constexpr int BM = 128;                 // query rows (MMA M)
   static constexpr int BN = BN_;                 // key rows per tile (MMA N of S, K of dQ)
@@ -100,13 +100,20 @@ struct DqCfg {
   static constexpr int SMEM_BAR = SMEM_SLOT + NSLOT * SLOT_BYTES;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
   static constexpr int T_BUF = 2 * BN;           // buffer b: S at b*T_BUF, dP at b*T_BUF + BN
-  static constexpr int T_ACC = NBUF * T_BUF;
+  // SDB (split columns only): two S buffers (S of tile j at (j % 2) * BN), one
+  // dP buffer at 2 * BN with dS packed over each warpgroup's own dP columns,
+  // so that S of tile j+1 is computed while the softmax forms dS of tile j
+  static constexpr bool SDB = SDB_;
+  static constexpr int T_DP = 2 * BN;
+  static constexpr int T_ACC = SDB ? 3 * BN : NBUF * T_BUF;
   // dS (BF16, the A operand of dQ += dS K): packed in place over S when one
   // warpgroup owns the whole tile; with split columns it goes to its own
-  // region, since the other warpgroup may still be reading S there
-  static constexpr int T_A = SPLIT ? T_ACC + D : -1;
+  // region, since the other warpgroup may still be reading S there (SDB:
+  // over the warpgroup's own dP columns)
+  static constexpr int T_A = SPLIT && !SDB ? T_ACC + D : 0;   // 0: unused
   static constexpr int TMEM_COLS = 512;
-  static_assert(NBUF * 2 * BN + D + (SPLIT ? BN / 2 : 0) <= 512, "TMEM");
+  static_assert(!SDB || (SPLIT && 3 * BN + D <= 512), "TMEM (SDB)");
+  static_assert(SDB || NBUF * 2 * BN + D + (SPLIT ? BN / 2 : 0) <= 512, "TMEM");
   static_assert((SPLIT ? BN / 2 : BN) % 32 == 0, "softmax chunking");
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
 };
@@ -439,12 +446,13 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tma_load_3d(smem + Cfg::SMEM_RES + Cfg::RES_BYTES + kc * BM * 128, &tm_do, kc * 64, h % p.hpg_q, row,
                       res_full);
         }
-        // stream order per KV tile: V_j (released after dP) then K_j (released after dQ)
+        // stream order per KV tile: V_j (released after dP) then K_j (released
+        // after dQ); SDB: K_j (for S, issued a tile ahead) then V_j
         for (int t = 0; !itr.done && ok; ++t) {
           const int slot = t % NSLOT;
           if (t >= NSLOT) ok = mbar_wait(empty + slot, ((t / NSLOT) - 1) & 1, abort_flag);
           if (!ok) break;
-          const bool is_v = (t & 1) == 0;
+          const bool is_v = Cfg::SDB ? (t & 1) == 1 : (t & 1) == 0;
           const int k0 = itr.k0();
           mbar_arrive_expect_tx(full + slot, Cfg::SLOT_BYTES);
           uint8_t* dst = smem + Cfg::SMEM_SLOT + slot * Cfg::SLOT_BYTES;
@@ -452,7 +460,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tma_load_3d(dst + kc * BN * 128, is_v ? &tm_v : &tm_k, kc * 64, g % p.hpg_kv, kv_group_row + k0,
                         full + slot);
           ++n_loads;
-          if (!is_v) itr.next();
+          if (Cfg::SDB ? is_v : !is_v) itr.next();
         }
         if (!ok) {
           raise_status(p.status, CCG_ERR_TIMEOUT);
@@ -499,12 +507,47 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           umma_commit(s_full + b);
           return true;
         };
+        if constexpr (Cfg::SDB) {
+          // S(j) into S buffer j % 2 from K_j (slot 2j), dP(j) from V_j (slot
+          // 2j+1); the softmax of tile j starts once both are complete.
+          // Order: S(0), dP(0), S(1), then per j: dQ(j), dP(j+1), S(j+2)
+          int n = 0;
+          for (DqIter<BN> c2 = ahead; !c2.done; c2.next()) ++n;
+          auto issue_s = [&](int jj) -> bool {
+            const int t = 2 * jj, sl = t % NSLOT;
+            if (!mbar_wait(full + sl, (t / NSLOT) & 1, abort_flag)) return false;
+            tc_fence_after();
+            mma_kk<BM, BN, D>(tmem + (jj & 1) * BN, q_desc, slot_k(sl));
+            return true;
+          };
+          auto issue_dp = [&](int jj) -> bool {
+            const int t = 2 * jj + 1, sl = t % NSLOT;
+            if (!mbar_wait(full + sl, (t / NSLOT) & 1, abort_flag)) return false;
+            tc_fence_after();
+            mma_kk<BM, BN, D>(tmem + Cfg::T_DP, do_desc, slot_k(sl));
+            umma_commit(empty + sl);                  // V_jj done
+            umma_commit(s_full);                      // S(jj) and dP(jj) complete
+            return true;
+          };
+          if (ok && n > 0) ok = issue_s(0) && issue_dp(0);
+          if (ok && n > 1) ok = issue_s(1);
+          for (int j = 0; ok && j < n; ++j) {
+            ok = mbar_wait(ds_full, j & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const int sk = (2 * j) % NSLOT;
+            mma_tn_split<BN, D, true>(tmem + Cfg::T_ACC, tmem + Cfg::T_DP, slot_mn(sk), j > 0);
+            umma_commit(empty + sk);                  // K_j done
+            if (j + 1 < n) ok = issue_dp(j + 1);      // over dS(j), after dQ(j) read it
+            if (ok && j + 2 < n) ok = issue_s(j + 2); // into S buffer j % 2, read by softmax(j)
+          }
+        }
         int j_sp = 0;
-        while (ok && !ahead.done && j_sp < Cfg::NBUF) {
+        while (!Cfg::SDB && ok && !ahead.done && j_sp < Cfg::NBUF) {
           ok = issue_sp(j_sp++);
           ahead.next();
         }
-        for (int j = 0; ok && j < j_sp; ++j) {
+        for (int j = 0; !Cfg::SDB && ok && j < j_sp; ++j) {
           const int b = j % Cfg::NBUF;
           ok = mbar_wait(ds_full + b, (j / Cfg::NBUF) & 1, abort_flag);
           if (!ok) break;
@@ -549,6 +592,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (!Cfg::SPLIT && (j & 1) != wg) continue;
       const int b = j % Cfg::NBUF;
       const uint32_t tb = t0 + b * Cfg::T_BUF;
+      // SDB: S in buffer j % 2, dP in its own buffer
+      const uint32_t ts = Cfg::SDB ? t0 + (j & 1) * BN : tb;
+      const uint32_t tdp = Cfg::SDB ? t0 + Cfg::T_DP : tb + BN;
       ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j / Cfg::NBUF) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
@@ -568,8 +614,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       uint32_t rs[32], rp[32];
 #pragma unroll
       for (int c = c_first; c < c_first + NC; ++c) {
-        tmem_ld32(tb + c * 32, rs);
-        tmem_ld32(tb + BN + c * 32, rp);
+        tmem_ld32(ts + c * 32, rs);
+        tmem_ld32(tdp + c * 32, rp);
         tmem_wait_ld();
         if (masked) {
 #pragma unroll
@@ -589,7 +635,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           f32x2_split(mul_f32x2(pv, t), d0, d1);
           pk[x] = pack_bf16x2(d0, d1);
         }
-        tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_A : tb) + c * 16, pk);
+        if constexpr (Cfg::SDB)
+          tmem_st16(tdp + c_first * 32 + (c - c_first) * 16, pk);   // over the warpgroup's own dP columns
+        else
+          tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_A : tb) + c * 16, pk);
         if (ds_tile != nullptr) {
           // 16-byte pieces 4c .. 4c+3 of this row: a warp's store covers 32
           // consecutive rows of one piece (512 bytes)
@@ -1551,8 +1600,9 @@ attn_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_
 // canonical order) the Q tile and the dS tile arrive together in one of two
 // 64 KB stages, the dO tile in one of two 32 KB stages.  TMEM: two S^T
 // buffers (128 columns each) next to the dV and dK accumulators, so the
-// softmax warpgroup of contribution j (j % 2) forms P^T while the tensor
-// core runs dV(j-1), dK(j) and S^T(j+1).  Product order: S^T(0), dK(0),
+// two softmax warpgroups (64 of the 128 query columns each, P^T packed over
+// the first half of their own columns) form P^T of contribution j while the
+// tensor core runs dV(j-1), dK(j) and S^T(j+1).  Product order: S^T(0), dK(0),
 // S^T(1), then per j: dV(j), dK(j+1), S^T(j+2) -- a Q/dS stage is released
 // by its dK product three products before the S^T that reuses it, a dO stage
 // by its dV five before.  The Q tile is read as the K-major B operand of
@@ -1623,7 +1673,7 @@ attn_bwd_dkdv_ds128_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       mbar_init(do_full + b, 1);
       mbar_init(do_empty + b, 1);
       mbar_init(s_full + b, 1);
-      mbar_init(p_full + b, 128);
+      mbar_init(p_full + b, 256);
     }
     mbar_init(acc_done, 1);
     *abort_flag = 0;
@@ -1734,8 +1784,8 @@ attn_bwd_dkdv_ds128_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
           ok = mbar_wait(do_full + b, (j >> 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          mma_tn<BN, D>(tmem + Cfg::T_DV, tmem + b * BN, smem_desc_sw128(do0 + b * Cfg::DO_BYTES, BN * 128, 1024),
-                        j > 0);
+          mma_tn_split<BN, D, true>(tmem + Cfg::T_DV, tmem + b * BN,
+                                    smem_desc_sw128(do0 + b * Cfg::DO_BYTES, BN * 128, 1024), j > 0);
           umma_commit(do_empty + b);
           if (j + 1 < n) issue_dk(j + 1);
           if (j + 2 < n) ok = issue_s(j + 2);       // into buffer b, after dV(j) has read P^T there
@@ -1750,69 +1800,67 @@ attn_bwd_dkdv_ds128_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
       mbar_wait(acc_done, 0, &never, 200000000ull);
     }
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax: P^T of contributions j % 2 == wg
+    // ------------------------------------------------------------ softmax: P^T, warpgroup w columns 64w..64w+63
     const int wg = (warp - 4) >> 2;
     const int row = ((warp & 3) << 5) + lane;        // key row of the tile
     const uint32_t t0 = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const int c_first = 2 * wg;                      // this warpgroup's two 32-column chunks
     const int k_pos = k_lo + row;
     const bool k_valid = k_pos < k_valid_hi;
     const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2);
     KvIter<BN> itr = itr0;
     bool ok = true;
     for (int j = 0; !itr.done; ++j, itr.next()) {
-      if ((j & 1) != wg) continue;
-      const uint32_t tb = t0 + wg * BN;
-      // -LSE (log2 units) of the contribution's query columns: lane l holds
-      // columns 2l, 2l+1 (lo) and 64+2l, 64+2l+1 (hi), handed out by shuffles
-      uint64_t lse_lo, lse_hi;
-      {
-        const int q0 = itr.q0();
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int col = (e >> 1) * 64 + 2 * lane + (e & 1);
-          v[e] = 0.f;
-          if (q0 + col < itr.q_valid_hi)
-            v[e] = -__ldg(p.lse + thd_row(si.start + q0 + col, itr.head(), p.hpg_q, p.T)) * kLog2e;
-        }
-        lse_lo = f32x2(v[0], v[1]);
-        lse_hi = f32x2(v[2], v[3]);
-      }
+      const int b = j & 1;
+      const uint32_t tb = t0 + b * BN;
+      // -LSE (log2 units) of the warpgroup's query columns: lane l holds
+      // columns 64w + 2l and 64w + 2l + 1, handed out by shuffles
       const int q0 = itr.q0();
+      uint64_t lse2;
+      {
+        const int col = c_first * 32 + 2 * lane;
+        float v0 = 0.f, v1 = 0.f;
+        if (q0 + col < itr.q_valid_hi)
+          v0 = -__ldg(p.lse + thd_row(si.start + q0 + col, itr.head(), p.hpg_q, p.T)) * kLog2e;
+        if (q0 + col + 1 < itr.q_valid_hi)
+          v1 = -__ldg(p.lse + thd_row(si.start + q0 + col + 1, itr.head(), p.hpg_q, p.T)) * kLog2e;
+        lse2 = f32x2(v0, v1);
+      }
       // query column c is visible to this key row iff q0+c >= k_pos and q0+c < q_valid_hi
       const int c_lo = k_valid ? max(0, k_pos - q0) : BN;
       const int c_hi = k_valid ? itr.q_valid_hi - q0 : 0;
       const bool masked = __any_sync(0xffffffffu, c_lo > 0 || c_hi < BN);
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full + wg, (j >> 1) & 1, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      uint32_t rs[32];
+      uint32_t rs[2][32];
+      tmem_ld32(tb + c_first * 32, rs[0]);
+      tmem_ld32(tb + c_first * 32 + 32, rs[1]);
+      tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        tmem_ld32(tb + c * 32, rs);
-        tmem_wait_ld();
+      for (int h = 0; h < 2; ++h) {
+        const int c = c_first + h;
         if (masked) {
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
             const int col = c * 32 + x;
-            rs[x] = (col >= c_lo && col < c_hi) ? rs[x] : 0xff800000u;
+            rs[h][x] = (col >= c_lo && col < c_hi) ? rs[h][x] : 0xff800000u;
           }
         }
         uint32_t pk[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-          // columns c*32 + 2x, +1: held by lane (16c + x) % 32, in lo (c < 2) or hi
-          const uint64_t nl = __shfl_sync(0xffffffffu, c < 2 ? lse_lo : lse_hi, (16 * c + x) & 31);
+          const uint64_t nl = __shfl_sync(0xffffffffu, lse2, h * 16 + x);
           float a0, a1;
-          f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[2 * x]), __uint_as_float(rs[2 * x + 1])), scale2, nl),
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(rs[h][2 * x]), __uint_as_float(rs[h][2 * x + 1])), scale2, nl),
                       a0, a1);
           pk[x] = pack_bf16x2(ex2_approx(a0), ex2_approx(a1));
         }
-        tmem_st16(tb + c * 16, pk);                 // P^T packed over the buffer's first 64 columns
+        tmem_st16(tb + c_first * 32 + h * 16, pk);  // in place, over the warpgroup's own first 32 columns
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full + wg);
+      mbar_arrive(p_full + b);
     }
     if (ok && any) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
     if (!ok) {
@@ -2237,7 +2285,7 @@ cudaError_t launch_dv256(const CUtensorMap* m, const BwdParams& p, int grid_item
 // Tile shapes.  D = 128: whole streamed tiles, dK and dV in one kernel.
 // D = 256: the dQ and dK passes (attn_bwd_half_kernel) and the dV pass
 // (attn_bwd_dv256_kernel) stream 128-column halves of 128-row tiles.
-using Dq128 = DqCfg<128, 128, 5, 1>;
+using Dq128 = DqCfg<128, 128, 5, 1, true>;
 using Kv128 = KvCfg<128, 128, 4, 1>;
 
 }  // namespace
