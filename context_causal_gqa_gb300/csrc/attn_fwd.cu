@@ -67,8 +67,11 @@ struct FwdCfg {
   // segment's O rows (128 columns, 256 B a row), so that O can be released
   // to the next segment's first P V product before the global stores of
   // the partial are issued
-  static constexpr bool STAGE = (D == 256 && NH == 1);
-  static constexpr int STAGE_BYTES = STAGE ? kBM * (D / 2) * 2 : 0;
+  // D=128, two heads: each head's finished O leaves through its own 16 KB
+  // box (64 columns x 128 rows, TMA stores), one K/V slot fewer
+  static constexpr bool STAGE = (D == 256 && NH == 1) || (D == 128 && NH == 2);
+  static constexpr int BOX_BYTES = kBM * 128;
+  static constexpr int STAGE_BYTES = (D == 256 && NH == 1) ? kBM * (D / 2) * 2 : (STAGE ? NH * BOX_BYTES : 0);
   // K and V tiles stream through NSLOT slots in the order the MMA warp
   // consumes them (per item: K_0..K_{LA-1}, then K_{j+LA} and V_j for
   // j = 0, 1, ...); a slot is released when its S or P V product is done.
@@ -76,7 +79,8 @@ struct FwdCfg {
   // softmax(t) runs and V_{t+1} while S(t+2) and softmax(t+1) run.  A pair
   // holds four half-tile slots in each CTA: V_t loads as soon as P V of tile
   // t-2 is done, K_{t+1} as soon as S(t-1) is.
-  static constexpr int NSLOT = (227 * 1024 - 2048 - NH * Q_BYTES - (PAIR ? STAGE_BYTES : 0)) / SLOT_BYTES;
+  static constexpr int NSLOT =
+      (227 * 1024 - 2048 - NH * Q_BYTES - ((D == 256 && NH == 1 && !PAIR) ? 0 : STAGE_BYTES)) / SLOT_BYTES;
   static constexpr int SMEM_Q = 0;
   static constexpr int SMEM_KV = SMEM_Q + NH * Q_BYTES;
   static constexpr int SMEM_STAGE = SMEM_KV + NSLOT * SLOT_BYTES;
@@ -567,7 +571,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // store issued by one thread; the two boxes alternate, so the
             // softmax threads never wait on global stores, only (rarely) on a
             // box's previous store having read it.
-            const bool issuer = warp == 4 && lane == 0;
+            const bool issuer = warp == 4 + 4 * h && lane == 0;
             uint8_t* sbox = smem + Cfg::SMEM_STAGE;
             const int grow = static_cast<int>(((h0 + h) / p.hpg_q) * p.T) + ir.seq_start + ir.q_lo;
             const int hc = (h0 + h) % p.hpg_q;
@@ -575,9 +579,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int swz = row & 7;
 #pragma unroll 1
             for (int qq = 0; qq < D / 64; ++qq) {
-              uint8_t* box = sbox + (qq & 1) * (kBM * 128);
-              if (issuer) bulk_wait_group_read<1>();    // the box's previous store has read it
-              named_bar_sync(1, 128);
+              // D=256: two boxes, alternating; D=128: the head's own box
+              uint8_t* box = sbox + (NH == 2 ? h : (qq & 1)) * Cfg::BOX_BYTES;
+              if (issuer) {                             // the box's previous store has read it
+                if constexpr (NH == 2) bulk_wait_group_read<0>();
+                else bulk_wait_group_read<1>();
+              }
+              named_bar_sync(1 + h, 128);
               uint32_t r0[32], r1[32];
               tmem_ld32(t_o + qq * 64, r0);
               tmem_ld32(t_o + qq * 64 + 32, r1);
@@ -598,7 +606,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 brow[j ^ swz] = w4;
               }
               fence_proxy_async_smem();
-              named_bar_sync(1, 128);
+              named_bar_sync(1 + h, 128);
               if (issuer) {
                 tma_store_4d(&tm_o, box, qq * 64, hc, grow, slab_c);
                 bulk_commit_group();
@@ -607,8 +615,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (valid) p.lse[slab * p.lse_slab + orow] = (mseg + __log2f(lseg)) * kLn2;
             return true;
           }
-          // (a partial tile) the staging area is free once the TMA stores of
-          // earlier whole tiles have read it
+          // (a partial tile, D=256) the staging area is free once the TMA
+          // stores of earlier whole tiles have read it; D=128 partial tiles
+          // take the plain row stores below
+          if constexpr (D == 256) {
           if (warp == 4 && lane == 0) bulk_wait_group_read<0>();
           named_bar_sync(1, 128);
           // Each half of the row (128 columns) goes from TMEM to this thread's
@@ -663,6 +673,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           store_half(D / 2);
           if (valid) p.lse[slab * p.lse_slab + orow] = (mseg + __log2f(lseg)) * kLn2;
           return true;
+          }
         }
         uint32_t r[32];
 #pragma unroll 1
@@ -838,7 +849,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       *abort_flag = 1;
     }
     // the TMA stores of O have read their boxes and written global memory
-    if (Cfg::STAGE && warp == 4 && lane == 0) bulk_wait_group<0>();
+    if (Cfg::STAGE && (warp & 3) == 0 && lane == 0) bulk_wait_group<0>();
   }
   tc_fence_before();
   __syncwarp();
