@@ -194,7 +194,9 @@ ccg_status ccg_attn_bwd(const ccg_attn_desc* desc, const void* q, const void* k,
  * request the rest of this header follows.
  *   Limit: ccg_workspace_size(desc, 1) must be at most 16,776,960 bytes
  *   (16 MiB - 256); larger problems return CCG_ERR_WORKSPACE and launch
- *   nothing.  The library itself allocates nothing here (no cudaMalloc,
+ *   nothing.  A padded-length bound (max_seqlen > 0) adds the dS tiles to
+ *   the workspace and exceeds the scratch for all but the smallest
+ *   problems: pass max_seqlen = 0 (the backward that recomputes dS) here.  The library itself allocates nothing here (no cudaMalloc,
  *   no cudaFree).
  *   d_status: the caller's status word, as in ccg_attn_bwd; NULL selects a
  *   status word inside the fixed scratch that is cleared at the start of

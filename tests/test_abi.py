@@ -97,6 +97,13 @@ def test_host_side_rejections_need_no_gpu(L):
                           ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1000), None) == 2   # H % cp
     big = _desc(hq=32, hkv=8, total_tokens=1 << 20, cp=1)
     assert L.ccg_attn_bwd_noalloc(ctypes.byref(big), *([null] * 12), null) == 4
+    # a padded-length bound adds the dS tiles to the workspace: a problem that
+    # fits the allocation-free entry point's fixed scratch then exceeds it
+    seq = _desc(hq=4, hkv=1, total_tokens=8192, cp=1)
+    assert ccg.workspace_size(seq, True) < (1 << 24) - 256      # fits without the bound
+    seq.max_seqlen = 8192
+    assert ccg.workspace_size(seq, True) > (1 << 24)             # ~100 MB of dS tiles with it
+    assert L.ccg_attn_bwd_noalloc(ctypes.byref(seq), *([null] * 12), null) == 4
 
 
 def test_head_parts_shrink_the_forward_workspace_and_are_validated(L):
