@@ -269,7 +269,8 @@ def bench_config(w, args, world):
     cfg["schedule"] = args.schedule
     fused = args.fwd == "fused" or args.schedule == "a2a"
     cfg["forward"] = "fused online softmax" if fused else "ring-step partials + LSE merge"
-    cfg["backward"] = ("dQ pass keeps dS, dK pass reads it back (D=256)" if getattr(args, "bwd", "") == "keep-ds"
+    cfg["backward"] = ("dQ pass keeps dS (and P at D=256), dK/dV passes read them back"
+                       if getattr(args, "bwd", "") == "keep-ds"
                        else "dK pass recomputes S^T and dP^T")
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "1 GPU, CP emulated"
     return cfg
@@ -492,8 +493,8 @@ def main():
     ap.add_argument("--fwd", default="partials", choices=["partials", "fused"],
                     help="partials: ring-step partials + LSE merge (the measured path); fused: one online softmax")
     ap.add_argument("--bwd", default="keep-ds", choices=["keep-ds", "recompute"],
-                    help="keep-ds (the measured path): the D=256 backward keeps dS (the dQ pass writes it, the dK "
-                         "pass reads it back); recompute: the dK pass recomputes S^T and dP^T")
+                    help="keep-ds (the measured path): the backward keeps dS, and at D=256 P (the dQ pass writes "
+                         "them, the dK/dV passes read them back); recompute: the dK/dV passes recompute S^T and dP^T")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-d128", action="store_true", help="skip the D=128 companion measurement")
