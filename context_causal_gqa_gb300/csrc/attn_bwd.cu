@@ -20,9 +20,17 @@
 //   stream through the slots.  Per contribution: S^T = K Q^T, dP^T = V dO^T,
 //   P^T and dS^T in registers -> TMEM (BF16), dV += P^T dO, dK += dS^T Q.
 // At D = 256 the two 256-column FP32 accumulators alone fill TMEM, so the
-// dK/dV pass runs as two kernels (dV, then dK), and every D = 256 kernel
-// streams its 128-row tiles as two 128-column halves, so that every product
-// runs at full width next to the resident tiles in shared memory.
+// recomputing dK/dV pass runs as two kernels (dV, then dK), and every D = 256
+// kernel streams its 128-row tiles as two 128-column halves, so that every
+// product runs at full width next to the resident tiles in shared memory.
+//
+// The backward that keeps dS (a padded-length bound in the descriptor) takes
+// one kv head's GQA group at a time: its dQ pass also stores every unit's
+// BF16 dS tile (and at D = 256 its P tile) in the workspace, and the dK/dV
+// passes read them back instead of recomputing dP^T (and at D = 256 S^T):
+// D = 256 one product per unit each for dK and dV, on CTA pairs
+// (attn_bwd_dkv_pair_kernel); D = 128 one pass recomputing only P^T
+// (attn_bwd_dkdv_ds128_kernel).
 #include <cuda_bf16.h>
 
 #include <type_traits>
