@@ -163,7 +163,7 @@ def attn_bwd(q, k, v, o, do, lse, cu_seqlens, cu_seqlens_padded, cp, *, head_gro
              dq=None, dk=None, dv=None, workspace=None, status=None, stream=None, check=True, max_seqlen=0):
     """Backward: returns (dq, dk, dv).  q, k, v, do may be row-strided views; o and the
     gradients are dense.  max_seqlen > 0: a bound on every padded sequence length,
-    which at D = 256 selects the backward that keeps dS (a larger workspace)."""
+    which selects the backward that keeps dS, and at D = 256 P (a larger workspace)."""
     import torch
     desc = _desc_for(q, k, cu_seqlens, cp, head_groups, scale, v=v, do=do, max_seqlen=max_seqlen)
     dense = lambda t: torch.empty(t.shape, dtype=t.dtype, device=t.device)  # noqa: E731

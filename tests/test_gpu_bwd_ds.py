@@ -120,3 +120,27 @@ def test_ds_backward_broken_bound_is_reported_and_writes_nothing(lib):
     assert "SEQLENS" in str(e.value)
     for t in outs:
         assert torch.all(t == 7.0)
+
+
+@pytest.mark.parametrize("D", [256, 128])
+def test_ds_backward_head_split_layout_equals_plain(lib, D):
+    """The head-split layout (head_groups = CP, the large workloads' A2A
+    layout) gives the same gradients, bit for bit, as the plain layout."""
+    w = W.custom_workload(f"ds_hs_d{D}", [2048, 1280], 8, 4, D, 4, pad_to=8)   # 2 KV tiles a chunk
+    x = W.make_inputs(w, device="cuda")
+    T, hg = w.total_tokens, w.cp
+    o, lse = _fwd(lib, x, w)
+    g1 = _bwd(lib, x, w, o, lse, _bound(w))
+
+    def split(t):
+        return t.view(T, hg, t.shape[1] // hg, t.shape[2]).transpose(0, 1).contiguous()
+
+    def join(t, heads):
+        return t.transpose(0, 1).reshape(T, heads, t.shape[3])
+
+    q, k, v, do = (split(x[n]) for n in ("q", "k", "v", "do"))
+    o2, lse2 = lib.attn_fwd(q, k, v, x["cu_seqlens"], x["cu_seqlens_padded"], w.cp, head_groups=hg)
+    g2 = lib.attn_bwd(q, k, v, o2, do, lse2, x["cu_seqlens"], x["cu_seqlens_padded"], w.cp, head_groups=hg,
+                      max_seqlen=_bound(w))
+    for a, b, heads in zip(g1, g2, (w.hq, w.hkv, w.hkv)):
+        assert torch.equal(a, join(b, heads))
