@@ -108,10 +108,16 @@ struct DqCfg {
   static constexpr int SMEM_BAR = SMEM_SLOT + NSLOT * SLOT_BYTES;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
   static constexpr int T_BUF = 2 * BN;           // buffer b: S at b*T_BUF, dP at b*T_BUF + BN
-  // SDB (split columns only): two S buffers (S of tile j at (j % 2) * BN), one
-  // dP buffer at 2 * BN with dS packed over each warpgroup's own dP columns,
-  // so that S of tile j+1 is computed while the softmax forms dS of tile j
+  // SDB (split columns only): two S buffers (S of tile j at (j % 2) * BN) with
+  // dS packed over each warpgroup's own S columns, and one dP buffer at 2 * BN
+  // that the softmax releases as soon as it has loaded dP of tile j: dP of
+  // tile j+1 is computed while the softmax forms dS of tile j, and S of tile
+  // j+2 right after dQ of tile j.  The slots form two rings, NK for K (held
+  // from S(j) to dQ(j)) and NV for V (held for dP(j) only), so that each
+  // ring's slots are released in the order they are loaded.
   static constexpr bool SDB = SDB_;
+  static constexpr int NV = SDB ? 2 : 0;
+  static constexpr int NK = NSLOT - NV;
   static constexpr int T_DP = 2 * BN;
   static constexpr int T_ACC = SDB ? 3 * BN : NBUF * T_BUF;
   // dS (BF16, the A operand of dQ += dS K): packed in place over S when one
@@ -403,7 +409,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   uint64_t* s_full = empty + NSLOT;       // [2]
   uint64_t* ds_full = s_full + 2;         // [2]
   uint64_t* acc_done = ds_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
+  uint64_t* dp_free = acc_done + 1;       // SDB: the softmax has loaded dP of the tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dp_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -427,6 +434,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_init(ds_full + b, Cfg::SPLIT ? 256 : 128);
     }
     mbar_init(acc_done, 1);
+    mbar_init(dp_free, 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -455,12 +463,15 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                       res_full);
         }
         // stream order per KV tile: V_j (released after dP) then K_j (released
-        // after dQ); SDB: K_j (for S, issued a tile ahead) then V_j
+        // after dQ), through one ring of NSLOT slots; SDB: K_j (for S, issued
+        // two tiles ahead) then V_j, K_j through the K ring, V_j the V ring
         for (int t = 0; !itr.done && ok; ++t) {
-          const int slot = t % NSLOT;
-          if (t >= NSLOT) ok = mbar_wait(empty + slot, ((t / NSLOT) - 1) & 1, abort_flag);
-          if (!ok) break;
           const bool is_v = Cfg::SDB ? (t & 1) == 1 : (t & 1) == 0;
+          const int pos = Cfg::SDB ? t >> 1 : t;             // position in its ring
+          const int ring = Cfg::SDB ? (is_v ? Cfg::NV : Cfg::NK) : NSLOT;
+          const int slot = (Cfg::SDB && is_v ? Cfg::NK : 0) + pos % ring;
+          if (pos >= ring) ok = mbar_wait(empty + slot, ((pos / ring) - 1) & 1, abort_flag);
+          if (!ok) break;
           const int k0 = itr.k0();
           mbar_arrive_expect_tx(full + slot, Cfg::SLOT_BYTES);
           uint8_t* dst = smem + Cfg::SMEM_SLOT + slot * Cfg::SLOT_BYTES;
@@ -476,7 +487,12 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         volatile int never = 0;
         mbar_wait(res_full, 0, &never, 200000000ull);
-        wait_last_copies(full, NSLOT, n_loads);
+        if constexpr (Cfg::SDB) {
+          wait_last_copies(full, Cfg::NK, (n_loads + 1) / 2);
+          wait_last_copies(full + Cfg::NK, Cfg::NV, n_loads / 2);
+        } else {
+          wait_last_copies(full, NSLOT, n_loads);
+        }
       }
     }
   } else if (warp == 1) {
@@ -516,21 +532,23 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           return true;
         };
         if constexpr (Cfg::SDB) {
-          // S(j) into S buffer j % 2 from K_j (slot 2j), dP(j) from V_j (slot
-          // 2j+1); the softmax of tile j starts once both are complete.
-          // Order: S(0), dP(0), S(1), then per j: dQ(j), dP(j+1), S(j+2)
+          // S(j) into S buffer j % 2 from K_j (K ring), dP(j) from V_j (V
+          // ring); the softmax of tile j starts once both are complete.
+          // Order: S(0), dP(0), S(1), then per j: dP(j+1) (once the softmax
+          // has loaded dP(j)), dQ(j) (once dS(j) is packed over S(j)), S(j+2)
+          // (into S buffer j % 2, after dQ(j) has read dS(j) there)
           int n = 0;
           for (DqIter<BN> c2 = ahead; !c2.done; c2.next()) ++n;
           auto issue_s = [&](int jj) -> bool {
-            const int t = 2 * jj, sl = t % NSLOT;
-            if (!mbar_wait(full + sl, (t / NSLOT) & 1, abort_flag)) return false;
+            const int sl = jj % Cfg::NK;
+            if (!mbar_wait(full + sl, (jj / Cfg::NK) & 1, abort_flag)) return false;
             tc_fence_after();
             mma_kk<BM, BN, D>(tmem + (jj & 1) * BN, q_desc, slot_k(sl));
             return true;
           };
           auto issue_dp = [&](int jj) -> bool {
-            const int t = 2 * jj + 1, sl = t % NSLOT;
-            if (!mbar_wait(full + sl, (t / NSLOT) & 1, abort_flag)) return false;
+            const int sl = Cfg::NK + jj % Cfg::NV;
+            if (!mbar_wait(full + sl, (jj / Cfg::NV) & 1, abort_flag)) return false;
             tc_fence_after();
             mma_kk<BM, BN, D>(tmem + Cfg::T_DP, do_desc, slot_k(sl));
             umma_commit(empty + sl);                  // V_jj done
@@ -540,14 +558,20 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           if (ok && n > 0) ok = issue_s(0) && issue_dp(0);
           if (ok && n > 1) ok = issue_s(1);
           for (int j = 0; ok && j < n; ++j) {
+            if (j + 1 < n) {
+              ok = mbar_wait(dp_free, j & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              ok = issue_dp(j + 1);
+              if (!ok) break;
+            }
             ok = mbar_wait(ds_full, j & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            const int sk = (2 * j) % NSLOT;
-            mma_tn_split<BN, D, true>(tmem + Cfg::T_ACC, tmem + Cfg::T_DP, slot_mn(sk), j > 0);
+            const int sk = j % Cfg::NK;
+            mma_tn_split<BN, D, true>(tmem + Cfg::T_ACC, tmem + (j & 1) * BN, slot_mn(sk), j > 0);
             umma_commit(empty + sk);                  // K_j done
-            if (j + 1 < n) ok = issue_dp(j + 1);      // over dS(j), after dQ(j) read it
-            if (ok && j + 2 < n) ok = issue_s(j + 2); // into S buffer j % 2, read by softmax(j)
+            if (j + 2 < n) ok = issue_s(j + 2);
           }
         }
         int j_sp = 0;
@@ -620,11 +644,32 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       // scores become -inf in registers, so P (and dS) come out exactly 0
       const bool masked = __any_sync(0xffffffffu, nvalid < BN);
       uint32_t rs[32], rp[32];
+      uint32_t rp2[Cfg::SDB ? 32 : 1];                  // SDB: dP of the second chunk
+      if constexpr (Cfg::SDB) {
+        // dP of both chunks (and S of the first) first, then release the dP
+        // buffer for the next tile's dP product
+        static_assert(NC == 2, "two 32-column chunks a warpgroup");
+        tmem_ld32(tdp + c_first * 32, rp);
+        tmem_ld32(tdp + (c_first + 1) * 32, rp2);
+        tmem_ld32(ts + c_first * 32, rs);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(dp_free);
+      }
 #pragma unroll
       for (int c = c_first; c < c_first + NC; ++c) {
-        tmem_ld32(ts + c * 32, rs);
-        tmem_ld32(tdp + c * 32, rp);
-        tmem_wait_ld();
+        if constexpr (Cfg::SDB) {
+          if (c != c_first) {
+            tmem_ld32(ts + c * 32, rs);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) rp[x] = rp2[x];
+            tmem_wait_ld();
+          }
+        } else {
+          tmem_ld32(ts + c * 32, rs);
+          tmem_ld32(tdp + c * 32, rp);
+          tmem_wait_ld();
+        }
         if (masked) {
 #pragma unroll
           for (int x = 0; x < 32; ++x) rs[x] = (c * 32 + x < nvalid) ? rs[x] : 0xff800000u;
@@ -644,7 +689,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           pk[x] = pack_bf16x2(d0, d1);
         }
         if constexpr (Cfg::SDB)
-          tmem_st16(tdp + c_first * 32 + (c - c_first) * 16, pk);   // over the warpgroup's own dP columns
+          tmem_st16(ts + c_first * 32 + (c - c_first) * 16, pk);    // over the warpgroup's own S columns
         else
           tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_A : tb) + c * 16, pk);
         if (ds_tile != nullptr) {
