@@ -56,10 +56,10 @@ struct FwdCfg {
   static constexpr int KCH = D / 64;                       // 64-wide (128-byte) column chunks
   static constexpr int Q_BYTES = kBM * D * 2;              // one head
   static constexpr int KV_BYTES = BN * D * 2;              // one K (or V) tile
-  // A CTA pair (two q heads of one kv group, one per CTA, in M = 256
-  // products) holds half of every K tile in each CTA (BN/2 keys, all D
-  // columns: the N half of S = Q K^T) and half of every V tile (all BN keys,
-  // D/2 columns: the N half of O += P V).
+  // A CTA pair (2 NH q heads of one kv group, NH per CTA; head slot h of
+  // both CTAs in one M = 256 product) holds half of every K tile in each CTA
+  // (BN/2 keys, all D columns: the N half of S = Q K^T) and half of every V
+  // tile (all BN keys, D/2 columns: the N half of O += P V).
   static constexpr int SLOT_BYTES = PAIR ? KV_BYTES / 2 : KV_BYTES;
   static constexpr int K_ROWS = PAIR ? BN / 2 : BN;        // key rows of a K slot
   static constexpr int V_CH = PAIR ? KCH / 2 : KCH;        // 64-column chunks of a V slot
@@ -92,7 +92,7 @@ struct FwdCfg {
   static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : (TMEM_USED <= 256 ? 256 : 512);
   static constexpr int THREADS = 128 + 128 * NH;
   static_assert(NSLOT >= 2, "K and V slots");
-  static_assert(!PAIR || (D == 256 && NH == 1), "CTA pairs: D = 256, one head per CTA");
+  static_assert(!PAIR || (D == 256 && NH == 1) || (D == 128 && NH == 2), "CTA pairs: D = 256 x 1 or D = 128 x 2 heads");
   static_assert(BAR_WORDS * 8 + 8 + 4 * NH * SBUF <= 512, "barrier region");
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM budget");
@@ -209,10 +209,11 @@ __device__ __forceinline__ int count_tiles(const FwdParams& p, const WorkItem& i
   return n;
 }
 
-// PAIR: launched as (2,1,1) clusters; the two CTAs of a cluster take two q
-// heads of one kv group (heads 2i and 2i+1) of the same work item and run
-// every product as one M = 256 tcgen05 product issued by rank 0, each CTA
-// loading its half of every K and V tile (tm_k2: boxes of BN/2 key rows).
+// PAIR: launched as (2,1,1) clusters; the two CTAs of a cluster take 2 NH q
+// heads of one kv group (heads 2 NH i + NH rank + h) of the same work item and
+// run every product as one M = 256 tcgen05 product issued by rank 0 (head
+// slot h of both CTAs), each CTA loading its half of every K and V tile
+// (tm_k2: boxes of BN/2 key rows).
 // tm_o (D = 256): the output (partials) as (D, heads of a group, rows, step
 // slab), boxes of 64 columns x 128 rows, for the TMA stores of O.
 template <int D, int NH, bool PAIR>
@@ -223,8 +224,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   using Cfg = FwdCfg<D, NH, PAIR>;
   constexpr int BN = Cfg::BN, SBUF = Cfg::SBUF, NSLOT = Cfg::NSLOT, KCH = Cfg::KCH;
 
-  // PAIR: work unit w = (item, head pair); this CTA's head is 2 (w % nhg) + rank
-  const int nhg = p.hq / (PAIR ? 2 : NH);              // work units per item
+  // PAIR: work unit w = (item, 2 NH heads); this CTA's heads are
+  // 2 NH (w % nhg) + NH rank + h
+  const int nhg = p.hq / (PAIR ? 2 * NH : NH);         // work units per item
   const int64_t n_work = static_cast<int64_t>(p.hdr->n_fwd_all) * nhg;
   const int64_t w_first = PAIR ? blockIdx.x / 2 : blockIdx.x;
   const int64_t w_step = PAIR ? gridDim.x / 2 : gridDim.x;
@@ -232,8 +234,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // (a pair never returns on the status word: its two reads could differ)
   if (!PAIR && status_bad(p.status)) return;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  auto head_of = [&](int64_t w) { return PAIR ? static_cast<int>(w % nhg) * 2 + static_cast<int>(rank)
-                                              : static_cast<int>(w % nhg) * NH; };
+  auto head_of = [&](int64_t w) {
+    return PAIR ? static_cast<int>(w % nhg) * 2 * NH + static_cast<int>(rank) * NH : static_cast<int>(w % nhg) * NH;
+  };
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -316,7 +319,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // a pair counts both CTAs' copies on rank 0's q_full / kv_full, which
       // rank 0 alone arms with the bytes of both halves
       const bool arm = !PAIR || rank == 0;
-      constexpr uint32_t kArmQ = (PAIR ? 2 : NH) * Cfg::Q_BYTES;
+      constexpr uint32_t kArmQ = (PAIR ? 2 * NH : NH) * Cfg::Q_BYTES;
       constexpr uint32_t kArmKV = PAIR ? 2 * Cfg::SLOT_BYTES : Cfg::SLOT_BYTES;
       for (int64_t w = w_first; w < n_work && ok; w += w_step, ++item_k) {
         const WorkItem it = p.items[w / nhg];
@@ -919,9 +922,10 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
 
 int fwd_heads_per_cta(int D, int group) { return (D == 128 && group % 2 == 0) ? 2 : 1; }
 
-// D = 256 with an even q-head group: CTA pairs, two q heads of one kv group
-// sharing every K/V tile load (each CTA loads half of it)
-bool fwd_uses_pairs(int D, int group) { return D == 256 && group % 2 == 0; }
+// CTA pairs sharing every K/V tile load (each CTA loads half of it): D = 256
+// with an even q-head group (two heads a pair), D = 128 with a group of a
+// multiple of 4 (four heads a pair, two a CTA)
+bool fwd_uses_pairs(int D, int group) { return (D == 256 && group % 2 == 0) || (D == 128 && group % 4 == 0); }
 
 // Persistent launch over the combined work list: one CTA per SM (the work
 // count is only known on the device; CTAs with nothing to do exit at once).
@@ -949,6 +953,8 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
   p.T = T;
   p.scale_log2 = scale * 1.4426950408889634f;
   const int nh = fwd_heads_per_cta(D, hq / hkv);
+  if (D == 128 && nh == 2 && fwd_uses_pairs(D, hq / hkv))
+    return launch_fwd_impl<128, 2, true>(tq, tk, tk2, tv, to, p, num_sms, stream);
   if (D == 128 && nh == 2) return launch_fwd_impl<128, 2, false>(tq, tk, tk, tv, to, p, num_sms, stream);
   if (D == 128) return launch_fwd_impl<128, 1, false>(tq, tk, tk, tv, to, p, num_sms, stream);
   if (D == 256 && fwd_uses_pairs(D, hq / hkv))
