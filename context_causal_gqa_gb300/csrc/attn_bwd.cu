@@ -88,47 +88,38 @@ __device__ __forceinline__ int64_t ds_tile_index(const BwdParams& p, int b, int 
 // warpgroups: tile (or contribution) j is formed by warpgroup j % 2 in
 // buffer j % 2 while the tensor core computes the neighbouring tile, since
 // with the final LSE every tile's P is independent of the others.
-constexpr int kThreads = 384;    // warp 0 TMA, 1 MMA, 2 TMEM alloc, 3 idle, 4-11 two softmax warpgroups
+constexpr int kThreads = 384;    // warp 0 TMA, 1 MMA, 2 TMEM alloc, 3 idle (dQ pass: 1-3 MMA), 4-11 two softmax warpgroups
 
-template <int D, int BN_, int NSLOT_, int NBUF_, bool SDB_ = false>
+// dQ pass (D = 128).  TMEM: S of tile j in buffer j % 2 at (j % 2) * BN,
+// with dS packed over each softmax warpgroup's own S columns; dP at 2 BN,
+// released by the softmax as soon as it has loaded dP of tile j; the dQ
+// accumulator at 3 BN.  dP of tile j+1 is computed while the softmax forms
+// dS of tile j, S of tile j+2 once dQ of tile j has read dS(j).  The slots
+// form two rings, NK for K (held from S(j) to dQ(j)) and NV for V (held for
+// dP(j) only), so that each ring's slots are released in the order they are
+// loaded.  The three products are issued by three threads (warps 1, 2, 3):
+// one thread issues a tcgen05 product about every 100 cycles whatever its
+// width, so at N = 128 (64 cycles of tensor work) a single issuer leaves the
+// tensor core a third idle.
+template <int D, int BN_, int NSLOT_>
 struct DqCfg {
   static constexpr int BM = 128;                 // query rows (MMA M)
   static constexpr int BN = BN_;                 // key rows per tile (MMA N of S, K of dQ)
   static constexpr int NSLOT = NSLOT_;           // single-tile slots for K_j / V_j
-  // NBUF = 2: tiles alternate between two TMEM buffers and the two softmax
-  // warpgroups (the tensor core works on the next tile meanwhile); NBUF = 1:
-  // one buffer, both warpgroups split every tile's columns (for shapes whose
-  // shared memory leaves too few slots to keep two tiles in flight).
-  static constexpr int NBUF = NBUF_;
-  static constexpr bool SPLIT = NBUF == 1;
+  static constexpr int NV = 2;
+  static constexpr int NK = NSLOT - NV;
   static constexpr int RES_BYTES = BM * D * 2;   // Q or dO
   static constexpr int SLOT_BYTES = BN * D * 2;
   static constexpr int SMEM_RES = 0;
   static constexpr int SMEM_SLOT = 2 * RES_BYTES;
   static constexpr int SMEM_BAR = SMEM_SLOT + NSLOT * SLOT_BYTES;
   static constexpr int SMEM_TOTAL = SMEM_BAR + 256;
-  static constexpr int T_BUF = 2 * BN;           // buffer b: S at b*T_BUF, dP at b*T_BUF + BN
-  // SDB (split columns only): two S buffers (S of tile j at (j % 2) * BN) with
-  // dS packed over each warpgroup's own S columns, and one dP buffer at 2 * BN
-  // that the softmax releases as soon as it has loaded dP of tile j: dP of
-  // tile j+1 is computed while the softmax forms dS of tile j, and S of tile
-  // j+2 right after dQ of tile j.  The slots form two rings, NK for K (held
-  // from S(j) to dQ(j)) and NV for V (held for dP(j) only), so that each
-  // ring's slots are released in the order they are loaded.
-  static constexpr bool SDB = SDB_;
-  static constexpr int NV = SDB ? 2 : 0;
-  static constexpr int NK = NSLOT - NV;
   static constexpr int T_DP = 2 * BN;
-  static constexpr int T_ACC = SDB ? 3 * BN : NBUF * T_BUF;
-  // dS (BF16, the A operand of dQ += dS K): packed in place over S when one
-  // warpgroup owns the whole tile; with split columns it goes to its own
-  // region, since the other warpgroup may still be reading S there (SDB:
-  // over the warpgroup's own dP columns)
-  static constexpr int T_A = SPLIT && !SDB ? T_ACC + D : 0;   // 0: unused
+  static constexpr int T_ACC = 3 * BN;
   static constexpr int TMEM_COLS = 512;
-  static_assert(!SDB || (SPLIT && 3 * BN + D <= 512), "TMEM (SDB)");
-  static_assert(SDB || NBUF * 2 * BN + D + (SPLIT ? BN / 2 : 0) <= 512, "TMEM");
-  static_assert((SPLIT ? BN / 2 : BN) % 32 == 0, "softmax chunking");
+  static_assert(T_ACC + D <= TMEM_COLS, "TMEM");
+  static_assert(BN == 128, "two 32-column chunks of every tile per softmax warpgroup");
+  static_assert(NK >= 2, "K ring");
   static_assert(SMEM_TOTAL + 1024 <= 232448, "SMEM");
 };
 
@@ -394,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const BwdParams p) {
-  constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, KCH = D / 64;
+  constexpr int BM = Cfg::BM, BN = Cfg::BN, NSLOT = Cfg::NSLOT, NK = Cfg::NK, NV = Cfg::NV, KCH = D / 64;
   const int item_idx = blockIdx.x / p.nheads;
   if (item_idx >= p.hdr->n_dq) return;
   if (status_bad(p.status)) return;
@@ -402,15 +393,20 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  // Barriers indexed [2] are per S buffer: phase k of barrier b belongs to
+  // tile 2k + b, so that no waiter can see a phase complete twice.
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::SMEM_BAR);
   uint64_t* res_full = bars;
   uint64_t* full = bars + 1;              // [NSLOT]
   uint64_t* empty = full + NSLOT;         // [NSLOT]
-  uint64_t* s_full = empty + NSLOT;       // [2]
-  uint64_t* ds_full = s_full + 2;         // [2]
-  uint64_t* acc_done = ds_full + 2;
-  uint64_t* dp_free = acc_done + 1;       // SDB: the softmax has loaded dP of the tile
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dp_free + 1);
+  uint64_t* s_full = empty + NSLOT;       // [2] S(j) complete
+  uint64_t* ds_full = s_full + 2;         // [2] dS(j) packed (both warpgroups)
+  uint64_t* dq_done = ds_full + 2;        // [2] dQ(j) complete: S buffer j % 2 is free
+  uint64_t* dp_full = dq_done + 2;        // dP(j) complete
+  uint64_t* dp_free = dp_full + 1;        // the softmax has loaded dP(j)
+  uint64_t* acc_done = dp_free + 1;
+  uint64_t* drained = acc_done + 1;       // [2] warps 1 and 3: their products are complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drained + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -431,10 +427,14 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full + b, 1);
-      mbar_init(ds_full + b, Cfg::SPLIT ? 256 : 128);
+      mbar_init(ds_full + b, 256);
+      mbar_init(dq_done + b, 1);
     }
-    mbar_init(acc_done, 1);
+    mbar_init(dp_full, 1);
     mbar_init(dp_free, 256);
+    mbar_init(acc_done, 1);
+    mbar_init(drained + 0, 1);
+    mbar_init(drained + 1, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -452,7 +452,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (lane == 0) {
       DqIter<BN> itr;
       itr.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
-      int64_t n_loads = 0;                       // copies issued (slot = position % NSLOT)
+      int64_t n_loads = 0;                       // copies issued: K_j then V_j per tile
       bool ok = true;
       if (!itr.done) {
         const int row = static_cast<int>((h / p.hpg_q) * p.T) + si.start + q_lo;
@@ -462,24 +462,21 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tma_load_3d(smem + Cfg::SMEM_RES + Cfg::RES_BYTES + kc * BM * 128, &tm_do, kc * 64, h % p.hpg_q, row,
                       res_full);
         }
-        // stream order per KV tile: V_j (released after dP) then K_j (released
-        // after dQ), through one ring of NSLOT slots; SDB: K_j (for S, issued
-        // two tiles ahead) then V_j, K_j through the K ring, V_j the V ring
+        // K_j through the K ring (slots 0 .. NK-1), V_j through the V ring
         for (int t = 0; !itr.done && ok; ++t) {
-          const bool is_v = Cfg::SDB ? (t & 1) == 1 : (t & 1) == 0;
-          const int pos = Cfg::SDB ? t >> 1 : t;             // position in its ring
-          const int ring = Cfg::SDB ? (is_v ? Cfg::NV : Cfg::NK) : NSLOT;
-          const int slot = (Cfg::SDB && is_v ? Cfg::NK : 0) + pos % ring;
+          const bool is_v = (t & 1) == 1;
+          const int pos = t >> 1;                                  // tile j = position in its ring
+          const int ring = is_v ? NV : NK;
+          const int slot = (is_v ? NK : 0) + pos % ring;
           if (pos >= ring) ok = mbar_wait(empty + slot, ((pos / ring) - 1) & 1, abort_flag);
           if (!ok) break;
-          const int k0 = itr.k0();
           mbar_arrive_expect_tx(full + slot, Cfg::SLOT_BYTES);
           uint8_t* dst = smem + Cfg::SMEM_SLOT + slot * Cfg::SLOT_BYTES;
           for (int kc = 0; kc < KCH; ++kc)
-            tma_load_3d(dst + kc * BN * 128, is_v ? &tm_v : &tm_k, kc * 64, g % p.hpg_kv, kv_group_row + k0,
+            tma_load_3d(dst + kc * BN * 128, is_v ? &tm_v : &tm_k, kc * 64, g % p.hpg_kv, kv_group_row + itr.k0(),
                         full + slot);
           ++n_loads;
-          if (Cfg::SDB ? is_v : !is_v) itr.next();
+          if (is_v) itr.next();
         }
         if (!ok) {
           raise_status(p.status, CCG_ERR_TIMEOUT);
@@ -487,110 +484,73 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         volatile int never = 0;
         mbar_wait(res_full, 0, &never, 200000000ull);
-        if constexpr (Cfg::SDB) {
-          wait_last_copies(full, Cfg::NK, (n_loads + 1) / 2);
-          wait_last_copies(full + Cfg::NK, Cfg::NV, n_loads / 2);
-        } else {
-          wait_last_copies(full, NSLOT, n_loads);
-        }
+        wait_last_copies(full, NK, (n_loads + 1) / 2);
+        wait_last_copies(full + NK, NV, n_loads / 2);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp <= 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // warp 1: S(j) = Q K_j^T into S buffer j % 2, S(j+2) once dQ(j) is done;
+    // warp 3: dP(j) = dO V_j^T, dP(j+1) once the softmax has loaded dP(j);
+    // warp 2: dQ += dS(j) K_j once dS(j) is packed
     if (lane == 0) {
-      DqIter<BN> ahead;
-      ahead.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
+      DqIter<BN> cnt;
+      cnt.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
+      int n = 0;
+      for (; !cnt.done; cnt.next()) ++n;
       bool ok = true;
-      if (!ahead.done) {
+      if (n > 0) {
         const uint32_t q_base = smem_u32(smem + Cfg::SMEM_RES);
-        const uint64_t q_desc = smem_desc_sw128(q_base, 16, 1024);
-        const uint64_t do_desc = smem_desc_sw128(q_base + Cfg::RES_BYTES, 16, 1024);
         const uint32_t slot_base = smem_u32(smem + Cfg::SMEM_SLOT);
-        // slot s: K-major (S, dP) and MN-major (dQ) descriptors = base + s * SLOT_BYTES/16
-        const uint64_t slot_k0 = smem_desc_sw128(slot_base, 16, 1024);
-        const uint64_t slot_mn0 = smem_desc_sw128(slot_base, BN * 128, 1024);
         constexpr uint32_t kSlotStep = Cfg::SLOT_BYTES >> 4;
-        auto slot_k = [&](int s2) { return slot_k0 + s2 * kSlotStep; };
-        auto slot_mn = [&](int s2) { return slot_mn0 + s2 * kSlotStep; };
-        ok = mbar_wait(res_full, 0, abort_flag);
-        tc_fence_after();
-        // S and dP of tile j into buffer j % 2.  dP goes first: V_j is released
-        // right after it, so K_{j+1} (which reuses V_j's slot when slots are
-        // few) is loading for a whole tile before S of tile j+1 needs it.
-        auto issue_sp = [&](int j) -> bool {
-          const int tv = 2 * j, tk = 2 * j + 1;
-          const int sv = tv % NSLOT, sk = tk % NSLOT;
-          const int b = j % Cfg::NBUF;
-          const uint32_t buf = tmem + b * Cfg::T_BUF;
-          if (!mbar_wait(full + sv, (tv / NSLOT) & 1, abort_flag)) return false;
-          tc_fence_after();
-          mma_kk<BM, BN, D>(buf + BN, do_desc, slot_k(sv));
-          umma_commit(empty + sv);
-          if (!mbar_wait(full + sk, (tk / NSLOT) & 1, abort_flag)) return false;
-          tc_fence_after();
-          mma_kk<BM, BN, D>(buf, q_desc, slot_k(sk));
-          umma_commit(s_full + b);
-          return true;
-        };
-        if constexpr (Cfg::SDB) {
-          // S(j) into S buffer j % 2 from K_j (K ring), dP(j) from V_j (V
-          // ring); the softmax of tile j starts once both are complete.
-          // Order: S(0), dP(0), S(1), then per j: dP(j+1) (once the softmax
-          // has loaded dP(j)), dQ(j) (once dS(j) is packed over S(j)), S(j+2)
-          // (into S buffer j % 2, after dQ(j) has read dS(j) there)
-          int n = 0;
-          for (DqIter<BN> c2 = ahead; !c2.done; c2.next()) ++n;
-          auto issue_s = [&](int jj) -> bool {
-            const int sl = jj % Cfg::NK;
-            if (!mbar_wait(full + sl, (jj / Cfg::NK) & 1, abort_flag)) return false;
-            tc_fence_after();
-            mma_kk<BM, BN, D>(tmem + (jj & 1) * BN, q_desc, slot_k(sl));
-            return true;
-          };
-          auto issue_dp = [&](int jj) -> bool {
-            const int sl = Cfg::NK + jj % Cfg::NV;
-            if (!mbar_wait(full + sl, (jj / Cfg::NV) & 1, abort_flag)) return false;
-            tc_fence_after();
-            mma_kk<BM, BN, D>(tmem + Cfg::T_DP, do_desc, slot_k(sl));
-            umma_commit(empty + sl);                  // V_jj done
-            umma_commit(s_full);                      // S(jj) and dP(jj) complete
-            return true;
-          };
-          if (ok && n > 0) ok = issue_s(0) && issue_dp(0);
-          if (ok && n > 1) ok = issue_s(1);
+        if (warp == 2) {
+          // slot s: MN-major descriptor of K_j (the B operand of dQ += dS K_j)
+          const uint64_t slot_mn0 = smem_desc_sw128(slot_base, BN * 128, 1024);
           for (int j = 0; ok && j < n; ++j) {
-            if (j + 1 < n) {
-              ok = mbar_wait(dp_free, j & 1, abort_flag);
-              if (!ok) break;
-              tc_fence_after();
-              ok = issue_dp(j + 1);
-              if (!ok) break;
-            }
-            ok = mbar_wait(ds_full, j & 1, abort_flag);
+            ok = mbar_wait(ds_full + (j & 1), (j >> 1) & 1, abort_flag);
+            if (!ok) break;
+            // K_j has landed (warp 1 saw it; its slot is released only below)
+            const int sk = j % NK;
+            ok = mbar_wait(full + sk, (j / NK) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            const int sk = j % Cfg::NK;
-            mma_tn_split<BN, D, true>(tmem + Cfg::T_ACC, tmem + (j & 1) * BN, slot_mn(sk), j > 0);
+            mma_tn_split<BN, D, true>(tmem + Cfg::T_ACC, tmem + (j & 1) * BN, slot_mn0 + sk * kSlotStep, j > 0);
             umma_commit(empty + sk);                  // K_j done
-            if (j + 2 < n) ok = issue_s(j + 2);
+            umma_commit(dq_done + (j & 1));
           }
-        }
-        int j_sp = 0;
-        while (!Cfg::SDB && ok && !ahead.done && j_sp < Cfg::NBUF) {
-          ok = issue_sp(j_sp++);
-          ahead.next();
-        }
-        for (int j = 0; !Cfg::SDB && ok && j < j_sp; ++j) {
-          const int b = j % Cfg::NBUF;
-          ok = mbar_wait(ds_full + b, (j / Cfg::NBUF) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const int sk = (2 * j + 1) % NSLOT;
-          const uint32_t a_op = Cfg::SPLIT ? tmem + Cfg::T_A : tmem + b * Cfg::T_BUF;
-          mma_tn<BN, D>(tmem + Cfg::T_ACC, a_op, slot_mn(sk), j > 0);
-          umma_commit(empty + sk);
-          if (!ahead.done) {
-            ok = issue_sp(j_sp++);
-            ahead.next();
+        } else {
+          ok = mbar_wait(res_full, 0, abort_flag);
+          const uint64_t r_desc = smem_desc_sw128(q_base + (warp == 1 ? 0 : Cfg::RES_BYTES), 16, 1024);
+          const uint64_t slot_k0 = smem_desc_sw128(slot_base, 16, 1024);
+          for (int j = 0; ok && j < n; ++j) {
+            int sl;
+            uint32_t ph;
+            if (warp == 1) {
+              if (j >= 2) {
+                ok = mbar_wait(dq_done + (j & 1), ((j - 2) >> 1) & 1, abort_flag);
+                if (!ok) break;
+              }
+              sl = j % NK;
+              ph = (j / NK) & 1;
+            } else {
+              if (j >= 1) {
+                ok = mbar_wait(dp_free, (j - 1) & 1, abort_flag);
+                if (!ok) break;
+              }
+              sl = NK + j % NV;
+              ph = (j / NV) & 1;
+            }
+            ok = mbar_wait(full + sl, ph, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            if (warp == 1) {
+              mma_kk<BM, BN, D>(tmem + (j & 1) * BN, r_desc, slot_k0 + sl * kSlotStep);
+              umma_commit(s_full + (j & 1));
+            } else {
+              mma_kk<BM, BN, D>(tmem + Cfg::T_DP, r_desc, slot_k0 + sl * kSlotStep);
+              umma_commit(empty + sl);                // V_j done
+              umma_commit(dp_full);
+            }
           }
         }
       }
@@ -598,17 +558,22 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         raise_status(p.status, CCG_ERR_TIMEOUT);
         *abort_flag = 1;
       }
-      umma_commit(acc_done);
+      // a commit tracks only its own thread's products: each issuer waits for
+      // its own before the CTA may free TMEM (on the normal path the S and dP
+      // products are long complete: the softmax of tile n-1 read them)
+      uint64_t* own = warp == 2 ? acc_done : drained + (warp == 1 ? 0 : 1);
+      umma_commit(own);
       volatile int never = 0;
-      mbar_wait(acc_done, 0, &never, 200000000ull);
+      mbar_wait(own, 0, &never, 200000000ull);
     }
-  } else if (warp >= 4) {
-    const int wg = (warp - 4) >> 2;   // softmax warpgroup: tiles j % 2 == wg, or half the columns (SPLIT)
+  } else {
+    // ------------------------------------------------------------ softmax
+    // two warpgroups, each 64 of every tile's 128 columns
+    const int wg = (warp - 4) >> 2;
     const int row = ((warp & 3) << 5) + lane;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t0 = tmem + lane_base;
-    constexpr int NC = Cfg::SPLIT ? BN / 64 : BN / 32;   // 32-column chunks per warpgroup
-    const int c_first = Cfg::SPLIT ? wg * NC : 0;
+    const int c_first = 2 * wg;                       // its two 32-column chunks
     const int q_pos = q_lo + row;
     const bool row_valid = q_pos < q_valid_hi;
     const int64_t grow = thd_row(si.start + q_pos, h, p.hpg_q, p.T);
@@ -621,13 +586,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const bool any = !itr.done;
     bool ok = true;
     for (int j = 0; !itr.done; ++j, itr.next()) {
-      if (!Cfg::SPLIT && (j & 1) != wg) continue;
-      const int b = j % Cfg::NBUF;
-      const uint32_t tb = t0 + b * Cfg::T_BUF;
-      // SDB: S in buffer j % 2, dP in its own buffer
-      const uint32_t ts = Cfg::SDB ? t0 + (j & 1) * BN : tb;
-      const uint32_t tdp = Cfg::SDB ? t0 + Cfg::T_DP : tb + BN;
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full + b, (j / Cfg::NBUF) & 1, abort_flag));
+      const uint32_t ts = t0 + (j & 1) * BN;
+      const uint32_t tdp = t0 + Cfg::T_DP;
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full + (j & 1), (j >> 1) & 1, abort_flag) &&
+                                       mbar_wait(dp_full, j & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       const int k0 = itr.k0();
@@ -643,31 +605,21 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       // hidden keys only on tiles that cross a row's last visible key: their
       // scores become -inf in registers, so P (and dS) come out exactly 0
       const bool masked = __any_sync(0xffffffffu, nvalid < BN);
-      uint32_t rs[32], rp[32];
-      uint32_t rp2[Cfg::SDB ? 32 : 1];                  // SDB: dP of the second chunk
-      if constexpr (Cfg::SDB) {
-        // dP of both chunks (and S of the first) first, then release the dP
-        // buffer for the next tile's dP product
-        static_assert(NC == 2, "two 32-column chunks a warpgroup");
-        tmem_ld32(tdp + c_first * 32, rp);
-        tmem_ld32(tdp + (c_first + 1) * 32, rp2);
-        tmem_ld32(ts + c_first * 32, rs);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(dp_free);
-      }
+      // dP of both chunks (and S of the first) first, then release the dP
+      // buffer for the next tile's dP product
+      uint32_t rs[32], rp[32], rp2[32];
+      tmem_ld32(tdp + c_first * 32, rp);
+      tmem_ld32(tdp + (c_first + 1) * 32, rp2);
+      tmem_ld32(ts + c_first * 32, rs);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(dp_free);
 #pragma unroll
-      for (int c = c_first; c < c_first + NC; ++c) {
-        if constexpr (Cfg::SDB) {
-          if (c != c_first) {
-            tmem_ld32(ts + c * 32, rs);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) rp[x] = rp2[x];
-            tmem_wait_ld();
-          }
-        } else {
+      for (int c = c_first; c < c_first + 2; ++c) {
+        if (c != c_first) {
           tmem_ld32(ts + c * 32, rs);
-          tmem_ld32(tdp + c * 32, rp);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) rp[x] = rp2[x];
           tmem_wait_ld();
         }
         if (masked) {
@@ -688,10 +640,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           f32x2_split(mul_f32x2(pv, t), d0, d1);
           pk[x] = pack_bf16x2(d0, d1);
         }
-        if constexpr (Cfg::SDB)
-          tmem_st16(ts + c_first * 32 + (c - c_first) * 16, pk);    // over the warpgroup's own S columns
-        else
-          tmem_st16((Cfg::SPLIT ? t0 + Cfg::T_A : tb) + c * 16, pk);
+        tmem_st16(ts + c_first * 32 + (c - c_first) * 16, pk);     // over the warpgroup's own S columns
         if (ds_tile != nullptr) {
           // 16-byte pieces 4c .. 4c+3 of this row: a warp's store covers 32
           // consecutive rows of one piece (512 bytes)
@@ -702,7 +651,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(ds_full + b);
+      mbar_arrive(ds_full + (j & 1));
     }
     if (ok && any) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, abort_flag));
     if (!ok) {
@@ -2340,7 +2289,7 @@ cudaError_t launch_dv256(const CUtensorMap* m, const BwdParams& p, int grid_item
 // Tile shapes.  D = 128: whole streamed tiles, dK and dV in one kernel.
 // D = 256: the dQ and dK passes (attn_bwd_half_kernel) and the dV pass
 // (attn_bwd_dv256_kernel) stream 128-column halves of 128-row tiles.
-using Dq128 = DqCfg<128, 128, 5, 1, true>;
+using Dq128 = DqCfg<128, 128, 5>;
 using Kv128 = KvCfg<128, 128, 4, 1>;
 
 }  // namespace
