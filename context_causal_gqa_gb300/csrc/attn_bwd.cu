@@ -1604,10 +1604,14 @@ attn_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_
 // buffers (128 columns each) next to the dV and dK accumulators, so the
 // softmax warpgroup of contribution j (j % 2) forms P^T while the tensor
 // core runs dV(j-1), dK(j) and S^T(j+1) (both warpgroups splitting every
-// contribution's columns instead measured 5.4 against 5.2 ms a launch).  Product order: S^T(0), dK(0),
-// S^T(1), then per j: dV(j), dK(j+1), S^T(j+2) -- a Q/dS stage is released
-// by its dK product three products before the S^T that reuses it, a dO stage
-// by its dV five before.  The Q tile is read as the K-major B operand of
+// contribution's columns instead measured 5.4 against 5.2 ms a launch).  The
+// three products are issued by three threads, since one thread issues a
+// tcgen05 product only about every 100 cycles whatever its width (an N = 128
+// product is 64 cycles of tensor work): warp 1 S^T(j) (S^T(j+2) once dV(j)
+// has read P^T(j) from buffer j % 2), warp 2 dK(j) (as soon as its stage has
+// landed), warp 3 dV(j) (once P^T(j) is packed).  A Q/dS stage is released
+// when both its S^T and dK products are done, a dO stage by its dV.  The Q
+// tile is read as the K-major B operand of
 // S^T and as the MN-major B operand of dK; dS^T is read MN-major from the
 // unswizzled stored tile (core matrices 128 B apart along K, 2048 B along M).
 struct DkvDs128Cfg {
@@ -1655,7 +1659,8 @@ attn_bwd_dkdv_ds128_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
   uint64_t* do_empty = do_full + 2;       // [2]
   uint64_t* s_full = do_empty + 2;        // [2] S^T in buffer b
   uint64_t* p_full = s_full + 2;          // [2] P^T packed over buffer b
-  uint64_t* acc_done = p_full + 2;
+  uint64_t* dv_done = p_full + 2;         // [2] dV(j) complete: buffer j % 2 is free
+  uint64_t* acc_done = dv_done + 2;       // every issuer's products complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -1671,13 +1676,14 @@ attn_bwd_dkdv_ds128_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     mbar_init(res_full, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(qs_full + b, 1);
-      mbar_init(qs_empty + b, 1);
+      mbar_init(qs_empty + b, 2);                  // S^T and dK
       mbar_init(do_full + b, 1);
       mbar_init(do_empty + b, 1);
       mbar_init(s_full + b, 1);
       mbar_init(p_full + b, 128);
+      mbar_init(dv_done + b, 1);
     }
-    mbar_init(acc_done, 1);
+    mbar_init(acc_done, 3);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1741,62 +1747,70 @@ attn_bwd_dkdv_ds128_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         wait_last_copies(do_full, 2, n_do);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp <= 3) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       KvIter<BN> cnt = itr0;
       int n = 0;
       for (; !cnt.done; cnt.next()) ++n;
       bool ok = true;
       if (n > 0) {
-        const uint64_t k_desc = smem_desc_sw128(smem_u32(smem), 16, 1024);
         const uint32_t qs0 = smem_u32(smem + Cfg::SMEM_QS), do0 = smem_u32(smem + Cfg::SMEM_DO);
-        constexpr uint32_t idesc_dk = idesc_bf16_f32(BM, D, true, true);
-        ok = mbar_wait(res_full, 0, abort_flag);
-        tc_fence_after();
-        // S^T(j) = K Q_j^T into buffer j % 2 (the Q/dS stage is waited for here)
-        auto issue_s = [&](int j) -> bool {
-          const int st = j & 1;
-          if (!mbar_wait(qs_full + st, (j >> 1) & 1, abort_flag)) return false;
-          tc_fence_after();
-          mma_kk<BM, BN, D>(tmem + st * BN, k_desc, smem_desc_sw128(qs0 + st * Cfg::QS_BYTES, 16, 1024));
-          umma_commit(s_full + st);
-          return true;
-        };
-        // dK += dS_j^T Q_j (after S^T(j): the stage is already waited for)
-        auto issue_dk = [&](int j) {
-          const int st = j & 1;
-          const uint32_t base = qs0 + st * Cfg::QS_BYTES;
-          const uint64_t a_desc = smem_desc_noswz(base + Cfg::Q_BYTES, 128, 2048);
-          const uint64_t b_desc = smem_desc_sw128(base, BN * 128, 1024);
+        if (warp == 1) {
+          // S^T(j) = K Q_j^T into buffer j % 2
+          const uint64_t k_desc = smem_desc_sw128(smem_u32(smem), 16, 1024);
+          ok = mbar_wait(res_full, 0, abort_flag);
+          for (int j = 0; ok && j < n; ++j) {
+            const int st = j & 1;
+            if (j >= 2) {
+              ok = mbar_wait(dv_done + st, ((j - 2) >> 1) & 1, abort_flag);
+              if (!ok) break;
+            }
+            ok = mbar_wait(qs_full + st, (j >> 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            mma_kk<BM, BN, D>(tmem + st * BN, k_desc, smem_desc_sw128(qs0 + st * Cfg::QS_BYTES, 16, 1024));
+            umma_commit(s_full + st);
+            umma_commit(qs_empty + st);
+          }
+        } else if (warp == 2) {
+          // dK += dS_j^T Q_j
+          constexpr uint32_t idesc_dk = idesc_bf16_f32(BM, D, true, true);
+          for (int j = 0; ok && j < n; ++j) {
+            const int st = j & 1;
+            ok = mbar_wait(qs_full + st, (j >> 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t base = qs0 + st * Cfg::QS_BYTES;
+            const uint64_t a_desc = smem_desc_noswz(base + Cfg::Q_BYTES, 128, 2048);
+            const uint64_t b_desc = smem_desc_sw128(base, BN * 128, 1024);
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k)
-            umma_ss(tmem + Cfg::T_DK, a_desc + static_cast<uint64_t>(k * 16 * 16 >> 4), b_desc + mnmajor_step(k),
-                    idesc_dk, (j > 0 || k > 0) ? 1u : 0u);
-          umma_commit(qs_empty + st);
-        };
-        if (ok) ok = issue_s(0);
-        if (ok) issue_dk(0);
-        if (ok && n > 1) ok = issue_s(1);
-        for (int j = 0; ok && j < n; ++j) {
-          const int b = j & 1;
+            for (int k = 0; k < BN / 16; ++k)
+              umma_ss(tmem + Cfg::T_DK, a_desc + static_cast<uint64_t>(k * 16 * 16 >> 4), b_desc + mnmajor_step(k),
+                      idesc_dk, (j > 0 || k > 0) ? 1u : 0u);
+            umma_commit(qs_empty + st);
+          }
+        } else {
           // dV += P_j^T dO_j
-          ok = mbar_wait(p_full + b, (j >> 1) & 1, abort_flag);
-          if (!ok) break;
-          ok = mbar_wait(do_full + b, (j >> 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          mma_tn<BN, D>(tmem + Cfg::T_DV, tmem + b * BN, smem_desc_sw128(do0 + b * Cfg::DO_BYTES, BN * 128, 1024),
-                        j > 0);
-          umma_commit(do_empty + b);
-          if (j + 1 < n) issue_dk(j + 1);
-          if (j + 2 < n) ok = issue_s(j + 2);       // into buffer b, after dV(j) has read P^T there
+          for (int j = 0; ok && j < n; ++j) {
+            const int b = j & 1;
+            ok = mbar_wait(p_full + b, (j >> 1) & 1, abort_flag);
+            if (!ok) break;
+            ok = mbar_wait(do_full + b, (j >> 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            mma_tn<BN, D>(tmem + Cfg::T_DV, tmem + b * BN, smem_desc_sw128(do0 + b * Cfg::DO_BYTES, BN * 128, 1024),
+                          j > 0);
+            umma_commit(do_empty + b);
+            umma_commit(dv_done + b);
+          }
         }
       }
       if (!ok) {
         raise_status(p.status, CCG_ERR_TIMEOUT);
         *abort_flag = 1;
       }
+      // a commit tracks only its own thread's products: all three arrive
       umma_commit(acc_done);
       volatile int never = 0;
       mbar_wait(acc_done, 0, &never, 200000000ull);
