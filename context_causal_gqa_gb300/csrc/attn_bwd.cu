@@ -493,7 +493,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // warp 1: S(j) = Q K_j^T into S buffer j % 2, S(j+2) once dQ(j) is done;
     // warp 3: dP(j) = dO V_j^T, dP(j+1) once the softmax has loaded dP(j);
     // warp 2: dQ += dS(j) K_j once dS(j) is packed
-    if (lane == 0) {
+    // (each a whole warp, one elected lane issuing)
+    {
       DqIter<BN> cnt;
       cnt.init(p.cp, it.c, si.L, si.S, q_lo, q_valid_hi);
       int n = 0;
@@ -507,11 +508,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           // slot s: MN-major descriptor of K_j (the B operand of dQ += dS K_j)
           const uint64_t slot_mn0 = smem_desc_sw128(slot_base, BN * 128, 1024);
           for (int j = 0; ok && j < n; ++j) {
-            ok = mbar_wait(ds_full + (j & 1), (j >> 1) & 1, abort_flag);
+            ok = mbar_wait_warp(ds_full + (j & 1), (j >> 1) & 1, abort_flag);
             if (!ok) break;
             // K_j has landed (warp 1 saw it; its slot is released only below)
             const int sk = j % NK;
-            ok = mbar_wait(full + sk, (j / NK) & 1, abort_flag);
+            ok = mbar_wait_warp(full + sk, (j / NK) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             mma_tn_split<BN, D, true>(tmem + Cfg::T_ACC, tmem + (j & 1) * BN, slot_mn0 + sk * kSlotStep, j > 0);
@@ -519,7 +520,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             umma_commit(dq_done + (j & 1));
           }
         } else {
-          ok = mbar_wait(res_full, 0, abort_flag);
+          ok = mbar_wait_warp(res_full, 0, abort_flag);
           const uint64_t r_desc = smem_desc_sw128(q_base + (warp == 1 ? 0 : Cfg::RES_BYTES), 16, 1024);
           const uint64_t slot_k0 = smem_desc_sw128(slot_base, 16, 1024);
           for (int j = 0; ok && j < n; ++j) {
@@ -527,20 +528,20 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             uint32_t ph;
             if (warp == 1) {
               if (j >= 2) {
-                ok = mbar_wait(dq_done + (j & 1), ((j - 2) >> 1) & 1, abort_flag);
+                ok = mbar_wait_warp(dq_done + (j & 1), ((j - 2) >> 1) & 1, abort_flag);
                 if (!ok) break;
               }
               sl = j % NK;
               ph = (j / NK) & 1;
             } else {
               if (j >= 1) {
-                ok = mbar_wait(dp_free, (j - 1) & 1, abort_flag);
+                ok = mbar_wait_warp(dp_free, (j - 1) & 1, abort_flag);
                 if (!ok) break;
               }
               sl = NK + j % NV;
               ph = (j / NV) & 1;
             }
-            ok = mbar_wait(full + sl, ph, abort_flag);
+            ok = mbar_wait_warp(full + sl, ph, abort_flag);
             if (!ok) break;
             tc_fence_after();
             if (warp == 1) {
@@ -785,7 +786,7 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {   // the whole warp; one elected lane issues
       KvIter<BN> ahead;
       ahead.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
       bool ok = true;
@@ -799,7 +800,7 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         constexpr uint32_t kSlotStep = Cfg::SLOT_BYTES >> 4;
         auto slot_k = [&](int s2) { return slot_k0 + s2 * kSlotStep; };
         auto slot_mn = [&](int s2) { return slot_mn0 + s2 * kSlotStep; };
-        ok = mbar_wait(res_full, 0, abort_flag);
+        ok = mbar_wait_warp(res_full, 0, abort_flag);
         tc_fence_after();
         auto slot_q = [&](int j) { return 2 * j + 1; };
         auto slot_do = [&](int j) { return 2 * j; };
@@ -810,10 +811,10 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           const int b = j % Cfg::NBUF;
           const uint32_t buf = tmem + b * Cfg::T_BUF;
           // dP^T first (dO_i arrives first)
-          if (!mbar_wait(full + sdo, (tdo / NSLOT) & 1, abort_flag)) return false;
+          if (!mbar_wait_warp(full + sdo, (tdo / NSLOT) & 1, abort_flag)) return false;
           tc_fence_after();
           mma_kk<BM, BN, D>(buf + BN, v_desc, slot_k(sdo));
-          if (!mbar_wait(full + sq, (tq / NSLOT) & 1, abort_flag)) return false;
+          if (!mbar_wait_warp(full + sq, (tq / NSLOT) & 1, abort_flag)) return false;
           tc_fence_after();
           mma_kk<BM, BN, D>(buf, k_desc, slot_k(sq));
           umma_commit(s_full + b);
@@ -829,7 +830,7 @@ attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           const int sq = tq % NSLOT, sdo = tdo % NSLOT;
           const int b = j % Cfg::NBUF;
           const uint32_t buf = tmem + b * Cfg::T_BUF;
-          ok = mbar_wait(p_full + b, (j / Cfg::NBUF) & 1, abort_flag);
+          ok = mbar_wait_warp(p_full + b, (j / Cfg::NBUF) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           mma_tn_split<BN, D, Cfg::SPLIT>(tmem + Cfg::T_DV, buf, slot_mn(sdo), j > 0);
@@ -1160,7 +1161,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {   // the whole warp; one elected lane issues
       Iter ahead;
       iter_init(ahead);
       bool ok = true;
@@ -1174,20 +1175,20 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         constexpr uint32_t kSlotStep = Cfg::HALF_BYTES >> 4;
         auto slot_k = [&](int s2) { return slot_k0 + s2 * kSlotStep; };
         auto slot_mn = [&](int s2) { return slot_mn0 + s2 * kSlotStep; };
-        ok = mbar_wait(res_full, 0, abort_flag);
+        ok = mbar_wait_warp(res_full, 0, abort_flag);
         tc_fence_after();
         // dP (from X0, X1) then S (from Y0, Y1) of unit j
         auto issue_sp = [&](int j) -> bool {
           for (int h = 0; h < 2; ++h) {
             const int t = 4 * j + h, sl = t % NSLOT;
-            if (!mbar_wait(full + sl, (t / NSLOT) & 1, abort_flag)) return false;
+            if (!mbar_wait_warp(full + sl, (t / NSLOT) & 1, abort_flag)) return false;
             tc_fence_after();
             mma_kk_half(tmem + Cfg::T_P, r1_desc + kmajor_step(128, 8 * h), slot_k(sl), h > 0);
             umma_commit(empty + sl);                  // X_h done
           }
           for (int h = 0; h < 2; ++h) {
             const int t = 4 * j + 2 + h, sl = t % NSLOT;
-            if (!mbar_wait(full + sl, (t / NSLOT) & 1, abort_flag)) return false;
+            if (!mbar_wait_warp(full + sl, (t / NSLOT) & 1, abort_flag)) return false;
             tc_fence_after();
             mma_kk_half(tmem + Cfg::T_S, r0_desc + kmajor_step(128, 8 * h), slot_k(sl), h > 0);
           }
@@ -1200,7 +1201,7 @@ attn_bwd_half_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           ahead.next();
         }
         for (int j = 0; ok && j < j_sp; ++j) {
-          ok = mbar_wait(ds_full, j & 1, abort_flag);
+          ok = mbar_wait_warp(ds_full, j & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           for (int h = 0; h < 2; ++h) {
@@ -1530,14 +1531,15 @@ attn_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_
       if (rank == 0) wait_last_copies(full, NST, n_loads);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (rank 0)
-    if (lane == 0 && rank == 0) {
+    // ------------------------------------------------------------ MMA issuer (rank 0's
+    // whole warp; one elected lane issues)
+    if (rank == 0) {
       KvIter<BN> itr = itr0;
       bool ok = true;
       constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, D, true, true);
       for (int j = 0; !itr.done && ok; ++j, itr.next()) {
         const int st = j % NST;
-        ok = mbar_wait(full + st, (j / NST) & 1, abort_flag);
+        ok = mbar_wait_warp(full + st, (j / NST) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t base = smem_u32(smem + st * Cfg::STAGE);
@@ -1749,7 +1751,8 @@ attn_bwd_dkdv_ds128_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
     }
   } else if (warp <= 3) {
     // ------------------------------------------------------------ MMA issuers
-    if (lane == 0) {
+    // (each a whole warp; one elected lane issues)
+    {
       KvIter<BN> cnt = itr0;
       int n = 0;
       for (; !cnt.done; cnt.next()) ++n;
@@ -1759,14 +1762,14 @@ attn_bwd_dkdv_ds128_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
         if (warp == 1) {
           // S^T(j) = K Q_j^T into buffer j % 2
           const uint64_t k_desc = smem_desc_sw128(smem_u32(smem), 16, 1024);
-          ok = mbar_wait(res_full, 0, abort_flag);
+          ok = mbar_wait_warp(res_full, 0, abort_flag);
           for (int j = 0; ok && j < n; ++j) {
             const int st = j & 1;
             if (j >= 2) {
-              ok = mbar_wait(dv_done + st, ((j - 2) >> 1) & 1, abort_flag);
+              ok = mbar_wait_warp(dv_done + st, ((j - 2) >> 1) & 1, abort_flag);
               if (!ok) break;
             }
-            ok = mbar_wait(qs_full + st, (j >> 1) & 1, abort_flag);
+            ok = mbar_wait_warp(qs_full + st, (j >> 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             mma_kk<BM, BN, D>(tmem + st * BN, k_desc, smem_desc_sw128(qs0 + st * Cfg::QS_BYTES, 16, 1024));
@@ -1778,7 +1781,7 @@ attn_bwd_dkdv_ds128_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
           constexpr uint32_t idesc_dk = idesc_bf16_f32(BM, D, true, true);
           for (int j = 0; ok && j < n; ++j) {
             const int st = j & 1;
-            ok = mbar_wait(qs_full + st, (j >> 1) & 1, abort_flag);
+            ok = mbar_wait_warp(qs_full + st, (j >> 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             const uint32_t base = qs0 + st * Cfg::QS_BYTES;
@@ -1794,9 +1797,9 @@ attn_bwd_dkdv_ds128_kernel(const __grid_constant__ CUtensorMap tm_q, const __gri
           // dV += P_j^T dO_j
           for (int j = 0; ok && j < n; ++j) {
             const int b = j & 1;
-            ok = mbar_wait(p_full + b, (j >> 1) & 1, abort_flag);
+            ok = mbar_wait_warp(p_full + b, (j >> 1) & 1, abort_flag);
             if (!ok) break;
-            ok = mbar_wait(do_full + b, (j >> 1) & 1, abort_flag);
+            ok = mbar_wait_warp(do_full + b, (j >> 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             mma_tn<BN, D>(tmem + Cfg::T_DV, tmem + b * BN, smem_desc_sw128(do0 + b * Cfg::DO_BYTES, BN * 128, 1024),
@@ -2047,7 +2050,8 @@ attn_bwd_dv256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (the whole warp; one elected lane issues)
+    {
       KvIter<BN> ahead;
       ahead.init(p.cp, it.c, si.L, si.S, k_lo, G, g);
       bool ok = true;
@@ -2058,13 +2062,13 @@ attn_bwd_dv256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const uint64_t slot_mn0 = smem_desc_sw128(slot_base, BN * 128, 1024);
         constexpr uint32_t kSlotStep = Cfg::HALF_BYTES >> 4;
         int u = 0;                                // stream position consumed
-        ok = mbar_wait(res_full, 0, abort_flag);
+        ok = mbar_wait_warp(res_full, 0, abort_flag);
         tc_fence_after();
         auto issue_st = [&](int j) -> bool {      // S^T of contribution j -> buffer j % 2
           const uint32_t buf = tmem + (j & 1) * Cfg::T_BUF;
           for (int hf = 0; hf < 2; ++hf, ++u) {
             const int sl = u % NSLOT;
-            if (!mbar_wait(full + sl, (u / NSLOT) & 1, abort_flag)) return false;
+            if (!mbar_wait_warp(full + sl, (u / NSLOT) & 1, abort_flag)) return false;
             tc_fence_after();
             mma_kk_half(buf, k_desc + kmajor_step(128, 8 * hf), slot_k0 + sl * kSlotStep, hf > 0);
             umma_commit(empty + sl);              // Q half done
@@ -2079,12 +2083,12 @@ attn_bwd_dv256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         }
         for (int j = 0; ok && j < j_st; ++j) {
           const int b = j & 1;
-          ok = mbar_wait(p_full + b, (j >> 1) & 1, abort_flag);
+          ok = mbar_wait_warp(p_full + b, (j >> 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           for (int hf = 0; hf < 2 && ok; ++hf, ++u) {
             const int sl = u % NSLOT;
-            ok = mbar_wait(full + sl, (u / NSLOT) & 1, abort_flag);
+            ok = mbar_wait_warp(full + sl, (u / NSLOT) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             mma_tn_split<BN, Cfg::DH, true>(tmem + Cfg::T_ACC + hf * Cfg::DH, tmem + b * Cfg::T_BUF,

@@ -398,8 +398,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // (a pair: rank 0 issues for both CTAs; M = 256, each CTA's TMEM gets its
-    // 128 rows, and every completion is signalled in both CTAs)
-    if (lane == 0 && rank == 0) {
+    // 128 rows, and every completion is signalled in both CTAs).  The whole
+    // warp runs this; one elected lane issues.
+    if (rank == 0) {
       constexpr int MM = PAIR ? 2 * kBM : kBM;
       constexpr uint32_t idesc_s = idesc_bf16_f32(MM, BN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(MM, D, false, true);
@@ -426,7 +427,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       int64_t gs = 0;    // S tiles computed (S buffers, P and O barriers)
       bool ok = true;
       auto wait_pos = [&](int64_t pos) -> bool {
-        const bool r = mbar_wait(kv_full + (pos % NSLOT), static_cast<uint32_t>(pos / NSLOT) & 1, abort_flag);
+        const bool r = mbar_wait_warp(kv_full + (pos % NSLOT), static_cast<uint32_t>(pos / NSLOT) & 1, abort_flag);
         tc_fence_after();
         return r;
       };
@@ -464,7 +465,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int64_t w = w_first; w < n_work && ok; w += w_step, ++item_k) {
         const WorkItem it = p.items[w / nhg];
         const int n = count_tiles<BN>(p, it, item_rows(p, it));
-        ok = mbar_wait(q_full, item_k & 1, abort_flag);
+        ok = mbar_wait_warp(q_full, item_k & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const int a = min(Cfg::LA, n);
@@ -491,13 +492,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const int vsl = static_cast<int>(vpos % NSLOT);
           for (int h = 0; h < NH && ok; ++h) {
             const int buf = static_cast<int>(t % SBUF);
-            ok = mbar_wait(p_full + h * SBUF + buf, static_cast<uint32_t>(t / SBUF) & 1, abort_flag);
+            ok = mbar_wait_warp(p_full + h * SBUF + buf, static_cast<uint32_t>(t / SBUF) & 1, abort_flag);
             if (!ok) break;
             const bool seg_start = p.mode == 1 ? seg_flag[h * SBUF + buf] != 0 : j == 0;
             if (h == 0 && seg_start) ++segs;
             if (seg_start && segs > 1) {
               // the previous segment's O must have been read out before it is overwritten
-              ok = mbar_wait(o_free + h, static_cast<uint32_t>(segs - 2) & 1, abort_flag);
+              ok = mbar_wait_warp(o_free + h, static_cast<uint32_t>(segs - 2) & 1, abort_flag);
               if (!ok) break;
             }
             tc_fence_after();
