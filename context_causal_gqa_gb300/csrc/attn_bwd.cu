@@ -88,7 +88,9 @@ __device__ __forceinline__ int64_t ds_tile_index(const BwdParams& p, int b, int 
 // warpgroups: tile (or contribution) j is formed by warpgroup j % 2 in
 // buffer j % 2 while the tensor core computes the neighbouring tile, since
 // with the final LSE every tile's P is independent of the others.
-constexpr int kThreads = 384;    // warp 0 TMA, 1 MMA, 2 TMEM alloc, 3 idle (dQ pass: 1-3 MMA), 4-11 two softmax warpgroups
+// warp 0 TMA, 1 MMA, 2 TMEM alloc, 3 idle, 4-11 two softmax warpgroups (the
+// D = 128 dQ and dK/dV passes of the dS backward: warps 1-3 issue products)
+constexpr int kThreads = 384;
 
 // dQ pass (D = 128).  TMEM: S of tile j in buffer j % 2 at (j % 2) * BN,
 // with dS packed over each softmax warpgroup's own S columns; dP at 2 BN,
@@ -97,10 +99,9 @@ constexpr int kThreads = 384;    // warp 0 TMA, 1 MMA, 2 TMEM alloc, 3 idle (dQ 
 // dS of tile j, S of tile j+2 once dQ of tile j has read dS(j).  The slots
 // form two rings, NK for K (held from S(j) to dQ(j)) and NV for V (held for
 // dP(j) only), so that each ring's slots are released in the order they are
-// loaded.  The three products are issued by three threads (warps 1, 2, 3):
-// one thread issues a tcgen05 product about every 100 cycles whatever its
-// width, so at N = 128 (64 cycles of tensor work) a single issuer leaves the
-// tensor core a third idle.
+// loaded.  The three products are issued by three warps (1, 2, 3), each
+// waiting only for its own inputs: dP(j+1) does not queue behind the wait
+// for dS(j), nor S(j+2) behind dP(j+1).
 template <int D, int BN_, int NSLOT_>
 struct DqCfg {
   static constexpr int BM = 128;                 // query rows (MMA M)
@@ -1607,11 +1608,10 @@ attn_bwd_dkv_pair_kernel(const __grid_constant__ CUtensorMap tm_b, const __grid_
 // softmax warpgroup of contribution j (j % 2) forms P^T while the tensor
 // core runs dV(j-1), dK(j) and S^T(j+1) (both warpgroups splitting every
 // contribution's columns instead measured 5.4 against 5.2 ms a launch).  The
-// three products are issued by three threads, since one thread issues a
-// tcgen05 product only about every 100 cycles whatever its width (an N = 128
-// product is 64 cycles of tensor work): warp 1 S^T(j) (S^T(j+2) once dV(j)
-// has read P^T(j) from buffer j % 2), warp 2 dK(j) (as soon as its stage has
-// landed), warp 3 dV(j) (once P^T(j) is packed).  A Q/dS stage is released
+// three products are issued by three warps, each waiting only for its own
+// inputs: warp 1 S^T(j) (S^T(j+2) once dV(j) has read P^T(j) from buffer
+// j % 2), warp 2 dK(j) (as soon as its stage has landed), warp 3 dV(j) (once
+// P^T(j) is packed).  A Q/dS stage is released
 // when both its S^T and dK products are done, a dO stage by its dV.  The Q
 // tile is read as the K-major B operand of
 // S^T and as the MN-major B operand of dK; dS^T is read MN-major from the
