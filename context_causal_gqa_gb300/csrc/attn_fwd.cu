@@ -581,7 +581,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int hc = (h0 + h) % p.hpg_q;
             const int slab_c = p.o_slab > 0 ? static_cast<int>(slab) : 0;   // one-slab outputs: slab 0
             const int swz = row & 7;
-#pragma unroll 1
+            // D=128: the row's whole O (128 columns) is loaded first and O
+            // released at once, before the conversions and box writes
+            uint32_t ro[D == 128 ? 4 : 1][32];
+            if constexpr (D == 128) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) tmem_ld32(t_o + c * 32, ro[c]);
+              tmem_wait_ld();
+              tc_fence_before();
+              arrive_mma(o_free + h);                   // O is free for the next segment's first P V
+            }
+#pragma unroll (D == 128 ? 2 : 1)
             for (int qq = 0; qq < D / 64; ++qq) {
               // D=256: two boxes, alternating; D=128: the head's own box
               uint8_t* box = sbox + (NH == 2 ? h : (qq & 1)) * Cfg::BOX_BYTES;
@@ -591,12 +601,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               }
               named_bar_sync(1 + h, 128);
               uint32_t r0[32], r1[32];
-              tmem_ld32(t_o + qq * 64, r0);
-              tmem_ld32(t_o + qq * 64 + 32, r1);
-              tmem_wait_ld();
-              if (qq == D / 64 - 1) {
-                tc_fence_before();
-                arrive_mma(o_free + h);                 // O is free for the next segment's first P V
+              if constexpr (D == 128) {
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                  r0[x] = ro[2 * qq][x];
+                  r1[x] = ro[2 * qq + 1][x];
+                }
+              } else {
+                tmem_ld32(t_o + qq * 64, r0);
+                tmem_ld32(t_o + qq * 64 + 32, r1);
+                tmem_wait_ld();
+                if (qq == D / 64 - 1) {
+                  tc_fence_before();
+                  arrive_mma(o_free + h);               // O is free for the next segment's first P V
+                }
               }
               uint4* brow = reinterpret_cast<uint4*>(box + row * 128);
 #pragma unroll
