@@ -48,7 +48,10 @@ struct SeqCache {
 // blocks an SM (64 registers a thread): rows of early query chunks have few
 // partials, so a thread has few loads in flight there, and the bytes in
 // flight come from more resident threads instead (12.3 -> 10.9 ms on the
-// large step against three blocks).
+// large step against three blocks).  The grid has up to 64 blocks an SM
+// (16 waves): rows of different query chunks carry 1 to CP partials, so
+// short blocks let the waves even out that imbalance (11.0 -> 10.3 ms
+// against 16 blocks an SM).
 template <int TPR, int NP>
 __global__ void __launch_bounds__(256, 4) lse_merge_kernel(MergeArgs a, int64_t rows_per_block) {
   if (a.status != nullptr && status_bad(a.status)) return;
@@ -293,7 +296,7 @@ int grid_for(int64_t units, int per_block, int max_blocks) {
 
 cudaError_t launch_lse_merge(const MergeArgs& a, int num_sms, cudaStream_t stream) {
   const int tpr = a.D / 8;
-  const int grid = grid_for(a.rows, 256 / tpr, num_sms * 16);
+  const int grid = grid_for(a.rows, 256 / tpr, num_sms * 64);
   const int64_t rpb = (a.rows + grid - 1) / grid;
   auto go = [&](auto np) -> cudaError_t {
     constexpr int NP = decltype(np)::value;
