@@ -340,7 +340,9 @@ cudaError_t launch_thd_permute(bool pack, const void* src, void* dst, const int3
                                int64_t T, int H, int D, int cp, int32_t* status, int num_sms,
                                cudaStream_t stream) {
   const int64_t nrows = static_cast<int64_t>(cp) * T;
-  const int grid = grid_for(nrows, 8, num_sms * 16);
+  // up to 64 blocks an SM: shorter row ranges a warp (1.73 -> 1.67 ms a
+  // launch at D=256 against 16 blocks an SM)
+  const int grid = grid_for(nrows, 8, num_sms * 64);
   const int64_t warps = static_cast<int64_t>(grid) * 8;
   const int64_t rpw = (nrows + warps - 1) / warps;
   auto* s = static_cast<const uint4*>(src);
